@@ -1,0 +1,107 @@
+"""Seeded synthetic rollout inputs, shared by the tests, the smoke check and the bench.
+
+This module holds no estimator arithmetic: it only draws random arrays with the
+shapes and distributions of the rl-triton workloads (README "Performance":
+num_envs=4096, seq_len=128; usage example: [64, 512] float tensors) and the
+five workload recipes listed below. Both the float64 oracle and the CUDA path
+receive exactly these arrays.
+
+Every tensor has its own independent stream, spawned in a fixed order from
+``numpy.random.SeedSequence(seed)``, so adding a tensor never changes the
+others. Arrays are numpy (fp32, int32 for ``x_int``), [N, T] row-major and
+time-contiguous; ``bootstrap_value`` is [N].
+"""
+from dataclasses import dataclass, field
+from typing import Dict, Tuple
+
+import numpy as np
+
+# Fixed draw order: one child stream per name.
+_STREAMS = ("rewards", "values", "bootstrap_value", "dones", "next_values",
+            "log_rhos", "q_values", "x", "x_int")
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic workload: sizes, distributions and estimator settings."""
+    name: str
+    N: int
+    T: int
+    estimators: Tuple[str, ...]
+    p_term: float
+    p_trunc: float = 0.0
+    gamma: float = 0.99
+    lambda_: float = 0.95
+    rho_bar: float = 1.0
+    c_bar: float = 1.0
+    log_rho_std: float = 0.5
+    seed: int = 1000
+    extra: Dict[str, float] = field(default_factory=dict)
+
+
+ALL7 = ("gae", "lambda_returns", "discounted_returns", "vtrace", "retrace",
+        "eligibility_traces", "episodic_prefix_sum")
+TRUNC5 = ("gae", "vtrace", "retrace", "lambda_returns", "discounted_returns")
+
+# The five workload recipes. Seeds are 1000 + the recipe's index.
+WORKLOADS = {
+    "gae_64x512": Workload("gae_64x512", 64, 512, ("gae",), p_term=0.01,
+                           seed=1001),
+    "all7_4096x128": Workload("all7_4096x128", 4096, 128, ALL7, p_term=0.01,
+                              seed=1002),
+    "trunc5_4096x128": Workload("trunc5_4096x128", 4096, 128, TRUNC5,
+                                p_term=0.01, p_trunc=0.005, seed=1003),
+    "longT_256x1024": Workload("longT_256x1024", 256, 1024, ALL7,
+                               p_term=0.001, gamma=0.997, seed=1004),
+    "longT_256x4096": Workload("longT_256x4096", 256, 4096, ALL7,
+                               p_term=0.001, gamma=0.997, seed=1004),
+    "longT_256x16384": Workload("longT_256x16384", 256, 16384, ALL7,
+                                p_term=0.001, gamma=0.997, seed=1004),
+    "vlong_8x131072": Workload("vlong_8x131072", 8, 131072,
+                               ("vtrace", "retrace"), p_term=1e-4,
+                               gamma=0.999, lambda_=1.0, seed=1005),
+}
+
+
+def rollout(N: int, T: int, seed: int, p_term: float, p_trunc: float = 0.0,
+            log_rho_std: float = 0.5, int_range: int = 100) -> Dict[str, np.ndarray]:
+    """Draw one rollout batch.
+
+    rewards, values, q_values, x, next_values, bootstrap_value ~ N(0, 1);
+    log_rhos ~ N(0, log_rho_std^2); x_int ~ U{-int_range..int_range} int32.
+    Done masks come from one uniform u per step: u < p_term marks a terminated
+    step, p_term <= u < p_term + p_trunc a truncated one, so the two masks are
+    disjoint with the exact rates. Masks are 0/1 float32. ``truncateds`` and
+    ``next_values`` are present only when p_trunc > 0.
+    """
+    children = np.random.SeedSequence(seed).spawn(len(_STREAMS))
+    g = {name: np.random.Generator(np.random.PCG64(c))
+         for name, c in zip(_STREAMS, children)}
+    shape = (N, T)
+    f32 = np.float32
+    out = {
+        "rewards": g["rewards"].standard_normal(shape, dtype=f32),
+        "values": g["values"].standard_normal(shape, dtype=f32),
+        "bootstrap_value": g["bootstrap_value"].standard_normal((N,), dtype=f32),
+    }
+    u = g["dones"].random(shape, dtype=np.float64)
+    out["terminateds"] = (u < p_term).astype(f32)
+    if p_trunc > 0.0:
+        out["truncateds"] = ((u >= p_term) & (u < p_term + p_trunc)).astype(f32)
+        out["next_values"] = g["next_values"].standard_normal(shape, dtype=f32)
+    out["log_rhos"] = (g["log_rhos"].standard_normal(shape, dtype=f32)
+                       * f32(log_rho_std))
+    out["q_values"] = g["q_values"].standard_normal(shape, dtype=f32)
+    out["x"] = g["x"].standard_normal(shape, dtype=f32)
+    out["x_int"] = g["x_int"].integers(-int_range, int_range + 1, size=shape,
+                                       dtype=np.int32)
+    return out
+
+
+def workload_inputs(w: Workload, N: int = None, T: int = None,
+                    seed: int = None) -> Dict[str, np.ndarray]:
+    """Inputs for a named workload; N, T or seed may be overridden (parity
+    tests use a few rows of a full-size recipe)."""
+    return rollout(w.N if N is None else N, w.T if T is None else T,
+                   w.seed if seed is None else seed, w.p_term, w.p_trunc,
+                   w.log_rho_std)
