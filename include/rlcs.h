@@ -1,0 +1,219 @@
+/*
+ * rlcs.h — C ABI of the GB300 affine-scan library for RL credit assignment.
+ *
+ * Seven estimators, each one batched first-order linear recurrence over
+ * [N, T] rollouts (N environments, T steps), solved on the GPU as an
+ * associative scan over affine pairs:
+ *
+ *   backward estimators:  A_t = alpha_t + beta_t * A_{t+1}
+ *   forward estimators:   e_t = alpha_t + beta_t * e_{t-1}
+ *   pair operator:        (alpha_B, beta_B) (+) (alpha_A, beta_A)
+ *                         = (alpha_B + beta_B*alpha_A, beta_A*beta_B)
+ *
+ * (rl-triton technical summary, Methodology 1 "Unified Algebraic Framework".)
+ * Each entry point builds its own (alpha_t, beta_t) in registers from the raw
+ * inputs and writes only the final outputs (same page, Methodology 2).
+ *
+ * ---------------------------------------------------------------------------
+ * Conventions common to every entry point
+ * ---------------------------------------------------------------------------
+ * Memory.    Every array pointer is DEVICE memory owned by the caller. The
+ *            library allocates nothing and frees nothing.
+ * Layout.    Per-step arrays are [N, T], row-major, time-contiguous
+ *            (element (n, t) at offset n*T + t). float32, except the prefix
+ *            sum's int32 input and output. bootstrap_value is [N].
+ *            Rows whose start is 16-byte aligned (T % 4 == 0 and 16-byte
+ *            aligned base pointers) take the vectorised / bulk-copy path;
+ *            anything else takes a scalar path with the same results.
+ * Masks.     terminateds / truncateds / dones are 0/1 float32; an entry
+ *            counts as set when it is nonzero.
+ * Boundary.  (Methodology 3 "Explicit Boundary Semantics".) The successor
+ *            value of step t is: 0 if terminateds[t] is set; otherwise
+ *            next_values[t] if truncateds[t] is set; otherwise
+ *            bootstrap_value[n] when t = T-1; otherwise values[t+1].
+ *            Termination wins when both masks are set. A step with any of
+ *            these three conditions is a cut: nothing is carried across it.
+ *            truncateds and next_values must be both NULL (no truncation)
+ *            or both non-NULL. bootstrap_value may be NULL (taken as 0).
+ * Aliasing.  Outputs must not overlap any input or each other; identical
+ *            input/output pointers are rejected with RLCS_ERR_INVALID_ARG.
+ * Streams.   Every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ *            the legacy default stream) and never synchronises the host,
+ *            except rlcs_check_status. Calls can be captured in CUDA graphs.
+ * Workspace. Long rows are split across thread blocks that pass carries
+ *            through `workspace`. Size it with rlcs_workspace_bytes(N, T)
+ *            and zero it once (rlcs_workspace_init, or any memset to 0)
+ *            before its first use; afterwards every call leaves it ready for
+ *            the next one. One workspace must not be used by two calls that
+ *            can run at the same time (give each stream its own). It may be
+ *            NULL with workspace_bytes = 0 only when the call needs none;
+ *            otherwise the call returns RLCS_ERR_WORKSPACE and launches
+ *            nothing.
+ * Errors.    Argument errors (N <= 0, T <= 0, NULL required pointer, half a
+ *            truncation pair, aliasing, workspace too small) return before
+ *            anything is launched. A launch failure returns RLCS_ERR_CUDA.
+ *            Device-side conditions (a bounded wait that ran out) are
+ *            recorded in the workspace and reported by rlcs_check_status.
+ * Device.    The library is built for sm_103a (GB300) only.
+ */
+#ifndef RLCS_H_
+#define RLCS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so the header needs no CUDA. */
+typedef struct CUstream_st *rlcs_stream_t;
+
+typedef enum {
+  RLCS_OK = 0,
+  RLCS_ERR_INVALID_ARG = 1, /* bad size, NULL pointer, aliasing, half pair */
+  RLCS_ERR_MISALIGNED = 2,  /* reserved: misalignment selects a scalar path */
+  RLCS_ERR_WORKSPACE = 3,   /* workspace missing, too small or corrupted    */
+  RLCS_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed         */
+  RLCS_ERR_TIMEOUT = 5      /* a device-side bounded wait ran out           */
+} rlcs_status;
+
+/* Bytes of workspace any entry point needs for an [N, T] call: a small
+ * header plus 16 bytes per possible row chunk. Depends only on N and T.
+ * Returns 0 if N <= 0 or T <= 0. */
+size_t rlcs_workspace_bytes(int64_t N, int64_t T);
+
+/* Zero `bytes` of `workspace` on `stream` (asynchronous). */
+rlcs_status rlcs_workspace_init(void *workspace, size_t bytes,
+                                rlcs_stream_t stream);
+
+/* Synchronise `stream`, then read and clear the device-side status that
+ * calls using `workspace` recorded (RLCS_ERR_TIMEOUT when a bounded wait ran
+ * out, RLCS_ERR_WORKSPACE when the workspace was not initialised). Returns
+ * RLCS_ERR_CUDA if the stream reported an error. workspace may be NULL, in
+ * which case only the stream is checked. */
+rlcs_status rlcs_check_status(void *workspace, rlcs_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *rlcs_status_string(rlcs_status status);
+
+/* Generalized Advantage Estimation.
+ * rl-triton README, Kernels table, compute_gae ("backward scan over
+ * delta + gamma*lambda*A"); boundary rules of Methodology 3.
+ *   delta_t = r_t + gamma*S_t - V_t          (S_t: successor value above)
+ *   A_t     = delta_t + gamma*lambda*A_{t+1} (nothing carried across a cut)
+ * Inputs rewards, values, terminateds [N,T]; optional truncateds and
+ * next_values [N,T]; optional bootstrap_value [N]. Output advantages [N,T]. */
+rlcs_status rlcs_gae(const float *rewards, const float *values,
+                     const float *terminateds, const float *truncateds,
+                     const float *next_values, const float *bootstrap_value,
+                     float *advantages, int64_t N, int64_t T, float gamma,
+                     float lambda, void *workspace, size_t workspace_bytes,
+                     rlcs_stream_t stream);
+
+/* TD(lambda) returns.
+ * README Kernels table, compute_lambda_returns ("lambda-return targets
+ * mixing one-step TD and Monte Carlo"):
+ *   G_t = r_t + gamma*((1-lambda)*V_{t+1} + lambda*G_{t+1})
+ *   G_t = r_t + gamma*S_t                                   at a cut
+ * Same inputs as rlcs_gae; output returns [N,T] (equals GAE + values). */
+rlcs_status rlcs_lambda_returns(const float *rewards, const float *values,
+                                const float *terminateds,
+                                const float *truncateds,
+                                const float *next_values,
+                                const float *bootstrap_value, float *returns,
+                                int64_t N, int64_t T, float gamma,
+                                float lambda, void *workspace,
+                                size_t workspace_bytes, rlcs_stream_t stream);
+
+/* Discounted reward-to-go.
+ * README Kernels table, compute_discounted_returns:
+ *   G_t = r_t + gamma*G_{t+1};   G_t = r_t + gamma*S_t at a cut.
+ * Takes no values array: the successor value at a cut is 0 (terminated),
+ * next_values[t] (truncated) or bootstrap_value[n] (t = T-1). */
+rlcs_status rlcs_discounted_returns(const float *rewards,
+                                    const float *terminateds,
+                                    const float *truncateds,
+                                    const float *next_values,
+                                    const float *bootstrap_value,
+                                    float *returns, int64_t N, int64_t T,
+                                    float gamma, void *workspace,
+                                    size_t workspace_bytes,
+                                    rlcs_stream_t stream);
+
+/* V-trace targets and policy-gradient advantages.
+ * README Kernels table, compute_vtrace ("IS-weighted targets and
+ * advantages"); definition of IMPALA V-trace with lambda in the trace:
+ *   ratio_t = exp(log_rhos_t), rho_t = min(rho_bar, ratio_t),
+ *   c_t = lambda*min(c_bar, ratio_t)
+ *   vs_t - V_t = rho_t*(r_t + gamma*S_t - V_t) + gamma*c_t*(vs_{t+1} - V_{t+1})
+ *   pg_t = rho_t*(r_t + gamma*W_t - V_t),  W_t = S_t at a cut, else vs_{t+1}
+ * log_rhos = log pi(a_t|s_t) - log mu(a_t|s_t), [N,T]. Outputs vs [N,T] and
+ * pg_advantages [N,T] (may be NULL to skip it). */
+rlcs_status rlcs_vtrace(const float *rewards, const float *values,
+                        const float *log_rhos, const float *terminateds,
+                        const float *truncateds, const float *next_values,
+                        const float *bootstrap_value, float *vs,
+                        float *pg_advantages, int64_t N, int64_t T,
+                        float gamma, float lambda, float rho_bar, float c_bar,
+                        void *workspace, size_t workspace_bytes,
+                        rlcs_stream_t stream);
+
+/* Retrace(lambda) targets.
+ * README Kernels table, compute_retrace ("off-policy return estimate with
+ * truncated IS ratios"); definition of Munos et al. (2016):
+ *   c_t = lambda*min(c_bar, exp(log_rhos_t))
+ *   Q_t = r_t + gamma*(values_{t+1} + c_{t+1}*(Q_{t+1} - q_values_{t+1}))
+ *   Q_t = r_t + gamma*S_t                                     at a cut
+ * values = E_pi Q(s_t, .), q_values = Q(s_t, a_t), log_rhos of a_t; all
+ * [N,T]. Output q_ret [N,T]. Note the trace at t+1 weighs the carry into t. */
+rlcs_status rlcs_retrace(const float *rewards, const float *values,
+                         const float *q_values, const float *log_rhos,
+                         const float *terminateds, const float *truncateds,
+                         const float *next_values,
+                         const float *bootstrap_value, float *q_ret,
+                         int64_t N, int64_t T, float gamma, float lambda,
+                         float c_bar, void *workspace, size_t workspace_bytes,
+                         rlcs_stream_t stream);
+
+/* Accumulating eligibility traces, forward in time.
+ * README Kernels table, compute_eligibility_traces:
+ *   e_t = x_t + gamma*lambda*(1 - d_{t-1})*e_{t-1},   e_{-1} = 0.
+ * Inputs x, dones [N,T]; output traces [N,T]. To cut at truncations too, OR
+ * them into dones. */
+rlcs_status rlcs_eligibility_traces(const float *x, const float *dones,
+                                    float *traces, int64_t N, int64_t T,
+                                    float gamma, float lambda,
+                                    void *workspace, size_t workspace_bytes,
+                                    rlcs_stream_t stream);
+
+/* Episodic prefix sum, forward in time, int32.
+ * README Kernels table, compute_episodic_prefix_sum ("episodic cumulative
+ * sum with done-mask resets"); reset index as for the traces:
+ *   s_t = x_t + (1 - d_{t-1})*s_{t-1},   s_{-1} = 0,   modulo 2^32.
+ * Bit-exact. Inputs x (int32) and dones (float) [N,T]; output out (int32). */
+rlcs_status rlcs_episodic_prefix_sum(const int32_t *x, const float *dones,
+                                     int32_t *out, int64_t N, int64_t T,
+                                     void *workspace, size_t workspace_bytes,
+                                     rlcs_stream_t stream);
+
+/* Launch-shape selection, exposed for testing and tuning. The library picks
+ * one of three shapes from (N, T): RLCS_SHAPE_WARP_ROW (one warp per row,
+ * T <= 512), RLCS_SHAPE_BLOCK_CHUNK (a thread block per row chunk, carries
+ * between chunks by decoupled look-back through the workspace). Setting an
+ * override forces a shape and a chunk length (a multiple of 512 up to 4096)
+ * for every later call in this process until reset with RLCS_SHAPE_AUTO.
+ * Not thread-safe with concurrent calls. Returns RLCS_ERR_INVALID_ARG for an
+ * unknown shape or chunk length. */
+typedef enum {
+  RLCS_SHAPE_AUTO = 0,
+  RLCS_SHAPE_WARP_ROW = 1,
+  RLCS_SHAPE_BLOCK_CHUNK = 2
+} rlcs_shape;
+rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RLCS_H_ */

@@ -1,0 +1,262 @@
+"""Thin ctypes binding over ``librlcs.so`` (the C ABI in include/rlcs.h).
+
+Argument marshalling only: every step of every estimator runs in the CUDA
+library. PyTorch supplies device memory (inputs, outputs, workspace) and the
+current CUDA stream. The functions carry the C ABI's names and raise
+``RlcsError`` on any non-OK status. There is no CPU fallback: if the library
+is missing, importing this module raises.
+"""
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librlcs.so")
+
+RLCS_OK = 0
+RLCS_SHAPE_AUTO, RLCS_SHAPE_WARP_ROW, RLCS_SHAPE_BLOCK_CHUNK = 0, 1, 2
+
+
+class RlcsError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        msg = _lib.rlcs_status_string(status).decode()
+        super().__init__("%s: %s (status %d)" % (where, msg, status))
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            "librlcs.so is not built (%s); run linear_recurrence_scan_affine_gb300.build.build()"
+            % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, F, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    sig = {
+        "rlcs_workspace_bytes": ([I64, I64], SZ),
+        "rlcs_workspace_init": ([P, SZ, P], ctypes.c_int),
+        "rlcs_check_status": ([P, P], ctypes.c_int),
+        "rlcs_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "rlcs_set_shape_override": ([ctypes.c_int, I64], ctypes.c_int),
+        "rlcs_gae": ([P] * 7 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_lambda_returns": ([P] * 7 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_discounted_returns": ([P] * 6 + [I64, I64, F, P, SZ, P], ctypes.c_int),
+        "rlcs_vtrace": ([P] * 9 + [I64, I64, F, F, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_retrace": ([P] * 9 + [I64, I64, F, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_eligibility_traces": ([P] * 3 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_episodic_prefix_sum": ([P] * 3 + [I64, I64, P, SZ, P], ctypes.c_int),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    return lib
+
+
+_lib = _load()
+EXPORTED = ("rlcs_workspace_bytes", "rlcs_workspace_init", "rlcs_check_status",
+            "rlcs_status_string", "rlcs_set_shape_override", "rlcs_gae",
+            "rlcs_lambda_returns", "rlcs_discounted_returns", "rlcs_vtrace",
+            "rlcs_retrace", "rlcs_eligibility_traces", "rlcs_episodic_prefix_sum")
+
+
+def lib():
+    """The loaded ctypes library (for tests that call the C ABI directly)."""
+    return _lib
+
+
+def _check(status, where):
+    if status != RLCS_OK:
+        raise RlcsError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+# One zeroed workspace per (device, stream), grown on demand. A workspace is
+# reused only by calls on its own stream, which the stream orders.
+_ws_lock = threading.Lock()
+_ws_cache = {}
+
+
+def workspace_for(N, T, device, stream=None):
+    need = _lib.rlcs_workspace_bytes(N, T)
+    if need == 0:
+        return None, 0
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    key = (device.index if device.index is not None else torch.cuda.current_device(),
+           s.cuda_stream)
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < need:
+            ws = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=device)
+            _ws_cache[key] = ws
+    return ws, ws.numel()
+
+
+def _rows(t, name, dtype=torch.float32):
+    if t.dim() == 1:
+        t = t.unsqueeze(0)
+    if t.dim() != 2:
+        raise ValueError("%s must be [N, T] (or [T])" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t.contiguous()
+
+
+def _opt(t, name, N, T):
+    if t is None:
+        return None
+    t = _rows(t, name)
+    if t.shape != (N, T):
+        raise ValueError("%s must have shape (%d, %d)" % (name, N, T))
+    return t
+
+
+def _boot(b, N):
+    if b is None:
+        return None
+    b = b.reshape(-1)
+    if not b.is_cuda or b.dtype != torch.float32 or b.numel() != N:
+        raise ValueError("bootstrap_value must be a float32 CUDA tensor of %d values" % N)
+    return b.contiguous()
+
+
+def _prep(main, others, rewards_name="rewards"):
+    r = _rows(main, rewards_name)
+    N, T = r.shape
+    outs = [r]
+    for t, name in others:
+        x = _rows(t, name)
+        if x.shape != (N, T):
+            raise ValueError("%s must have shape (%d, %d)" % (name, N, T))
+        outs.append(x)
+    return N, T, outs
+
+
+def _finish(out, like):
+    return out.reshape(like.shape)
+
+
+def rlcs_gae(rewards, values, terminateds, gamma=0.99, lambda_=0.95, bootstrap_value=None,
+             truncateds=None, next_values=None, out=None, stream=None):
+    N, T, (r, v, d) = _prep(rewards, [(values, "values"), (terminateds, "terminateds")])
+    tr, nv = _opt(truncateds, "truncateds", N, T), _opt(next_values, "next_values", N, T)
+    b = _boot(bootstrap_value, N)
+    o = torch.empty_like(r) if out is None else out
+    ws, wsb = workspace_for(N, T, r.device, stream)
+    _check(_lib.rlcs_gae(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b), _ptr(o),
+                         N, T, gamma, lambda_, _ptr(ws), wsb, _stream(stream)), "rlcs_gae")
+    return _finish(o, rewards)
+
+
+def rlcs_lambda_returns(rewards, values, terminateds, gamma=0.99, lambda_=0.95,
+                        bootstrap_value=None, truncateds=None, next_values=None, out=None,
+                        stream=None):
+    N, T, (r, v, d) = _prep(rewards, [(values, "values"), (terminateds, "terminateds")])
+    tr, nv = _opt(truncateds, "truncateds", N, T), _opt(next_values, "next_values", N, T)
+    b = _boot(bootstrap_value, N)
+    o = torch.empty_like(r) if out is None else out
+    ws, wsb = workspace_for(N, T, r.device, stream)
+    _check(_lib.rlcs_lambda_returns(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
+                                    _ptr(o), N, T, gamma, lambda_, _ptr(ws), wsb,
+                                    _stream(stream)), "rlcs_lambda_returns")
+    return _finish(o, rewards)
+
+
+def rlcs_discounted_returns(rewards, terminateds, gamma=0.99, bootstrap_value=None,
+                            truncateds=None, next_values=None, out=None, stream=None):
+    N, T, (r, d) = _prep(rewards, [(terminateds, "terminateds")])
+    tr, nv = _opt(truncateds, "truncateds", N, T), _opt(next_values, "next_values", N, T)
+    b = _boot(bootstrap_value, N)
+    o = torch.empty_like(r) if out is None else out
+    ws, wsb = workspace_for(N, T, r.device, stream)
+    _check(_lib.rlcs_discounted_returns(_ptr(r), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b), _ptr(o),
+                                        N, T, gamma, _ptr(ws), wsb, _stream(stream)),
+           "rlcs_discounted_returns")
+    return _finish(o, rewards)
+
+
+def rlcs_vtrace(rewards, values, log_rhos, terminateds, gamma=0.99, lambda_=1.0, rho_bar=1.0,
+                c_bar=1.0, bootstrap_value=None, truncateds=None, next_values=None,
+                with_pg=True, out=None, out_pg=None, stream=None):
+    """Returns (vs, pg_advantages); pg_advantages is None when with_pg=False."""
+    N, T, (r, v, lr, d) = _prep(rewards, [(values, "values"), (log_rhos, "log_rhos"),
+                                          (terminateds, "terminateds")])
+    tr, nv = _opt(truncateds, "truncateds", N, T), _opt(next_values, "next_values", N, T)
+    b = _boot(bootstrap_value, N)
+    vs = torch.empty_like(r) if out is None else out
+    pg = (torch.empty_like(r) if out_pg is None else out_pg) if with_pg else None
+    ws, wsb = workspace_for(N, T, r.device, stream)
+    _check(_lib.rlcs_vtrace(_ptr(r), _ptr(v), _ptr(lr), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
+                            _ptr(vs), _ptr(pg), N, T, gamma, lambda_, rho_bar, c_bar,
+                            _ptr(ws), wsb, _stream(stream)), "rlcs_vtrace")
+    return _finish(vs, rewards), (None if pg is None else _finish(pg, rewards))
+
+
+def rlcs_retrace(rewards, values, q_values, log_rhos, terminateds, gamma=0.99, lambda_=1.0,
+                 c_bar=1.0, bootstrap_value=None, truncateds=None, next_values=None, out=None,
+                 stream=None):
+    N, T, (r, v, q, lr, d) = _prep(rewards, [(values, "values"), (q_values, "q_values"),
+                                             (log_rhos, "log_rhos"),
+                                             (terminateds, "terminateds")])
+    tr, nv = _opt(truncateds, "truncateds", N, T), _opt(next_values, "next_values", N, T)
+    b = _boot(bootstrap_value, N)
+    o = torch.empty_like(r) if out is None else out
+    ws, wsb = workspace_for(N, T, r.device, stream)
+    _check(_lib.rlcs_retrace(_ptr(r), _ptr(v), _ptr(q), _ptr(lr), _ptr(d), _ptr(tr), _ptr(nv),
+                             _ptr(b), _ptr(o), N, T, gamma, lambda_, c_bar, _ptr(ws), wsb,
+                             _stream(stream)), "rlcs_retrace")
+    return _finish(o, rewards)
+
+
+def rlcs_eligibility_traces(x, dones, gamma=0.99, lambda_=0.95, out=None, stream=None):
+    N, T, (xx, d) = _prep(x, [(dones, "dones")], rewards_name="x")
+    o = torch.empty_like(xx) if out is None else out
+    ws, wsb = workspace_for(N, T, xx.device, stream)
+    _check(_lib.rlcs_eligibility_traces(_ptr(xx), _ptr(d), _ptr(o), N, T, gamma, lambda_,
+                                        _ptr(ws), wsb, _stream(stream)),
+           "rlcs_eligibility_traces")
+    return _finish(o, x)
+
+
+def rlcs_episodic_prefix_sum(x, dones, out=None, stream=None):
+    xx = _rows(x, "x", dtype=torch.int32)
+    N, T = xx.shape
+    d = _rows(dones, "dones")
+    if d.shape != (N, T):
+        raise ValueError("dones must have shape (%d, %d)" % (N, T))
+    o = torch.empty_like(xx) if out is None else out
+    ws, wsb = workspace_for(N, T, xx.device, stream)
+    _check(_lib.rlcs_episodic_prefix_sum(_ptr(xx), _ptr(d), _ptr(o), N, T, _ptr(ws), wsb,
+                                         _stream(stream)), "rlcs_episodic_prefix_sum")
+    return _finish(o, x)
+
+
+def rlcs_check_status(workspace=None, stream=None):
+    _check(_lib.rlcs_check_status(_ptr(workspace), _stream(stream)), "rlcs_check_status")
+
+
+def rlcs_set_shape_override(shape=RLCS_SHAPE_AUTO, chunk=0):
+    _check(_lib.rlcs_set_shape_override(shape, chunk), "rlcs_set_shape_override")
+
+
+def rlcs_workspace_bytes(N, T):
+    return _lib.rlcs_workspace_bytes(N, T)
+
+
+def check_all_workspaces():
+    """Synchronise and check the status word of every cached workspace."""
+    with _ws_lock:
+        items = list(_ws_cache.values())
+    for ws in items:
+        _check(_lib.rlcs_check_status(_ptr(ws), None), "rlcs_check_status")

@@ -1,0 +1,227 @@
+// Per-estimator coefficient functors: each turns the raw inputs of one step
+// into its affine pair (beta_t, alpha_t) in registers, and turns the scanned
+// value back into the estimator's output(s). Nothing here touches memory.
+//
+// Boundary rules (rl-triton technical summary, Methodology 3): the successor
+// value S_t of step t is 0 if the step terminated, next_values[t] if it was
+// truncated, bootstrap[n] at the window end t = T-1, else values[t+1]; such a
+// step is a cut and carries nothing across (beta_t = 0). Termination wins.
+#pragma once
+
+#include "scan_core.cuh"
+
+namespace rlcs {
+
+// Input slots. Backward estimators use R, V, Q, LR, D (+ TAU, NV with
+// truncation); forward ones put x in R and the done mask in D.
+enum Slot : int { kR = 0, kV = 1, kQ = 2, kLR = 3, kD = 4, kTau = 5, kNV = 6, kNumSlots = 7 };
+
+constexpr uint32_t bit(int s) { return 1u << s; }
+
+struct Params {
+  const float *in[kNumSlots];  // device pointers, [N, T]; unused slots NULL
+  const float *boot;           // [N] or NULL
+  void *out0;                  // [N, T] float (int32 for the prefix sum)
+  float *out1;                 // [N, T] second output (V-trace pg) or NULL
+  int64_t N, T;
+  float gamma, lambda, rho_bar, c_bar;
+  int vec;                     // 1: rows 16-byte aligned (T % 4 == 0, aligned bases)
+};
+
+// What a functor sees for step t. Fields an estimator does not use are never
+// loaded (their slots are absent from its masks) and fold away.
+struct StepIn {
+  float r, v, q, lr, d, tau, nv;  // at t
+  float vn, qn, lrn;              // at t+1 (backward, only where needed)
+  float dp;                       // done mask at t-1 (forward)
+  bool last;                      // t == T-1
+  bool first;                     // t == 0
+};
+
+template <bool TRUNC>
+__device__ __forceinline__ float successor(const StepIn &s, float boot, bool &cut) {
+  const bool term = s.d != 0.0f;
+  const bool trunc = TRUNC && s.tau != 0.0f;
+  cut = term || trunc || s.last;
+  return term ? 0.0f : (trunc ? s.nv : (s.last ? boot : s.vn));
+}
+
+constexpr uint32_t kTruncSlots = bit(kTau) | bit(kNV);
+
+// ---------------------------------------------------------------------------
+// GAE: alpha = r + gamma*S - V, beta = gamma*lambda (0 at a cut). Out: A.
+// ---------------------------------------------------------------------------
+struct Gae {
+  static constexpr bool kBackward = true;
+  static constexpr uint32_t kSlots = bit(kR) | bit(kV) | bit(kD);
+  static constexpr uint32_t kNext = bit(kV);
+  static constexpr int kOuts = 1;
+  using Pair = FPair;
+  template <bool TRUNC>
+  __device__ static __forceinline__ void coeff(const Params &p, const StepIn &s, float boot,
+                                               Pair &e, float &, float &) {
+    bool cut;
+    const float S = successor<TRUNC>(s, boot, cut);
+    e.c = fmaf(p.gamma, S, s.r) - s.v;
+    e.m = cut ? 0.0f : p.gamma * p.lambda;
+  }
+  __device__ static __forceinline__ float out0(float A, float, const Pair &, float, float) {
+    return A;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// TD(lambda) returns: alpha = r + gamma*(1-lambda)*V_{t+1}, beta = gamma*lambda;
+// at a cut alpha = r + gamma*S, beta = 0. Out: G.
+// ---------------------------------------------------------------------------
+struct LambdaReturns {
+  static constexpr bool kBackward = true;
+  static constexpr uint32_t kSlots = bit(kR) | bit(kV) | bit(kD);
+  static constexpr uint32_t kNext = bit(kV);
+  static constexpr int kOuts = 1;
+  using Pair = FPair;
+  template <bool TRUNC>
+  __device__ static __forceinline__ void coeff(const Params &p, const StepIn &s, float boot,
+                                               Pair &e, float &, float &) {
+    bool cut;
+    const float S = successor<TRUNC>(s, boot, cut);
+    const float w = cut ? p.gamma : p.gamma * (1.0f - p.lambda);
+    e.c = fmaf(w, S, s.r);  // S == V_{t+1} when not a cut
+    e.m = cut ? 0.0f : p.gamma * p.lambda;
+  }
+  __device__ static __forceinline__ float out0(float A, float, const Pair &, float, float) {
+    return A;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Discounted returns: alpha = r (+ gamma*S at a cut), beta = gamma (0 at a cut).
+// ---------------------------------------------------------------------------
+struct DiscountedReturns {
+  static constexpr bool kBackward = true;
+  static constexpr uint32_t kSlots = bit(kR) | bit(kD);
+  static constexpr uint32_t kNext = 0;
+  static constexpr int kOuts = 1;
+  using Pair = FPair;
+  template <bool TRUNC>
+  __device__ static __forceinline__ void coeff(const Params &p, const StepIn &s, float boot,
+                                               Pair &e, float &, float &) {
+    const bool term = s.d != 0.0f;
+    const bool trunc = TRUNC && s.tau != 0.0f;
+    const bool cut = term || trunc || s.last;
+    const float S = term ? 0.0f : (trunc ? s.nv : boot);  // only used at a cut
+    e.c = cut ? fmaf(p.gamma, S, s.r) : s.r;
+    e.m = cut ? 0.0f : p.gamma;
+  }
+  __device__ static __forceinline__ float out0(float A, float, const Pair &, float, float) {
+    return A;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// V-trace (IMPALA, lambda in the trace weight):
+//   rho = min(rho_bar, e^lr), c = lambda*min(c_bar, e^lr)
+//   alpha = rho*(r + gamma*S - V), beta = gamma*c (0 at a cut), A = vs - V.
+// Outputs vs = V + A and pg = alpha + [not cut]*gamma*rho*A_{t+1}, which is
+// rho*(r + gamma*W - V) with W = vs_{t+1} (or S at a cut).
+// aux0 = gamma*rho (0 at a cut), aux1 = V.
+// ---------------------------------------------------------------------------
+struct VTrace {
+  static constexpr bool kBackward = true;
+  static constexpr uint32_t kSlots = bit(kR) | bit(kV) | bit(kLR) | bit(kD);
+  static constexpr uint32_t kNext = bit(kV);
+  static constexpr int kOuts = 2;
+  using Pair = FPair;
+  template <bool TRUNC>
+  __device__ static __forceinline__ void coeff(const Params &p, const StepIn &s, float boot,
+                                               Pair &e, float &aux0, float &aux1) {
+    bool cut;
+    const float S = successor<TRUNC>(s, boot, cut);
+    const float ratio = expf(s.lr);
+    const float rho = fminf(p.rho_bar, ratio);
+    const float c = p.lambda * fminf(p.c_bar, ratio);
+    e.c = rho * (fmaf(p.gamma, S, s.r) - s.v);
+    e.m = cut ? 0.0f : p.gamma * c;
+    aux0 = cut ? 0.0f : p.gamma * rho;
+    aux1 = s.v;
+  }
+  __device__ static __forceinline__ float out0(float A, float, const Pair &, float, float v) {
+    return v + A;
+  }
+  __device__ static __forceinline__ float out1(float, float A_next, const Pair &e, float g_rho,
+                                               float) {
+    return fmaf(g_rho, A_next, e.c);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Retrace(lambda) (Munos et al.), values = E_pi Q(s_t,.), q = Q(s_t, a_t):
+//   c_{t+1} = lambda*min(c_bar, e^{lr_{t+1}})
+//   alpha = r + gamma*(V_{t+1} - c_{t+1}*Q_{t+1}), beta = gamma*c_{t+1};
+//   at a cut alpha = r + gamma*S, beta = 0. Out: Q^ret.
+// ---------------------------------------------------------------------------
+struct Retrace {
+  static constexpr bool kBackward = true;
+  static constexpr uint32_t kSlots = bit(kR) | bit(kV) | bit(kQ) | bit(kLR) | bit(kD);
+  static constexpr uint32_t kNext = bit(kV) | bit(kQ) | bit(kLR);
+  static constexpr int kOuts = 1;
+  using Pair = FPair;
+  template <bool TRUNC>
+  __device__ static __forceinline__ void coeff(const Params &p, const StepIn &s, float boot,
+                                               Pair &e, float &, float &) {
+    bool cut;
+    const float S = successor<TRUNC>(s, boot, cut);
+    if (cut) {
+      e.c = fmaf(p.gamma, S, s.r);
+      e.m = 0.0f;
+    } else {
+      const float c_next = p.lambda * fminf(p.c_bar, expf(s.lrn));
+      e.c = fmaf(p.gamma, fmaf(-c_next, s.qn, s.vn), s.r);
+      e.m = p.gamma * c_next;
+    }
+  }
+  __device__ static __forceinline__ float out0(float A, float, const Pair &, float, float) {
+    return A;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Eligibility traces (forward): alpha = x, beta = gamma*lambda*(1 - d_{t-1}),
+// beta_0 = 0 (e_{-1} = 0). Out: e.
+// ---------------------------------------------------------------------------
+struct EligibilityTraces {
+  static constexpr bool kBackward = false;
+  static constexpr uint32_t kSlots = bit(kR) | bit(kD);
+  static constexpr uint32_t kNext = 0;
+  static constexpr int kOuts = 1;
+  using Pair = FPair;
+  template <bool TRUNC>
+  __device__ static __forceinline__ void coeff(const Params &p, const StepIn &s, float,
+                                               Pair &e, float &, float &) {
+    e.c = s.r;
+    e.m = (s.first || s.dp != 0.0f) ? 0.0f : p.gamma * p.lambda;
+  }
+  __device__ static __forceinline__ float out0(float A, float, const Pair &, float, float) {
+    return A;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Episodic prefix sum (forward, int32 modulo 2^32): alpha = x, carry flag
+// m = (1 - d_{t-1}), m_0 = 0. The int32 input travels in slot R as raw bits.
+// ---------------------------------------------------------------------------
+struct EpisodicPrefixSum {
+  static constexpr bool kBackward = false;
+  static constexpr uint32_t kSlots = bit(kR) | bit(kD);
+  static constexpr uint32_t kNext = 0;
+  static constexpr int kOuts = 1;
+  using Pair = IPair;
+  template <bool TRUNC>
+  __device__ static __forceinline__ void coeff(const Params &, const StepIn &s, float, Pair &e,
+                                               float &, float &) {
+    e.c = __float_as_uint(s.r);
+    e.m = (s.first || s.dp != 0.0f) ? 0u : 1u;
+  }
+};
+
+}  // namespace rlcs

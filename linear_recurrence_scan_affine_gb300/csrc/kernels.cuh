@@ -1,0 +1,605 @@
+// The two launch shapes of the scan, templated on an estimator functor.
+//
+// Data layout on chip ("strip-major"): a warp walks its span of a row in
+// strips of 128 steps; in strip j lane l owns the four consecutive steps
+// 128*j + 4*l .. +3, so each warp-wide float4 access covers 512 contiguous
+// bytes. Per strip: each lane composes its four pairs (lane-serial
+// sub-scan), a 5-round shuffle scan composes the lanes, and the strips of a
+// warp are chained by their totals.
+//
+//  * warp_row_kernel    one warp per row (T <= 128*S): inputs go straight
+//                       to registers with 128-bit loads; no shared memory.
+//  * block_chunk_kernel one 256-thread block per row chunk of 1024*S steps:
+//                       the chunk's inputs are staged into shared memory by
+//                       cp.async.bulk (1-D TMA) completing on an mbarrier;
+//                       warp aggregates are composed in shared memory; the
+//                       chunks of one row are chained in a single pass by
+//                       decoupled look-back through the workspace
+//                       (ticket-ordered chunks, epoch-tagged flags, bounded
+//                       waits).
+#pragma once
+
+#include "estimators.cuh"
+
+namespace rlcs {
+
+constexpr int kStrip = 128;              // steps per warp strip
+constexpr int kChunkWarps = 8;           // warps per block in the chunk tier
+constexpr int kChunkThreads = kChunkWarps * 32;
+constexpr int kRowWarps = 4;             // rows (warps) per block, warp-row tier
+constexpr uint64_t kWaitLimitNs = 1ull << 30;  // ~1.07 s bound on every wait
+
+// Workspace: a 64-byte header, then one 16-byte record per chunk ticket.
+struct WsHeader {
+  uint32_t epoch;   // bumped by the last block of every chunked launch
+  uint32_t ticket;  // next chunk ticket
+  uint32_t done;    // blocks of the current launch that finished
+  uint32_t status;  // sticky device-side error (an rlcs_status code)
+  uint32_t pad[12];
+};
+struct WsRecord {
+  uint32_t flag;  // (epoch tag << 2) | state
+  uint32_t m;     // chunk aggregate pair, raw bits
+  uint32_t c;
+  uint32_t inc;   // inclusive value (value at the chunk's far end), raw bits
+};
+static_assert(sizeof(WsHeader) == 64 && sizeof(WsRecord) == 16, "workspace layout");
+constexpr uint32_t kStateAgg = 1u, kStateInc = 2u;
+constexpr uint32_t kTagMask = 0x3fffffffu;
+constexpr uint32_t kStatusWorkspace = 3u, kStatusTimeout = 5u;
+
+struct ChunkShape {
+  WsHeader *ws;            // workspace header (records follow it); may be
+                           // NULL when chunks_per_row == 1
+  int64_t chunks_per_row;  // Q
+  int64_t total_chunks;    // N * Q = grid size
+};
+
+// ---------------------------------------------------------------------------
+// Small helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float4 f4zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
+
+__device__ __forceinline__ float f4get(const float4 &v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+__device__ __forceinline__ void f4set(float4 &v, int i, float x) {
+  if (i == 0) v.x = x; else if (i == 1) v.y = x; else if (i == 2) v.z = x; else v.w = x;
+}
+
+// Four consecutive steps of one row starting at t (t % 4 == 0); steps past T
+// read as 0. vec: the row is 16-byte aligned and T % 4 == 0.
+__device__ __forceinline__ float4 load4(const float *row, int64_t t, int64_t T, bool vec) {
+  if (vec) return t < T ? __ldg(reinterpret_cast<const float4 *>(row + t)) : f4zero();
+  float4 v = f4zero();
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (t + i < T) f4set(v, i, __ldg(row + t + i));
+  return v;
+}
+
+__device__ __forceinline__ void store4(float *row, int64_t t, int64_t T, bool vec, float4 v) {
+  if (vec) {
+    if (t < T) *reinterpret_cast<float4 *>(row + t) = v;
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    if (t + i < T) row[t + i] = f4get(v, i);
+}
+
+// The step after each of a lane's four steps: lanes pass their first element
+// down; lane 31 takes `following` (first step after the strip).
+__device__ __forceinline__ float4 next4(const float4 &a, float following, int lane) {
+  float n = __shfl_down_sync(kFull, a.x, 1);
+  if (lane == 31) n = following;
+  return make_float4(a.y, a.z, a.w, n);
+}
+// The step before each of a lane's four steps; lane 0 takes `preceding`.
+__device__ __forceinline__ float4 prev4(const float4 &a, float preceding, int lane) {
+  float q = __shfl_up_sync(kFull, a.w, 1);
+  if (lane == 0) q = preceding;
+  return make_float4(q, a.x, a.y, a.z);
+}
+
+template <class P>
+__device__ __forceinline__ P lane_aggregate(const P (&e)[4], bool backward) {
+  P a;
+  if (backward) {  // e0 ∘ e1 ∘ e2 ∘ e3
+    a = compose(e[2], e[3]);
+    a = compose(e[1], a);
+    a = compose(e[0], a);
+  } else {  // e3 ∘ e2 ∘ e1 ∘ e0
+    a = compose(e[1], e[0]);
+    a = compose(e[2], a);
+    a = compose(e[3], a);
+  }
+  return a;
+}
+
+template <class P> struct ValueOf;
+template <> struct ValueOf<FPair> { using type = float; };
+template <> struct ValueOf<IPair> { using type = uint32_t; };
+
+__device__ __forceinline__ uint32_t vbits(float x) { return __float_as_uint(x); }
+__device__ __forceinline__ uint32_t vbits(uint32_t x) { return x; }
+__device__ __forceinline__ void vfrom(uint32_t b, float &x) { x = __uint_as_float(b); }
+__device__ __forceinline__ void vfrom(uint32_t b, uint32_t &x) { x = b; }
+
+// Where a warp's raw inputs come from.
+//  RegSource: every strip already in registers (warp-row tier).
+//  SmemSource: the block's staged chunk in shared memory (chunk tier).
+template <int S>
+struct RegSource {
+  const float4 (&raw)[kNumSlots][S];
+  const float (&halo_next)[kNumSlots];  // first step after the span
+  float halo_prev_d;                    // done mask just before the span
+  int lane;
+  __device__ __forceinline__ float4 get(int k, int j) const { return raw[k][j]; }
+  __device__ __forceinline__ float following(int k, int j) const {
+    return (j + 1 < S) ? __shfl_sync(kFull, raw[k][j + 1].x, 0) : halo_next[k];
+  }
+  __device__ __forceinline__ float preceding_d(int j) const {
+    return (j > 0) ? __shfl_sync(kFull, raw[kD][j - 1].w, 31) : halo_prev_d;
+  }
+};
+
+template <int S>
+struct SmemSource {
+  const float *slot[kNumSlots];         // per slot: the chunk's staged steps
+  int span_off;                         // warp's first step within the chunk
+  int chunk;                            // steps per chunk
+  const float (&halo_next)[kNumSlots];  // first step after the chunk
+  float halo_prev_d;                    // done mask before the chunk
+  int lane;
+  __device__ __forceinline__ float4 get(int k, int j) const {
+    return *reinterpret_cast<const float4 *>(slot[k] + span_off + j * kStrip + 4 * lane);
+  }
+  __device__ __forceinline__ float following(int k, int j) const {
+    const int pos = span_off + (j + 1) * kStrip;
+    return pos < chunk ? slot[k][pos] : halo_next[k];
+  }
+  __device__ __forceinline__ float preceding_d(int j) const {
+    const int pos = span_off + j * kStrip - 1;
+    return pos >= 0 ? slot[kD][pos] : halo_prev_d;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Strip engine for one warp's span of S strips.
+// ---------------------------------------------------------------------------
+template <class E, bool TRUNC, int S>
+struct Strips {
+  using P = typename E::Pair;
+  using V = typename ValueOf<P>::type;
+  static constexpr uint32_t kUse = E::kSlots | ((TRUNC && E::kBackward) ? kTruncSlots : 0u);
+
+  P el[S][4];
+  float aux0[S][4], aux1[S][4];
+  P excl[S], tot[S];
+
+  // t_span: the span's first step within the row; T: the row length.
+  template <class Src>
+  __device__ __forceinline__ void build(const Params &p, const Src &src, float boot,
+                                        int64_t t_span, int64_t T, int lane) {
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+      float4 raw[kNumSlots], nx[kNumSlots];
+#pragma unroll
+      for (int k = 0; k < kNumSlots; ++k) raw[k] = (kUse & bit(k)) ? src.get(k, j) : f4zero();
+#pragma unroll
+      for (int k = 0; k < kNumSlots; ++k)
+        nx[k] = (E::kBackward && (E::kNext & bit(k))) ? next4(raw[k], src.following(k, j), lane)
+                                                      : f4zero();
+      float4 dp = f4zero();
+      if (!E::kBackward) dp = prev4(raw[kD], src.preceding_d(j), lane);
+      const int64_t t0 = t_span + (int64_t)j * kStrip + 4 * lane;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t t = t0 + i;
+        StepIn s;
+        s.r = f4get(raw[kR], i);
+        s.v = f4get(raw[kV], i);
+        s.q = f4get(raw[kQ], i);
+        s.lr = f4get(raw[kLR], i);
+        s.d = f4get(raw[kD], i);
+        s.tau = f4get(raw[kTau], i);
+        s.nv = f4get(raw[kNV], i);
+        s.vn = f4get(nx[kV], i);
+        s.qn = f4get(nx[kQ], i);
+        s.lrn = f4get(nx[kLR], i);
+        s.dp = f4get(dp, i);
+        s.last = (t == T - 1);
+        s.first = (t == 0);
+        float a0 = 0.f, a1 = 0.f;
+        P e;
+        E::template coeff<TRUNC>(p, s, boot, e, a0, a1);
+        if (t >= T) e = identity(P{});  // ragged tail: padding is the identity
+        el[j][i] = e;
+        aux0[j][i] = a0;
+        aux1[j][i] = a1;
+      }
+    }
+  }
+
+  // Lane aggregates and per-strip warp scans. Returns the span's aggregate
+  // (strip 0 outermost for backward, strip S-1 outermost for forward).
+  __device__ __forceinline__ P scan(int lane) {
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+      const P a = lane_aggregate(el[j], E::kBackward);
+      if (E::kBackward) {
+        const P inc = warp_suffix_scan(a, lane);
+        tot[j] = shfl_idx(inc, 0);
+        const P x = shfl_down(inc, 1);
+        excl[j] = (lane == 31) ? identity(P{}) : x;
+      } else {
+        const P inc = warp_prefix_scan(a, lane);
+        tot[j] = shfl_idx(inc, 31);
+        const P x = shfl_up(inc, 1);
+        excl[j] = (lane == 0) ? identity(P{}) : x;
+      }
+    }
+    P agg = identity(P{});
+    if (E::kBackward) {
+#pragma unroll
+      for (int j = S - 1; j >= 0; --j) agg = compose(tot[j], agg);
+    } else {
+#pragma unroll
+      for (int j = 0; j < S; ++j) agg = compose(tot[j], agg);
+    }
+    return agg;
+  }
+
+  // Given the value just outside the span (after it for backward, before it
+  // for forward), produce every owned step's output(s).
+  __device__ __forceinline__ void finish(V carry, float4 (&o0)[S], float4 (&o1)[S]) {
+    V X = carry;
+    V outside[S];
+    if (E::kBackward) {
+#pragma unroll
+      for (int j = S - 1; j >= 0; --j) {
+        outside[j] = X;
+        X = apply(tot[j], X);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < S; ++j) {
+        outside[j] = X;
+        X = apply(tot[j], X);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < S; ++j) {
+      V nb = apply(excl[j], outside[j]);  // value adjacent to the lane's run
+      if (E::kBackward) {
+#pragma unroll
+        for (int i = 3; i >= 0; --i) {
+          const V A = apply(el[j][i], nb);
+          emit(j, i, A, nb, o0, o1);
+          nb = A;
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const V A = apply(el[j][i], nb);
+          emit(j, i, A, nb, o0, o1);
+          nb = A;
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ void emit(int j, int i, float A, float A_adj, float4 (&o0)[S],
+                                       float4 (&o1)[S]) {
+    f4set(o0[j], i, E::out0(A, A_adj, el[j][i], aux0[j][i], aux1[j][i]));
+    if constexpr (E::kOuts > 1)
+      f4set(o1[j], i, E::out1(A, A_adj, el[j][i], aux0[j][i], aux1[j][i]));
+  }
+  __device__ __forceinline__ void emit(int j, int i, uint32_t A, uint32_t, float4 (&o0)[S],
+                                       float4 (&)[S]) {
+    f4set(o0[j], i, __uint_as_float(A));
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Warp-row tier: one warp per row, S strips (T <= 128*S).
+// ---------------------------------------------------------------------------
+template <class E, bool TRUNC, int S>
+__global__ void __launch_bounds__(kRowWarps * 32) warp_row_kernel(Params p) {
+  using St = Strips<E, TRUNC, S>;
+  using V = typename St::V;
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  if (row >= p.N) return;  // whole warp leaves together
+  const int64_t T = p.T;
+  const int64_t base = row * T;
+  const bool vec = p.vec != 0;
+
+  float4 raw[kNumSlots][S];
+#pragma unroll
+  for (int k = 0; k < kNumSlots; ++k) {
+#pragma unroll
+    for (int j = 0; j < S; ++j)
+      raw[k][j] = (St::kUse & bit(k)) ? load4(p.in[k] + base, (int64_t)j * kStrip + 4 * lane, T, vec)
+                                      : f4zero();
+  }
+  const float boot = (E::kBackward && p.boot) ? __ldg(p.boot + row) : 0.f;
+  pdl_launch_dependents();
+
+  float halo[kNumSlots];
+#pragma unroll
+  for (int k = 0; k < kNumSlots; ++k) halo[k] = 0.f;  // past the row end: never used
+  const RegSource<S> src{raw, halo, 0.f, lane};
+  St st;
+  st.build(p, src, boot, 0, T, lane);
+  st.scan(lane);
+  float4 o0[S], o1[S];
+  st.finish(V(0), o0, o1);
+#pragma unroll
+  for (int j = 0; j < S; ++j) {
+    const int64_t t = (int64_t)j * kStrip + 4 * lane;
+    store4(static_cast<float *>(p.out0) + base, t, T, vec, o0[j]);
+    if constexpr (E::kOuts > 1) {
+      if (p.out1) store4(p.out1 + base, t, T, vec, o1[j]);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Block-chunk tier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void set_status(WsHeader *ws, uint32_t code) {
+  if (ws != nullptr) atomicCAS(&ws->status, 0u, code);
+}
+
+// Bounded wait on phase 0 of the block's mbarrier. False on timeout.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar) {
+  if (mbar_try_wait(bar, 0)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, 0)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+
+// Decoupled look-back for the chunk with ticket `ticket` (warp-wide call).
+// Publishes the chunk aggregate, walks predecessor tickets (nearer first, 32
+// per round) until one holds an inclusive value, composes the aggregates in
+// between, publishes this chunk's inclusive value and returns the value just
+// outside the chunk on its scan-origin side. Every wait is bounded; on
+// timeout the status word records RLCS_ERR_TIMEOUT and missing aggregates
+// count as the identity, so the launch always finishes.
+template <class P, class V>
+__device__ V lookback(WsHeader *ws, int64_t ticket, int64_t row_first, P agg, uint32_t tag,
+                      int lane) {
+  WsRecord *rec = reinterpret_cast<WsRecord *>(ws + 1);
+  if (ticket == row_first) {  // the row's scan origin: nothing before it
+    if (lane == 0) {
+      __stcg(&rec[ticket].m, vbits(agg.m));
+      __stcg(&rec[ticket].c, vbits(agg.c));
+      __stcg(&rec[ticket].inc, vbits(apply(agg, V(0))));
+      st_release_gpu(&rec[ticket].flag, (tag << 2) | kStateInc);
+    }
+    return V(0);
+  }
+  if (lane == 0) {
+    __stcg(&rec[ticket].m, vbits(agg.m));
+    __stcg(&rec[ticket].c, vbits(agg.c));
+    st_release_gpu(&rec[ticket].flag, (tag << 2) | kStateAgg);
+  }
+  P acc = identity(P{});
+  V X = V(0);
+  bool timed_out = false;
+  int64_t look = ticket - 1;
+  while (true) {
+    const int64_t tk = look - lane;
+    const bool valid = tk >= row_first;
+    uint32_t f = 0;
+    uint64_t start = 0;
+    while (true) {
+      if (valid) f = ld_acquire_gpu(&rec[tk].flag);
+      const bool ready = !valid || (((f >> 2) == tag) && (f & 3u) != 0u);
+      if (__all_sync(kFull, ready)) break;
+      const uint64_t now = globaltimer_ns();
+      if (start == 0) start = now;
+      if (__any_sync(kFull, now - start > kWaitLimitNs)) {
+        timed_out = true;
+        break;
+      }
+      __nanosleep(40);
+    }
+    const bool ready = valid && ((f >> 2) == tag) && (f & 3u) != 0u;
+    const unsigned pm = __ballot_sync(kFull, ready && (f & 3u) == kStateInc);
+    const int firstP = pm ? __ffs(pm) - 1 : 32;
+    P mine = identity(P{});
+    uint32_t inc_bits = 0;
+    if (ready && lane < firstP) {
+      vfrom(__ldcg(&rec[tk].m), mine.m);
+      vfrom(__ldcg(&rec[tk].c), mine.c);
+    }
+    if (lane == firstP) inc_bits = __ldcg(&rec[tk].inc);
+    P win = warp_reduce_outer_first(mine);
+    win = shfl_idx(win, 0);
+    acc = compose(acc, win);
+    if (pm) {
+      V incv;
+      vfrom(__shfl_sync(kFull, inc_bits, firstP), incv);
+      X = apply(acc, incv);
+      break;
+    }
+    if (timed_out || look - 32 < row_first) {  // only reachable after a timeout
+      X = apply(acc, V(0));
+      timed_out = true;
+      break;
+    }
+    look -= 32;
+  }
+  if (lane == 0) {
+    if (timed_out) set_status(ws, kStatusTimeout);
+    __stcg(&rec[ticket].inc, vbits(apply(agg, X)));
+    st_release_gpu(&rec[ticket].flag, (tag << 2) | kStateInc);
+  }
+  return X;
+}
+
+template <class E, bool TRUNC, int S>
+__global__ void __launch_bounds__(kChunkThreads) block_chunk_kernel(Params p, ChunkShape cs) {
+  using St = Strips<E, TRUNC, S>;
+  using P = typename St::P;
+  using V = typename St::V;
+  constexpr int C = kChunkWarps * kStrip * S;  // steps per chunk
+  constexpr uint32_t kUse = St::kUse;
+  constexpr int kNumUsed = __builtin_popcount(kUse);
+
+  extern __shared__ __align__(128) float smem[];  // [kNumUsed][C]
+  __shared__ uint64_t bar;
+  __shared__ P s_warp[kChunkWarps];
+  __shared__ V s_carry[kChunkWarps];
+  __shared__ int64_t s_ticket;
+  __shared__ uint32_t s_epoch;
+  __shared__ int s_ok;
+
+  pdl_wait();
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool vec = p.vec != 0;
+  const int64_t T = p.T, Q = cs.chunks_per_row;
+
+  if (tid == 0) {
+    int64_t ticket = blockIdx.x;
+    uint32_t epoch = 0;
+    int ok = 1;
+    if (Q > 1) {
+      ticket = atomicAdd(&cs.ws->ticket, 1u);
+      epoch = ld_relaxed_gpu(&cs.ws->epoch);
+      if (ticket >= cs.total_chunks) {
+        set_status(cs.ws, kStatusWorkspace);
+        ok = 0;
+      }
+    }
+    s_ticket = ticket;
+    s_epoch = epoch;
+    s_ok = ok;
+    if (ok && vec) {
+      const int64_t row = ticket / Q, kk = ticket - row * Q;
+      const int64_t q = E::kBackward ? (Q - 1 - kk) : kk;
+      const int64_t t0 = q * C;
+      const int64_t len = (T - t0 < C) ? (T - t0) : C;
+      mbar_init(&bar, 1);
+      fence_mbar_init();
+      fence_proxy_async_shared();
+      mbar_arrive_expect_tx(&bar, (uint32_t)(kNumUsed * len * 4));
+      int idx = 0;
+#pragma unroll
+      for (int k = 0; k < kNumSlots; ++k) {
+        if (kUse & bit(k)) {
+          bulk_g2s(smem + idx * C, p.in[k] + row * T + t0, (uint32_t)(len * 4), &bar);
+          ++idx;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (!s_ok) return;  // uniform: a corrupted workspace handed out a bad ticket
+
+  const int64_t ticket = s_ticket;
+  const int64_t row = ticket / Q, kk = ticket - row * Q;
+  const int64_t q = E::kBackward ? (Q - 1 - kk) : kk;
+  const int64_t t0 = q * C;
+  const int64_t base = row * T;
+  const int span_off = warp * kStrip * S;
+
+  if (!vec) {  // unaligned rows: stage with plain loads
+    int idx = 0;
+#pragma unroll
+    for (int k = 0; k < kNumSlots; ++k) {
+      if (kUse & bit(k)) {
+        for (int e = tid; e < C; e += kChunkThreads)
+          smem[idx * C + e] = (t0 + e < T) ? __ldg(p.in[k] + base + t0 + e) : 0.f;
+        ++idx;
+      }
+    }
+  }
+
+  // Halo steps just outside the chunk (read while the bulk copy is in flight).
+  float halo[kNumSlots];
+#pragma unroll
+  for (int k = 0; k < kNumSlots; ++k) {
+    halo[k] = 0.f;
+    if (E::kBackward && (E::kNext & bit(k)) && warp == kChunkWarps - 1 && t0 + C < T)
+      halo[k] = __ldg(p.in[k] + base + t0 + C);
+  }
+  const float halo_d = (!E::kBackward && warp == 0 && t0 > 0) ? __ldg(p.in[kD] + base + t0 - 1)
+                                                              : 0.f;
+  const float boot = (E::kBackward && p.boot) ? __ldg(p.boot + row) : 0.f;
+
+  if (vec) {
+    if (!wait_bar(&bar)) set_status(cs.ws, kStatusTimeout);
+  } else {
+    __syncthreads();
+  }
+  pdl_launch_dependents();
+
+  SmemSource<S> src{{}, span_off, C, halo, halo_d, lane};
+  {
+    int idx = 0;
+#pragma unroll
+    for (int k = 0; k < kNumSlots; ++k) {
+      src.slot[k] = smem + idx * C;  // unused slots alias a used one; never read
+      if (kUse & bit(k)) ++idx;
+    }
+  }
+  St st;
+  st.build(p, src, boot, t0 + span_off, T, lane);
+  const P wagg = st.scan(lane);
+  if (lane == 0) s_warp[warp] = wagg;
+  __syncthreads();
+
+  if (warp == 0) {
+    const P w = (lane < kChunkWarps) ? s_warp[lane] : identity(P{});
+    P inc, nb;
+    P chunk_agg;
+    if (E::kBackward) {
+      inc = warp_suffix_scan(w, lane);
+      chunk_agg = shfl_idx(inc, 0);
+      const P x = shfl_down(inc, 1);
+      nb = (lane >= kChunkWarps - 1) ? identity(P{}) : x;
+    } else {
+      inc = warp_prefix_scan(w, lane);
+      chunk_agg = shfl_idx(inc, kChunkWarps - 1);
+      const P x = shfl_up(inc, 1);
+      nb = (lane == 0) ? identity(P{}) : x;
+    }
+    V X = V(0);
+    if (Q > 1) {
+      const uint32_t epoch = s_epoch;
+      X = lookback<P, V>(cs.ws, ticket, row * Q, chunk_agg, epoch & kTagMask, lane);
+      if (lane == 0) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(&cs.ws->done, 1u);
+        if (prev == (uint32_t)(cs.total_chunks - 1)) {  // last block of the launch
+          cs.ws->ticket = 0u;
+          cs.ws->done = 0u;
+          __threadfence();
+          cs.ws->epoch = epoch + 1u;
+        }
+      }
+    }
+    if (lane < kChunkWarps) s_carry[lane] = apply(nb, X);
+  }
+  __syncthreads();
+
+  float4 o0[S], o1[S];
+  st.finish(s_carry[warp], o0, o1);
+#pragma unroll
+  for (int j = 0; j < S; ++j) {
+    const int64_t t = t0 + span_off + (int64_t)j * kStrip + 4 * lane;
+    store4(static_cast<float *>(p.out0) + base, t, T, vec, o0[j]);
+    if constexpr (E::kOuts > 1) {
+      if (p.out1) store4(p.out1 + base, t, T, vec, o1[j]);
+    }
+  }
+}
+
+}  // namespace rlcs

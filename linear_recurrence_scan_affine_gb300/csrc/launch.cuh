@@ -1,0 +1,81 @@
+// Host-side launch of one estimator in the shape the planner chose.
+#pragma once
+
+#include <mutex>
+
+#include "kernels.cuh"
+#include "rlcs.h"
+
+namespace rlcs {
+
+struct Plan {
+  int shape;       // RLCS_SHAPE_WARP_ROW or RLCS_SHAPE_BLOCK_CHUNK
+  int S;           // strips per warp: 1, 2 or 4
+  int64_t Q;       // chunks per row (block-chunk shape)
+  bool trunc;      // truncation inputs present
+  bool pdl;        // launch with programmatic stream serialization
+};
+
+template <class K, class... Args>
+inline cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <class E, bool TRUNC, int S>
+inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws, cudaStream_t s) {
+  if (plan.shape == RLCS_SHAPE_WARP_ROW) {
+    const dim3 grid((unsigned)((p.N + kRowWarps - 1) / kRowWarps));
+    return launch_ex(warp_row_kernel<E, TRUNC, S>, grid, dim3(kRowWarps * 32), 0, s, plan.pdl, p);
+  }
+  constexpr uint32_t kUse = Strips<E, TRUNC, S>::kUse;
+  constexpr size_t smem = (size_t)__builtin_popcount(kUse) * kChunkWarps * kStrip * S * 4;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(block_chunk_kernel<E, TRUNC, S>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  ChunkShape cs{ws, plan.Q, p.N * plan.Q};
+  return launch_ex(block_chunk_kernel<E, TRUNC, S>, dim3((unsigned)(p.N * plan.Q)),
+                   dim3(kChunkThreads), smem, s, plan.pdl, p, cs);
+}
+
+template <class E, bool TRUNC>
+inline cudaError_t launch_trunc(const Params &p, const Plan &plan, WsHeader *ws, cudaStream_t s) {
+  switch (plan.S) {
+    case 1: return launch_shape<E, TRUNC, 1>(p, plan, ws, s);
+    case 2: return launch_shape<E, TRUNC, 2>(p, plan, ws, s);
+    case 4: return launch_shape<E, TRUNC, 4>(p, plan, ws, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+template <class E>
+inline cudaError_t launch_estimator(const Params &p, const Plan &plan, WsHeader *ws,
+                                    cudaStream_t s) {
+  if (E::kBackward && plan.trunc) return launch_trunc<E, true>(p, plan, ws, s);
+  return launch_trunc<E, false>(p, plan, ws, s);
+}
+
+// One launcher per estimator, each in its own translation unit.
+cudaError_t launch_gae(const Params &, const Plan &, WsHeader *, cudaStream_t);
+cudaError_t launch_lambda_returns(const Params &, const Plan &, WsHeader *, cudaStream_t);
+cudaError_t launch_discounted_returns(const Params &, const Plan &, WsHeader *, cudaStream_t);
+cudaError_t launch_vtrace(const Params &, const Plan &, WsHeader *, cudaStream_t);
+cudaError_t launch_retrace(const Params &, const Plan &, WsHeader *, cudaStream_t);
+cudaError_t launch_eligibility_traces(const Params &, const Plan &, WsHeader *, cudaStream_t);
+cudaError_t launch_episodic_prefix_sum(const Params &, const Plan &, WsHeader *, cudaStream_t);
+
+}  // namespace rlcs

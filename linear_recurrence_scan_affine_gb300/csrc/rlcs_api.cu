@@ -1,0 +1,324 @@
+// C ABI entry points: argument validation, launch-shape planning and the
+// workspace/status helpers declared in include/rlcs.h.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "launch.cuh"
+
+namespace rlcs {
+namespace {
+
+constexpr int64_t kRowMaxT = 512;       // warp-row shape: T <= 4 strips
+constexpr int64_t kMinChunk = 1024;     // smallest block chunk (S = 1)
+constexpr int kMaxDevices = 64;
+
+std::atomic<int> g_override_shape{RLCS_SHAPE_AUTO};
+std::atomic<int64_t> g_override_chunk{0};
+std::atomic<int> g_sm_count[kMaxDevices];
+
+int sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
+  int v = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+      v = 152;
+    g_sm_count[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Choose the launch shape for an [N, T] call.
+rlcs_status plan_call(int64_t N, int64_t T, bool trunc, Plan &plan) {
+  plan = Plan{};
+  plan.trunc = trunc;
+  plan.pdl = true;
+  const int ov = g_override_shape.load(std::memory_order_relaxed);
+  if (ov == RLCS_SHAPE_WARP_ROW || (ov == RLCS_SHAPE_AUTO && T <= kRowMaxT)) {
+    if (T > kRowMaxT) return RLCS_ERR_INVALID_ARG;
+    plan.shape = RLCS_SHAPE_WARP_ROW;
+    plan.S = T <= 128 ? 1 : (T <= 256 ? 2 : 4);
+    plan.Q = 1;
+    return RLCS_OK;
+  }
+  plan.shape = RLCS_SHAPE_BLOCK_CHUNK;
+  int64_t chunk = g_override_chunk.load(std::memory_order_relaxed);
+  if (ov != RLCS_SHAPE_BLOCK_CHUNK || chunk == 0) {
+    // Largest chunk that still gives every SM a few blocks to overlap.
+    const int64_t want_blocks = 4 * (int64_t)sm_count();
+    chunk = 4096;
+    while (chunk > kMinChunk && N * ceil_div(T, chunk) < want_blocks) chunk /= 2;
+    while (chunk > kMinChunk && chunk / 2 >= T) chunk /= 2;
+  }
+  plan.S = (int)(chunk / kMinChunk);
+  plan.Q = ceil_div(T, chunk);
+  return RLCS_OK;
+}
+
+size_t ws_bytes_for(int64_t N, int64_t Q) {
+  return sizeof(WsHeader) + sizeof(WsRecord) * (size_t)N * (size_t)Q;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Buf {
+  const void *p;
+  size_t bytes;
+};
+bool overlaps(const Buf &a, const Buf &b) {
+  if (!a.p || !b.p) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// Shared tail of every entry point.
+template <class Launch>
+rlcs_status run(Params &p, const float *trunc, const float *next_values, void *const *outs,
+                int n_outs, void *ws, size_t ws_bytes, cudaStream_t stream, Launch launch) {
+  const int64_t N = p.N, T = p.T;
+  if (N <= 0 || T <= 0) return RLCS_ERR_INVALID_ARG;
+  if (N > (int64_t)(INT64_MAX / 4) / T) return RLCS_ERR_INVALID_ARG;
+  if ((trunc == nullptr) != (next_values == nullptr)) return RLCS_ERR_INVALID_ARG;
+  p.in[kTau] = trunc;
+  p.in[kNV] = next_values;
+  const size_t plane = (size_t)N * (size_t)T * 4u;
+  bool vec = (T % 4) == 0;
+  for (int k = 0; k < kNumSlots; ++k)
+    if (p.in[k] && !aligned16(p.in[k])) vec = false;
+  for (int o = 0; o < n_outs; ++o) {
+    if (!outs[o]) continue;
+    if (!aligned16(outs[o])) vec = false;
+    const Buf ob{outs[o], plane};
+    for (int k = 0; k < kNumSlots; ++k)
+      if (overlaps(ob, Buf{p.in[k], plane})) return RLCS_ERR_INVALID_ARG;
+    if (overlaps(ob, Buf{p.boot, (size_t)N * 4u})) return RLCS_ERR_INVALID_ARG;
+    for (int o2 = o + 1; o2 < n_outs; ++o2)
+      if (overlaps(ob, Buf{outs[o2], plane})) return RLCS_ERR_INVALID_ARG;
+  }
+  p.vec = vec ? 1 : 0;
+
+  Plan plan;
+  const rlcs_status st = plan_call(N, T, trunc != nullptr, plan);
+  if (st != RLCS_OK) return st;
+  WsHeader *wsh = nullptr;
+  if (plan.shape == RLCS_SHAPE_BLOCK_CHUNK) {
+    if (N * plan.Q >= (int64_t)UINT32_MAX) return RLCS_ERR_INVALID_ARG;
+    if (plan.Q > 1) {
+      if (!ws || ws_bytes < ws_bytes_for(N, plan.Q) || !aligned16(ws)) return RLCS_ERR_WORKSPACE;
+    }
+    if (ws && ws_bytes >= sizeof(WsHeader) && aligned16(ws)) wsh = static_cast<WsHeader *>(ws);
+    for (const Buf &b : {Buf{ws, ws_bytes}})
+      for (int k = 0; k < kNumSlots; ++k)
+        if (overlaps(b, Buf{p.in[k], plane})) return RLCS_ERR_INVALID_ARG;
+  }
+  const cudaError_t err = launch(p, plan, wsh, stream);
+  if (err != cudaSuccess) {
+    cudaGetLastError();  // clear the non-sticky launch error
+    return RLCS_ERR_CUDA;
+  }
+  return RLCS_OK;
+}
+
+Params base_params(int64_t N, int64_t T, const float *boot) {
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.N = N;
+  p.T = T;
+  p.boot = boot;
+  return p;
+}
+
+}  // namespace
+}  // namespace rlcs
+
+using namespace rlcs;
+
+extern "C" {
+
+size_t rlcs_workspace_bytes(int64_t N, int64_t T) {
+  if (N <= 0 || T <= 0) return 0;
+  return ws_bytes_for(N, ceil_div(T, kMinChunk));
+}
+
+rlcs_status rlcs_workspace_init(void *workspace, size_t bytes, rlcs_stream_t stream) {
+  if (!workspace || bytes == 0) return RLCS_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(workspace, 0, bytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return RLCS_ERR_CUDA;
+  }
+  return RLCS_OK;
+}
+
+rlcs_status rlcs_check_status(void *workspace, rlcs_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return RLCS_ERR_CUDA;
+  }
+  if (!workspace) return RLCS_OK;
+  uint32_t code = 0;
+  WsHeader *h = static_cast<WsHeader *>(workspace);
+  if (cudaMemcpy(&code, &h->status, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return RLCS_ERR_CUDA;
+  }
+  if (code == 0) return RLCS_OK;
+  if (cudaMemset(&h->status, 0, sizeof(code)) != cudaSuccess) {
+    cudaGetLastError();
+    return RLCS_ERR_CUDA;
+  }
+  return static_cast<rlcs_status>(code);
+}
+
+const char *rlcs_status_string(rlcs_status status) {
+  switch (status) {
+    case RLCS_OK: return "RLCS_OK";
+    case RLCS_ERR_INVALID_ARG: return "RLCS_ERR_INVALID_ARG: bad size, NULL pointer, aliasing or half a truncation pair";
+    case RLCS_ERR_MISALIGNED: return "RLCS_ERR_MISALIGNED";
+    case RLCS_ERR_WORKSPACE: return "RLCS_ERR_WORKSPACE: workspace missing, too small or not initialised";
+    case RLCS_ERR_CUDA: return "RLCS_ERR_CUDA: a CUDA call or kernel launch failed";
+    case RLCS_ERR_TIMEOUT: return "RLCS_ERR_TIMEOUT: a device-side bounded wait ran out";
+  }
+  return "unknown rlcs_status";
+}
+
+rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk) {
+  if (shape != RLCS_SHAPE_AUTO && shape != RLCS_SHAPE_WARP_ROW && shape != RLCS_SHAPE_BLOCK_CHUNK)
+    return RLCS_ERR_INVALID_ARG;
+  if (shape == RLCS_SHAPE_BLOCK_CHUNK && !(chunk == 0 || chunk == 1024 || chunk == 2048 || chunk == 4096))
+    return RLCS_ERR_INVALID_ARG;
+  g_override_chunk.store(shape == RLCS_SHAPE_BLOCK_CHUNK ? chunk : 0);
+  g_override_shape.store(shape);
+  return RLCS_OK;
+}
+
+rlcs_status rlcs_gae(const float *rewards, const float *values, const float *terminateds,
+                     const float *truncateds, const float *next_values,
+                     const float *bootstrap_value, float *advantages, int64_t N, int64_t T,
+                     float gamma, float lambda, void *workspace, size_t workspace_bytes,
+                     rlcs_stream_t stream) {
+  if (!rewards || !values || !terminateds || !advantages) return RLCS_ERR_INVALID_ARG;
+  Params p = base_params(N, T, bootstrap_value);
+  p.in[kR] = rewards;
+  p.in[kV] = values;
+  p.in[kD] = terminateds;
+  p.out0 = advantages;
+  p.gamma = gamma;
+  p.lambda = lambda;
+  void *outs[1] = {advantages};
+  return run(p, truncateds, next_values, outs, 1, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), launch_gae);
+}
+
+rlcs_status rlcs_lambda_returns(const float *rewards, const float *values,
+                                const float *terminateds, const float *truncateds,
+                                const float *next_values, const float *bootstrap_value,
+                                float *returns, int64_t N, int64_t T, float gamma, float lambda,
+                                void *workspace, size_t workspace_bytes, rlcs_stream_t stream) {
+  if (!rewards || !values || !terminateds || !returns) return RLCS_ERR_INVALID_ARG;
+  Params p = base_params(N, T, bootstrap_value);
+  p.in[kR] = rewards;
+  p.in[kV] = values;
+  p.in[kD] = terminateds;
+  p.out0 = returns;
+  p.gamma = gamma;
+  p.lambda = lambda;
+  void *outs[1] = {returns};
+  return run(p, truncateds, next_values, outs, 1, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), launch_lambda_returns);
+}
+
+rlcs_status rlcs_discounted_returns(const float *rewards, const float *terminateds,
+                                    const float *truncateds, const float *next_values,
+                                    const float *bootstrap_value, float *returns, int64_t N,
+                                    int64_t T, float gamma, void *workspace,
+                                    size_t workspace_bytes, rlcs_stream_t stream) {
+  if (!rewards || !terminateds || !returns) return RLCS_ERR_INVALID_ARG;
+  Params p = base_params(N, T, bootstrap_value);
+  p.in[kR] = rewards;
+  p.in[kD] = terminateds;
+  p.out0 = returns;
+  p.gamma = gamma;
+  void *outs[1] = {returns};
+  return run(p, truncateds, next_values, outs, 1, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), launch_discounted_returns);
+}
+
+rlcs_status rlcs_vtrace(const float *rewards, const float *values, const float *log_rhos,
+                        const float *terminateds, const float *truncateds,
+                        const float *next_values, const float *bootstrap_value, float *vs,
+                        float *pg_advantages, int64_t N, int64_t T, float gamma, float lambda,
+                        float rho_bar, float c_bar, void *workspace, size_t workspace_bytes,
+                        rlcs_stream_t stream) {
+  if (!rewards || !values || !log_rhos || !terminateds || !vs) return RLCS_ERR_INVALID_ARG;
+  Params p = base_params(N, T, bootstrap_value);
+  p.in[kR] = rewards;
+  p.in[kV] = values;
+  p.in[kLR] = log_rhos;
+  p.in[kD] = terminateds;
+  p.out0 = vs;
+  p.out1 = pg_advantages;
+  p.gamma = gamma;
+  p.lambda = lambda;
+  p.rho_bar = rho_bar;
+  p.c_bar = c_bar;
+  void *outs[2] = {vs, pg_advantages};
+  return run(p, truncateds, next_values, outs, 2, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), launch_vtrace);
+}
+
+rlcs_status rlcs_retrace(const float *rewards, const float *values, const float *q_values,
+                         const float *log_rhos, const float *terminateds,
+                         const float *truncateds, const float *next_values,
+                         const float *bootstrap_value, float *q_ret, int64_t N, int64_t T,
+                         float gamma, float lambda, float c_bar, void *workspace,
+                         size_t workspace_bytes, rlcs_stream_t stream) {
+  if (!rewards || !values || !q_values || !log_rhos || !terminateds || !q_ret)
+    return RLCS_ERR_INVALID_ARG;
+  Params p = base_params(N, T, bootstrap_value);
+  p.in[kR] = rewards;
+  p.in[kV] = values;
+  p.in[kQ] = q_values;
+  p.in[kLR] = log_rhos;
+  p.in[kD] = terminateds;
+  p.out0 = q_ret;
+  p.gamma = gamma;
+  p.lambda = lambda;
+  p.c_bar = c_bar;
+  void *outs[1] = {q_ret};
+  return run(p, truncateds, next_values, outs, 1, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), launch_retrace);
+}
+
+rlcs_status rlcs_eligibility_traces(const float *x, const float *dones, float *traces, int64_t N,
+                                    int64_t T, float gamma, float lambda, void *workspace,
+                                    size_t workspace_bytes, rlcs_stream_t stream) {
+  if (!x || !dones || !traces) return RLCS_ERR_INVALID_ARG;
+  Params p = base_params(N, T, nullptr);
+  p.in[kR] = x;
+  p.in[kD] = dones;
+  p.out0 = traces;
+  p.gamma = gamma;
+  p.lambda = lambda;
+  void *outs[1] = {traces};
+  return run(p, nullptr, nullptr, outs, 1, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), launch_eligibility_traces);
+}
+
+rlcs_status rlcs_episodic_prefix_sum(const int32_t *x, const float *dones, int32_t *out,
+                                     int64_t N, int64_t T, void *workspace,
+                                     size_t workspace_bytes, rlcs_stream_t stream) {
+  if (!x || !dones || !out) return RLCS_ERR_INVALID_ARG;
+  Params p = base_params(N, T, nullptr);
+  p.in[kR] = reinterpret_cast<const float *>(x);  // raw int32 bits travel in slot R
+  p.in[kD] = dones;
+  p.out0 = out;
+  void *outs[1] = {out};
+  return run(p, nullptr, nullptr, outs, 1, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), launch_episodic_prefix_sum);
+}
+
+}  // extern "C"

@@ -1,0 +1,152 @@
+"""Host-side checks of the C ABI boundary (no GPU needed, no kernel launched).
+
+The library must load, export every function include/rlcs.h declares, and
+reject bad arguments with the documented status before anything reaches the
+GPU. Fake device addresses are fine here: argument errors return before any
+CUDA call that would touch them.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rlcs.h")
+
+OK, INVALID, MISALIGNED, WORKSPACE, CUDA, TIMEOUT = 0, 1, 2, 3, 4, 5
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from linear_recurrence_scan_affine_gb300 import build
+    build.build()
+    from linear_recurrence_scan_affine_gb300 import binding
+    return binding.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(rlcs_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_the_seven_estimators():
+    names = declared_functions()
+    for est in ("gae", "vtrace", "retrace", "lambda_returns", "discounted_returns",
+                "eligibility_traces", "episodic_prefix_sum"):
+        assert "rlcs_" + est in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_exports_match_nm():
+    # the dynamic symbol table holds each declared function with C linkage
+    import subprocess
+    from linear_recurrence_scan_affine_gb300 import binding
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    syms = {l.split()[-1] for l in out.splitlines() if l.strip()}
+    for name in declared_functions():
+        assert name in syms, name
+
+
+def test_status_strings(lib):
+    for code in range(6):
+        s = lib.rlcs_status_string(code).decode()
+        assert s.startswith("RLCS_")
+    assert lib.rlcs_status_string(99).decode() == "unknown rlcs_status"
+
+
+def test_workspace_bytes(lib):
+    assert lib.rlcs_workspace_bytes(0, 10) == 0
+    assert lib.rlcs_workspace_bytes(10, 0) == 0
+    assert lib.rlcs_workspace_bytes(-1, 10) == 0
+    # 64-byte header + 16 bytes per 1024-step chunk of every row
+    assert lib.rlcs_workspace_bytes(4096, 128) == 64 + 16 * 4096
+    assert lib.rlcs_workspace_bytes(8, 131072) == 64 + 16 * 8 * 128
+    assert lib.rlcs_workspace_bytes(3, 1025) == 64 + 16 * 3 * 2
+
+
+FAKE = 0x7f0000000000  # 16-byte aligned fake device address, never dereferenced
+
+
+def fake(i, nbytes=1 << 24):
+    return ctypes.c_void_p(FAKE + i * nbytes)
+
+
+def gae(lib, r, v, d, tr, nv, b, out, N, T, ws=None, wsb=0):
+    return lib.rlcs_gae(r, v, d, tr, nv, b, out, N, T, 0.99, 0.95, ws, wsb, None)
+
+
+def test_gae_rejects_bad_sizes(lib):
+    a = [fake(i) for i in range(4)]
+    for N, T in [(0, 8), (8, 0), (-1, 8), (8, -5), (1 << 40, 1 << 40)]:
+        assert gae(lib, a[0], a[1], a[2], None, None, None, a[3], N, T) == INVALID
+
+
+def test_rejects_null_required_pointers(lib):
+    a = [fake(i) for i in range(4)]
+    assert gae(lib, None, a[1], a[2], None, None, None, a[3], 4, 8) == INVALID
+    assert gae(lib, a[0], None, a[2], None, None, None, a[3], 4, 8) == INVALID
+    assert gae(lib, a[0], a[1], None, None, None, None, a[3], 4, 8) == INVALID
+    assert gae(lib, a[0], a[1], a[2], None, None, None, None, 4, 8) == INVALID
+    assert lib.rlcs_vtrace(a[0], a[1], None, a[2], None, None, None, a[3], None, 4, 8,
+                           0.99, 1.0, 1.0, 1.0, None, 0, None) == INVALID
+    assert lib.rlcs_retrace(a[0], a[1], a[2], None, a[3], None, None, None, fake(9), 4, 8,
+                            0.99, 1.0, 1.0, None, 0, None) == INVALID
+    assert lib.rlcs_eligibility_traces(None, a[1], a[2], 4, 8, 0.9, 0.9, None, 0, None) == INVALID
+    assert lib.rlcs_episodic_prefix_sum(a[0], None, a[2], 4, 8, None, 0, None) == INVALID
+    assert lib.rlcs_discounted_returns(a[0], a[1], None, None, None, None, 4, 8, 0.9,
+                                       None, 0, None) == INVALID
+
+
+def test_rejects_half_truncation_pair(lib):
+    a = [fake(i) for i in range(6)]
+    assert gae(lib, a[0], a[1], a[2], a[4], None, None, a[3], 4, 8) == INVALID
+    assert gae(lib, a[0], a[1], a[2], None, a[5], None, a[3], 4, 8) == INVALID
+
+
+def test_rejects_aliasing(lib):
+    a = [fake(i) for i in range(4)]
+    # output identical to an input
+    assert gae(lib, a[0], a[1], a[2], None, None, None, a[0], 4, 8) == INVALID
+    assert gae(lib, a[0], a[1], a[2], None, None, None, a[2], 4, 8) == INVALID
+    # output overlapping an input by part of a row
+    inner = ctypes.c_void_p(a[1].value + 16)
+    assert gae(lib, a[0], a[1], a[2], None, None, None, inner, 4, 8) == INVALID
+    # V-trace outputs overlapping each other
+    assert lib.rlcs_vtrace(a[0], a[1], a[2], a[3], None, None, None, fake(7),
+                           ctypes.c_void_p(fake(7).value + 64), 4, 8, 0.99, 1.0, 1.0, 1.0,
+                           None, 0, None) == INVALID
+    # output overlapping the bootstrap array
+    assert gae(lib, a[0], a[1], a[2], None, None, fake(5), fake(5), 4, 8) == INVALID
+
+
+def test_long_rows_need_a_workspace(lib):
+    a = [fake(i, 1 << 30) for i in range(4)]
+    lib.rlcs_set_shape_override(0, 0)
+    N, T = 4, 1 << 16
+    assert gae(lib, a[0], a[1], a[2], None, None, None, a[3], N, T) == WORKSPACE
+    small = lib.rlcs_workspace_bytes(N, T) // 8
+    assert gae(lib, a[0], a[1], a[2], None, None, None, a[3], N, T, fake(20, 1 << 30),
+               small) == WORKSPACE
+
+
+def test_shape_override_validation(lib):
+    assert lib.rlcs_set_shape_override(7, 0) == INVALID
+    assert lib.rlcs_set_shape_override(2, 3000) == INVALID
+    assert lib.rlcs_set_shape_override(2, 2048) == OK
+    assert lib.rlcs_set_shape_override(0, 0) == OK
+    # warp-row is limited to T <= 512
+    assert lib.rlcs_set_shape_override(1, 0) == OK
+    a = [fake(i) for i in range(4)]
+    assert gae(lib, a[0], a[1], a[2], None, None, None, a[3], 4, 1000) == INVALID
+    assert lib.rlcs_set_shape_override(0, 0) == OK
+
+
+def test_workspace_init_rejects_null(lib):
+    assert lib.rlcs_workspace_init(None, 64, None) == INVALID
