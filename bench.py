@@ -1,0 +1,573 @@
+"""Benchmark: the seven credit-assignment estimators at num_envs=4096, seq_len=128.
+
+One step = one pass of the whole hot path over one synthetic batch: GAE,
+TD(lambda) returns, discounted returns, V-trace (vs + pg advantages),
+Retrace(lambda), eligibility traces and the episodic prefix sum, each on its
+own inputs (so no kernel reads another's data out of L2). value = env-steps
+per second with all seven outputs produced for every (env, t).
+
+Timing: CUDA graphs of the step's launches, replayed over 8 rotating sets of
+input/output buffers whose footprint is several times the L2, CUDA events on
+the launching stream, barrier + synchronize on both sides, max over ranks.
+Also reported: every estimator alone (graph of back-to-back launches on
+rotating buffers), the roofline of the dominant kernel against the measured
+HBM copy bandwidth, an end-to-end figure through host buffers (pinned H2D
+copies + kernels + D2H copies per step), SM clocks sampled during the timed
+region, and the float64 CPU oracle timed on the host cores as a baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank processes its own batch (rows are independent: weak
+scaling, no collective on the data path).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from synthetic_rollouts import WORKLOADS, rollout  # noqa: E402
+
+WORKLOAD = "all7_4096x128"
+METRIC = "env-steps/s and achieved HBM GB/s (% of 8 TB/s) at N=4096,T=128, 1×GB300"
+UNIT = "env-steps/s"
+ROTATING_SETS = 8
+NOMINAL_HBM_GBS = 8000.0
+
+# Per-estimator inputs (in launch order), outputs, and algorithmic bytes per
+# env-step (each input read once, each output written once; bootstrap [N]
+# counted separately).
+ESTIMATORS = {
+    "gae": (("rewards", "values", "terminateds"), ("out",)),
+    "lambda_returns": (("rewards", "values", "terminateds"), ("out",)),
+    "discounted_returns": (("rewards", "terminateds"), ("out",)),
+    "vtrace": (("rewards", "values", "log_rhos", "terminateds"), ("vs", "pg")),
+    "retrace": (("rewards", "values", "q_values", "log_rhos", "terminateds"), ("out",)),
+    "eligibility_traces": (("x", "terminateds"), ("out",)),
+    "episodic_prefix_sum": (("x_int", "terminateds"), ("out",)),
+}
+BACKWARD = ("gae", "lambda_returns", "discounted_returns", "vtrace", "retrace")
+
+
+def bytes_per_env_step(est):
+    ins, outs = ESTIMATORS[est]
+    return 4 * (len(ins) + len(outs))
+
+
+def bytes_per_launch(est, N, T):
+    return bytes_per_env_step(est) * N * T + (4 * N if est in BACKWARD else 0)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (torchrun)
+# ---------------------------------------------------------------------------
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world, backend):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(dist, value, device=None):
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_pass(oracle, src, rows, prm):
+    """All seven estimators over rows [r0, r1) of the batch (float64 oracle)."""
+    r0, r1 = rows
+    s = {k: (v[r0:r1] if v.ndim == 2 else v[r0:r1]) for k, v in src.items()}
+    g, lm = prm["gamma"], prm["lambda_"]
+    B = s["bootstrap_value"]
+    oracle.gae(s["rewards"], s["values"], s["terminateds"], g, lm, B)
+    oracle.lambda_returns(s["rewards"], s["values"], s["terminateds"], g, lm, B)
+    oracle.discounted_returns(s["rewards"], s["terminateds"], g, B)
+    oracle.vtrace(s["rewards"], s["values"], s["log_rhos"], s["terminateds"], g, lm,
+                  prm["rho_bar"], prm["c_bar"], B)
+    oracle.retrace(s["rewards"], s["values"], s["q_values"], s["log_rhos"], s["terminateds"],
+                   g, lm, prm["c_bar"], B)
+    oracle.eligibility_traces(s["x"], s["terminateds"], g, lm)
+    oracle.episodic_prefix_sum(s["x_int"], s["terminateds"])
+
+
+def oracle_step(oracle, src, nrows, prm, pool, threads):
+    """One oracle step over the first nrows rows, rows split across threads."""
+    bounds = np.linspace(0, nrows, threads + 1).astype(int)
+    jobs = [(int(a), int(b)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+    list(pool.map(lambda rg: oracle_pass(oracle, src, rg, prm), jobs))
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle(src, prm, budget_s=10.0):
+    """The oracle as it stands, on all host cores, for about budget_s seconds."""
+    import concurrent.futures as cf
+    import oracle
+    threads = cpu_threads()
+    N = src["rewards"].shape[0]
+    T = src["rewards"].shape[1]
+    with cf.ThreadPoolExecutor(threads) as pool:
+        oracle_step(oracle, src, N, prm, pool, threads)  # warm (loads the library)
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            oracle_step(oracle, src, N, prm, pool, threads)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s or reps >= 10000:
+                break
+    return {"value": reps * N * T / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "%d full %dx%d batches, all seven estimators, float64 C oracle, rows "
+                      "split over %d threads, %.1f s" % (reps, N, T, threads, el)}
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle, timed per step
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import concurrent.futures as cf
+    import oracle
+    w = WORKLOADS[WORKLOAD]
+    prm = dict(gamma=w.gamma, lambda_=w.lambda_, rho_bar=w.rho_bar, c_bar=w.c_bar)
+    src = rollout(w.N, w.T, w.seed, w.p_term)
+    threads = cpu_threads()
+    with cf.ThreadPoolExecutor(threads) as pool:
+        t0 = time.perf_counter()
+        oracle_step(oracle, src, w.N, prm, pool, threads)
+        full = time.perf_counter() - t0
+        budget = 150.0  # seconds for warmup + steps
+        nrows = w.N
+        if full * (args.steps + args.warmup) > budget:
+            nrows = max(threads, int(w.N * budget / (full * (args.steps + args.warmup))))
+        for _ in range(args.warmup):
+            oracle_step(oracle, src, nrows, prm, pool, threads)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            oracle_step(oracle, src, nrows, prm, pool, threads)
+        el = time.perf_counter() - t0
+    value = nrows * w.T * args.steps / el
+    sample = ("%d of %d rows x T=%d per step, all seven estimators, float64 C oracle on %d "
+              "threads" % (nrows, w.N, w.T, threads))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "num_envs": w.N, "seq_len": w.T, "estimators": 7,
+                   "rows_per_step": nrows},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def make_sets(torch, rl, src, dev, nsets):
+    """nsets independent device copies of every estimator's inputs and outputs."""
+    sets = []
+    for _ in range(nsets):
+        st = {}
+        for est, (ins, outs) in ESTIMATORS.items():
+            e = {k: torch.from_numpy(src[k]).to(dev) for k in ins}
+            e["bootstrap_value"] = torch.from_numpy(src["bootstrap_value"]).to(dev)
+            like = e[ins[0]]
+            for o in outs:
+                e[o] = torch.empty_like(like)
+            st[est] = e
+        sets.append(st)
+    return sets
+
+
+def launch(rl, est, e, prm):
+    g, lm = prm["gamma"], prm["lambda_"]
+    if est == "gae":
+        rl.rlcs_gae(e["rewards"], e["values"], e["terminateds"], g, lm, e["bootstrap_value"],
+                    out=e["out"])
+    elif est == "lambda_returns":
+        rl.rlcs_lambda_returns(e["rewards"], e["values"], e["terminateds"], g, lm,
+                               e["bootstrap_value"], out=e["out"])
+    elif est == "discounted_returns":
+        rl.rlcs_discounted_returns(e["rewards"], e["terminateds"], g, e["bootstrap_value"],
+                                   out=e["out"])
+    elif est == "vtrace":
+        rl.rlcs_vtrace(e["rewards"], e["values"], e["log_rhos"], e["terminateds"], g, lm,
+                       prm["rho_bar"], prm["c_bar"], e["bootstrap_value"], out=e["vs"],
+                       out_pg=e["pg"])
+    elif est == "retrace":
+        rl.rlcs_retrace(e["rewards"], e["values"], e["q_values"], e["log_rhos"],
+                        e["terminateds"], g, lm, prm["c_bar"], e["bootstrap_value"], out=e["out"])
+    elif est == "eligibility_traces":
+        rl.rlcs_eligibility_traces(e["x"], e["terminateds"], g, lm, out=e["out"])
+    elif est == "episodic_prefix_sum":
+        rl.rlcs_episodic_prefix_sum(e["x_int"], e["terminateds"], out=e["out"])
+
+
+def capture(torch, stream, fn):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    return g
+
+
+def time_graph(torch, stream, graph, reps):
+    """Seconds for `reps` replays; replay() launches on the current stream, so
+    the replays and both events go to `stream`."""
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    dist = init_dist(world, "nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import linear_recurrence_scan_affine_gb300 as rl
+
+    w = WORKLOADS[WORKLOAD]
+    N, T = w.N, w.T
+    prm = dict(gamma=w.gamma, lambda_=w.lambda_, rho_bar=w.rho_bar, c_bar=w.c_bar)
+    src = rollout(N, T, w.seed + rank, w.p_term)
+    sets = make_sets(torch, rl, src, dev, ROTATING_SETS)
+    footprint = sum(t.numel() * t.element_size() for st in sets for e in st.values()
+                    for t in e.values())
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    stream = torch.cuda.Stream(dev)
+    order = list(ESTIMATORS)
+
+    def step(i):
+        st = sets[i % ROTATING_SETS]
+        for est in order:
+            launch(rl, est, st[est], prm)
+
+    # eager warm-up on the capture stream: loads kernels, allocates workspaces
+    stream.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(stream):
+        for i in range(ROTATING_SETS):
+            step(i)
+    torch.cuda.synchronize()
+    rl.check_all_workspaces()
+
+    # one graph = BLOCK steps cycling through the rotating sets
+    BLOCK = 8 * ROTATING_SETS
+    block_graph = capture(torch, stream, lambda: [step(i) for i in range(BLOCK)])
+    K = max(args.steps, 1)
+    reps = (K + BLOCK - 1) // BLOCK
+    K = reps * BLOCK
+    wreps = max(1, (max(args.warmup, 3) + BLOCK - 1) // BLOCK)
+    with torch.cuda.stream(stream):
+        for _ in range(wreps):
+            block_graph.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ
+                           else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+    sampler.start()
+    time.sleep(0.3)  # let the sampler take its first reading
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t_start.record(stream)
+        for _ in range(reps):
+            block_graph.replay()
+        t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    elapsed = max_over_ranks(dist, elapsed, dev)
+    rl.check_all_workspaces()
+
+    step_bytes = sum(bytes_per_launch(e, N, T) for e in order)
+    value = world * N * T * K / elapsed
+    step_gbs = step_bytes * K / elapsed / 1e9
+
+    # every estimator alone: a graph of back-to-back launches, each on its own
+    # buffer set, with enough sets that the rotation spans >= 3x the L2
+    per_est = {}
+    for est in order:
+        per_est[est] = time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T)
+    dom = max(per_est, key=lambda e: per_est[e]["us_per_launch"])
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            peaks = json.load(fh)
+    except (OSError, ValueError):
+        pass
+    peak = peaks.get("hbm_gbs")
+    peak_src = "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    if not peak:
+        peak, peak_src = 6800.0, "fallback 6.8 TB/s"
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        with open(tr_path) as fh:
+            traffic = json.load(fh).get("%s_%dx%d" % (dom, N, T))
+    achieved = per_est[dom]["gbs"]
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
+                "traffic": traffic, "bytes_per_launch": bytes_per_launch(dom, N, T),
+                "us_per_launch": per_est[dom]["us_per_launch"],
+                "timing": "kernel alone: CUDA graph of back-to-back launches, each on its own "
+                          "buffer set (rotation >= 3x L2), CUDA events on the launching stream"}
+
+    e2e = run_e2e(torch, rl, src, dev, stream, prm, order, max(32, min(K, 512)), N, T)
+    e2e["value"] *= world
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = time_oracle(src, prm, budget_s=args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": wreps * BLOCK, "ms_per_step": 1e3 * elapsed / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "num_envs": N, "seq_len": T, "estimators": 7,
+                       "env_step": "one (env, t) element through all seven estimators",
+                       "bytes_per_step_algorithmic": step_bytes,
+                       "l2": "inputs larger than L2: %d rotating buffer sets, %.0f MB footprint "
+                             "= %.1fx L2" % (ROTATING_SETS, footprint / 1e6, footprint / l2),
+                       "launch": "CUDA graph of %d steps, one stream, programmatic dependent "
+                                 "launch" % BLOCK,
+                       "parallelism": "weak: each rank its own batch"},
+            "hbm_gbs": step_gbs, "hbm_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
+            "hbm_frac_of_measured": step_gbs / peak,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 7 * K, "clocks": clocks, "per_estimator": per_est,
+        }
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T, seconds=0.15):
+    ins, outs = ESTIMATORS[est]
+    set_bytes = bytes_per_launch(est, N, T)
+    nsets = int(min(256, max(8, -(-3 * l2 // set_bytes))))
+    sets = []
+    for _ in range(nsets):
+        e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + ("bootstrap_value",)}
+        for o in outs:
+            e[o] = torch.empty_like(e[ins[0]])
+        sets.append(e)
+    with torch.cuda.stream(stream):
+        for e in sets:
+            launch(rl, est, e, prm)
+    torch.cuda.synchronize()
+    g = capture(torch, stream, lambda: [launch(rl, est, e, prm) for e in sets])
+    with torch.cuda.stream(stream):
+        g.replay()
+    once = time_graph(torch, stream, g, 1)
+    reps = max(3, int(seconds / max(1e-6, once)))
+    sec = time_graph(torch, stream, g, reps) / (reps * nsets)
+    del g, sets
+    torch.cuda.synchronize()
+    return {"us_per_launch": sec * 1e6, "env_steps_per_s": N * T / sec,
+            "gbs": bytes_per_launch(est, N, T) / sec / 1e9,
+            "bytes_per_env_step": bytes_per_env_step(est), "rotating_sets": nsets,
+            "footprint_over_l2": nsets * set_bytes / l2}
+
+
+def run_e2e(torch, rl, src, dev, stream, prm, order, steps, N, T):
+    """Whole step through the public API from pinned host buffers: copy every
+    estimator's inputs in, run the seven kernels, copy every output back."""
+    host_in, dev_set = {}, {}
+    h2d = d2h = 0
+    for est in order:
+        ins, outs = ESTIMATORS[est]
+        e, h = {}, {}
+        for k in ins + ("bootstrap_value",):
+            h[k] = torch.from_numpy(src[k]).pin_memory()
+            e[k] = torch.empty_like(h[k], device=dev)
+            h2d += h[k].numel() * h[k].element_size()
+        for o in outs:
+            e[o] = torch.empty_like(e[ins[0]])
+            h[o] = torch.empty_like(h[ins[0]]).pin_memory()
+            d2h += h[o].numel() * h[o].element_size()
+        host_in[est], dev_set[est] = h, e
+
+    def step():
+        for est in order:
+            ins, outs = ESTIMATORS[est]
+            for k in ins + ("bootstrap_value",):
+                dev_set[est][k].copy_(host_in[est][k], non_blocking=True)
+        for est in order:
+            launch(rl, est, dev_set[est], prm)
+        for est in order:
+            for o in ESTIMATORS[est][1]:
+                host_in[est][o].copy_(dev_set[est][o], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    g = capture(torch, stream, step)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    sec = time_graph(torch, stream, g, steps) / steps
+    return {"value": N * T / sec, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": sec * 1e3,
+            "path": "pinned host -> device copies, seven rlcs_* calls, device -> pinned host "
+                    "copies, one CUDA graph per step"}
+
+
+def run_profile(args):
+    """Eager launches of one estimator on rotating buffer sets (no graphs, no
+    timing): a small, fixed launch sequence for ncu captures."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    import linear_recurrence_scan_affine_gb300 as rl
+    w = WORKLOADS[args.workload]
+    N = args.rows or w.N
+    prm = dict(gamma=w.gamma, lambda_=w.lambda_, rho_bar=w.rho_bar, c_bar=w.c_bar)
+    src = rollout(N, w.T, w.seed, w.p_term)
+    est = args.profile
+    nsets = max(2, min(ROTATING_SETS, args.sets))
+    sets = []
+    for _ in range(nsets):
+        ins, outs = ESTIMATORS[est]
+        e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + ("bootstrap_value",)}
+        for o in outs:
+            e[o] = torch.empty_like(e[ins[0]])
+        sets.append(e)
+    for i in range(args.warmup + args.steps):
+        launch(rl, est, sets[i % nsets], prm)
+    torch.cuda.synchronize()
+    rl.check_all_workspaces()
+    print(json.dumps({"profile": est, "workload": args.workload, "N": N, "T": w.T,
+                      "launches": args.warmup + args.steps,
+                      "bytes_per_launch": bytes_per_launch(est, N, w.T)}))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=256)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=tuple(ESTIMATORS), default=None,
+                    help="eager launches of one estimator only (for ncu)")
+    ap.add_argument("--workload", default=WORKLOAD, choices=tuple(WORKLOADS))
+    ap.add_argument("--rows", type=int, default=0, help="profile mode: rows (0 = workload's N)")
+    ap.add_argument("--sets", type=int, default=ROTATING_SETS)
+    args = ap.parse_args()
+    if args.profile:
+        return run_profile(args)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -74,6 +74,9 @@ def build(force=False, verbose=False, extra_flags=()):
 
 
 if __name__ == "__main__":
+    # python build.py [--force] [--ptxas] [-DNAME=VALUE ...]
     import sys
-    print(build(force="--force" in sys.argv, verbose=True,
-                extra_flags=["-Xptxas", "-v"] if "--ptxas" in sys.argv else []))
+    extra = [a for a in sys.argv[1:] if a.startswith("-D")]
+    if "--ptxas" in sys.argv:
+        extra += ["-Xptxas", "-v"]
+    print(build(force="--force" in sys.argv or bool(extra), verbose=True, extra_flags=extra))

@@ -26,7 +26,10 @@ namespace rlcs {
 constexpr int kStrip = 128;              // steps per warp strip
 constexpr int kChunkWarps = 8;           // warps per block in the chunk tier
 constexpr int kChunkThreads = kChunkWarps * 32;
-constexpr int kRowWarps = 4;             // rows (warps) per block, warp-row tier
+#ifndef RLCS_ROW_WARPS
+#define RLCS_ROW_WARPS 4
+#endif
+constexpr int kRowWarps = RLCS_ROW_WARPS;  // rows (warps) per block, warp-row tier
 constexpr uint64_t kWaitLimitNs = 1ull << 30;  // ~1.07 s bound on every wait
 
 // Workspace: a 64-byte header, then one 16-byte record per chunk ticket.
@@ -309,13 +312,21 @@ template <class E, bool TRUNC, int S>
 __global__ void __launch_bounds__(kRowWarps * 32) warp_row_kernel(Params p) {
   using St = Strips<E, TRUNC, S>;
   using V = typename St::V;
-  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5);
-  if (row >= p.N) return;  // whole warp leaves together
   const int64_t T = p.T;
   const int64_t base = row * T;
   const bool vec = p.vec != 0;
+  // Start this row's inputs streaming into L2 while the previous grid in the
+  // stream may still be running; the loads below come after the dependency
+  // wait and find them there.
+  if (vec && lane == 0 && row < p.N) {
+#pragma unroll
+    for (int k = 0; k < kNumSlots; ++k)
+      if (St::kUse & bit(k)) prefetch_l2(p.in[k] + base, (uint32_t)(T * 4));
+  }
+  pdl_wait();
+  if (row >= p.N) return;  // whole warp leaves together
 
   float4 raw[kNumSlots][S];
 #pragma unroll
@@ -461,10 +472,22 @@ __global__ void __launch_bounds__(kChunkThreads) block_chunk_kernel(Params p, Ch
   __shared__ uint32_t s_epoch;
   __shared__ int s_ok;
 
-  pdl_wait();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool vec = p.vec != 0;
   const int64_t T = p.T, Q = cs.chunks_per_row;
+  // L2 prefetch of the chunk this block will most likely get (tickets follow
+  // block order closely; exact when Q == 1), issued before the dependency
+  // wait so it overlaps the previous grid. A wrong guess only costs traffic.
+  if (vec && tid == 0) {
+    const int64_t g = blockIdx.x, grow = g / Q, gk = g - grow * Q;
+    const int64_t gq = E::kBackward ? (Q - 1 - gk) : gk;
+    const int64_t gt0 = gq * C;
+    const int64_t glen = (T - gt0 < C) ? (T - gt0) : C;
+#pragma unroll
+    for (int k = 0; k < kNumSlots; ++k)
+      if (kUse & bit(k)) prefetch_l2(p.in[k] + grow * T + gt0, (uint32_t)(glen * 4));
+  }
+  pdl_wait();
 
   if (tid == 0) {
     int64_t ticket = blockIdx.x;

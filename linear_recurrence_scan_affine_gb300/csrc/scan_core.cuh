@@ -173,6 +173,14 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
       : "memory");
 }
 
+// Bulk prefetch of [src, src+bytes) into L2 (no data returned to the thread).
+// src 16-byte aligned, bytes a multiple of 16. L2 is the device's point of
+// coherence, so prefetching a range that an earlier grid is still writing
+// can never yield stale data: later loads see whatever L2 holds by then.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Programmatic dependent launch: wait for the preceding grid in the stream
 // (and its memory) before touching global memory; let the next grid start
 // its launch early.

@@ -19,8 +19,8 @@ OK, INVALID, MISALIGNED, WORKSPACE, CUDA, TIMEOUT = 0, 1, 2, 3, 4, 5
 
 @pytest.fixture(scope="module")
 def lib():
-    from linear_recurrence_scan_affine_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     from linear_recurrence_scan_affine_gb300 import binding
     return binding.lib()
 
