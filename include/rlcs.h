@@ -197,6 +197,33 @@ rlcs_status rlcs_episodic_prefix_sum(const int32_t *x, const float *dones,
                                      void *workspace, size_t workspace_bytes,
                                      rlcs_stream_t stream);
 
+/* GAE for callers that cannot allocate device memory.
+ * The paper has no counterpart: this is a library convenience. Some callers
+ * cannot call cudaMalloc, such as a plugin inside a host program that owns
+ * every device allocation, or a real-time loop that forbids allocating after
+ * start-up; they cannot provide the workspace long rows need. This entry
+ * point takes the same arguments as rlcs_gae minus the workspace and gives
+ * the same results; long rows pass their carries through a fixed scratch
+ * array that the library keeps in device memory (64 + 16*65536 bytes, about
+ * 1 MiB, held on every GPU that loads the library until the process exits).
+ * It calls no allocation routine.
+ *  - Sizes: returns RLCS_ERR_WORKSPACE, launching nothing, when
+ *    N * ceil(T / 1024) > 65536, the array's capacity in chunk records
+ *    (the same count rlcs_workspace_bytes(N, T) is based on).
+ *  - Set-up: the first call on each device looks up the array's device
+ *    address and zeroes it, synchronously; make that first call before any
+ *    CUDA stream capture.
+ *  - Sharing: every call on a device uses the same array and leaves its
+ *    contents behind, so calls that can overlap on the GPU (other streams,
+ *    other threads) race; the caller must serialise them. Device-side wait
+ *    timeouts are recorded in the array, where rlcs_check_status cannot see
+ *    them. */
+rlcs_status rlcs_gae_noalloc(const float *rewards, const float *values,
+                             const float *terminateds, const float *truncateds,
+                             const float *next_values, const float *bootstrap_value,
+                             float *advantages, int64_t N, int64_t T, float gamma,
+                             float lambda, rlcs_stream_t stream);
+
 /* Launch-shape selection, exposed for testing and tuning. The library picks
  * one of three shapes from (N, T): RLCS_SHAPE_WARP_ROW (one warp per row,
  * T <= 512), RLCS_SHAPE_BLOCK_CHUNK (a thread block per row chunk, carries

@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "launch.cuh"
 
@@ -322,3 +323,72 @@ rlcs_status rlcs_episodic_prefix_sum(const int32_t *x, const float *dones, int32
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// GAE for callers that cannot allocate device memory.
+//
+// Some callers have no way to call cudaMalloc: a plugin inside a host
+// program that owns every device allocation, or a real-time loop that
+// forbids allocating after start-up. They cannot provide the workspace that
+// long rows need, so here the look-back scratch lives in a fixed array of
+// device memory that belongs to this library: a 64-byte header plus 65536
+// chunk records of 16 bytes (about 1 MiB), held on every GPU that loads the
+// library until the process exits.
+// ---------------------------------------------------------------------------
+namespace rlcs {
+namespace {
+
+constexpr int64_t kNoAllocRecords = 65536;
+constexpr size_t kNoAllocBytes = sizeof(WsHeader) + sizeof(WsRecord) * kNoAllocRecords;
+
+// Device memory. In host code this name is only a stand-in for the symbol;
+// the array's device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices];  // device address of the array, per device
+
+// Once per device, with that device current: look up the array's device
+// address and zero it. The header's ticket and done counters must start at
+// zero; every call leaves them at zero again when it finishes.
+rlcs_status noalloc_scratch(void **out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return RLCS_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return RLCS_ERR_CUDA;
+    }
+    if (cudaMemset(p, 0, kNoAllocBytes) != cudaSuccess ||
+        cudaStreamSynchronize(nullptr) != cudaSuccess) {
+      cudaGetLastError();
+      return RLCS_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return RLCS_OK;
+}
+
+}  // namespace
+}  // namespace rlcs
+
+extern "C" rlcs_status rlcs_gae_noalloc(const float *rewards, const float *values,
+                                        const float *terminateds, const float *truncateds,
+                                        const float *next_values, const float *bootstrap_value,
+                                        float *advantages, int64_t N, int64_t T, float gamma,
+                                        float lambda, rlcs_stream_t stream) {
+  if (!rewards || !values || !terminateds || !advantages || N <= 0 || T <= 0)
+    return RLCS_ERR_INVALID_ARG;
+  if (rlcs_workspace_bytes(N, T) > kNoAllocBytes) return RLCS_ERR_WORKSPACE;
+  void *scratch = nullptr;
+  const rlcs_status st = noalloc_scratch(&scratch);
+  if (st != RLCS_OK) return st;
+  return rlcs_gae(rewards, values, terminateds, truncateds, next_values, bootstrap_value,
+                  advantages, N, T, gamma, lambda, scratch, kNoAllocBytes, stream);
+}
