@@ -441,6 +441,23 @@ def run_ours(args):
                 "timing": "kernel alone: CUDA graph of back-to-back launches, each on its own "
                           "buffer set (rotation >= 3x L2), CUDA events on the launching stream"}
 
+    # the long-row recipes, every estimator alone (same method as above)
+    long_t = {}
+    if not args.no_long_t:
+        for name in ("longT_256x1024", "longT_256x4096", "longT_256x16384", "vlong_8x131072"):
+            wl = WORKLOADS[name]
+            prm_l = dict(gamma=wl.gamma, lambda_=wl.lambda_, rho_bar=wl.rho_bar, c_bar=wl.c_bar)
+            src_l = rollout(wl.N, wl.T, wl.seed, wl.p_term)
+            res = {}
+            for est in wl.estimators:
+                r_ = time_alone(torch, rl, est, src_l, dev, stream, prm_l, l2, wl.N, wl.T,
+                                seconds=0.08)
+                r_["frac_of_measured_hbm"] = r_["gbs"] * 1e9 / (peak * 1e9)
+                res[est] = r_
+            long_t[name] = res
+            del src_l
+        rl.check_all_workspaces()
+
     e2e = run_e2e(torch, rl, src, dev, stream, prm, order, max(32, min(K, 512)), N, T)
     e2e["value"] *= world
 
@@ -470,6 +487,7 @@ def run_ours(args):
             "hbm_frac_of_measured": step_gbs / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 7 * K, "clocks": clocks, "per_estimator": per_est,
+            "long_t_sweep": long_t,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -587,6 +605,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-long-t", action="store_true", help="skip the long-row sweep")
     ap.add_argument("--profile", choices=tuple(ESTIMATORS), default=None,
                     help="eager launches of one estimator only (for ncu)")
     ap.add_argument("--workload", default=WORKLOAD, choices=tuple(WORKLOADS))

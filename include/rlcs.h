@@ -79,7 +79,7 @@ typedef enum {
 } rlcs_status;
 
 /* Bytes of workspace any entry point needs for an [N, T] call: a small
- * header plus 16 bytes per possible row chunk. Depends only on N and T.
+ * header plus 32 bytes per possible row chunk. Depends only on N and T.
  * Returns 0 if N <= 0 or T <= 0. */
 size_t rlcs_workspace_bytes(int64_t N, int64_t T);
 
@@ -204,8 +204,8 @@ rlcs_status rlcs_episodic_prefix_sum(const int32_t *x, const float *dones,
  * start-up; they cannot provide the workspace long rows need. This entry
  * point takes the same arguments as rlcs_gae minus the workspace and gives
  * the same results; long rows pass their carries through a fixed scratch
- * array that the library keeps in device memory (64 + 16*65536 bytes, about
- * 1 MiB, held on every GPU that loads the library until the process exits).
+ * array that the library keeps in device memory (64 + 32*65536 bytes, about
+ * 2 MiB, held on every GPU that loads the library until the process exits).
  * It calls no allocation routine.
  *  - Sizes: returns RLCS_ERR_WORKSPACE, launching nothing, when
  *    N * ceil(T / 1024) > 65536, the array's capacity in chunk records
@@ -225,17 +225,24 @@ rlcs_status rlcs_gae_noalloc(const float *rewards, const float *values,
                              float lambda, rlcs_stream_t stream);
 
 /* Launch-shape selection, exposed for testing and tuning. The library picks
- * one of three shapes from (N, T): RLCS_SHAPE_WARP_ROW (one warp per row,
- * T <= 512), RLCS_SHAPE_BLOCK_CHUNK (a thread block per row chunk, carries
- * between chunks by decoupled look-back through the workspace). Setting an
- * override forces a shape and a chunk length (a multiple of 512 up to 4096)
+ * a shape from (N, T) and the SM count:
+ *   RLCS_SHAPE_WARP_ROW    one warp per row, inputs in registers (T <= 512);
+ *   RLCS_SHAPE_BLOCK_TILE  one 256-thread block per row tile, inputs loaded
+ *                          into registers, tiles of a row chained by
+ *                          decoupled look-back through the workspace;
+ *   RLCS_SHAPE_BLOCK_CHUNK one 256-thread block per row chunk, the chunk
+ *                          staged into shared memory by bulk copy (TMA),
+ *                          chunks chained by decoupled look-back.
+ * Setting an override forces a shape and, for the two block shapes, a tile
+ * or chunk length of 1024, 2048 or 4096 steps (0 lets the library choose),
  * for every later call in this process until reset with RLCS_SHAPE_AUTO.
  * Not thread-safe with concurrent calls. Returns RLCS_ERR_INVALID_ARG for an
- * unknown shape or chunk length. */
+ * unknown shape or length. */
 typedef enum {
   RLCS_SHAPE_AUTO = 0,
   RLCS_SHAPE_WARP_ROW = 1,
-  RLCS_SHAPE_BLOCK_CHUNK = 2
+  RLCS_SHAPE_BLOCK_CHUNK = 2,
+  RLCS_SHAPE_BLOCK_TILE = 3
 } rlcs_shape;
 rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk);
 

@@ -8,7 +8,7 @@ package is a thin ctypes binding with the same names. Importing it loads
 ``librlcs.so`` and fails loudly if the library has not been built.
 """
 from .binding import (  # noqa: F401
-    RLCS_SHAPE_AUTO, RLCS_SHAPE_BLOCK_CHUNK, RLCS_SHAPE_WARP_ROW, RlcsError,
+    RLCS_SHAPE_AUTO, RLCS_SHAPE_BLOCK_CHUNK, RLCS_SHAPE_BLOCK_TILE, RLCS_SHAPE_WARP_ROW, RlcsError,
     check_all_workspaces, lib, rlcs_check_status, rlcs_discounted_returns,
     rlcs_eligibility_traces, rlcs_episodic_prefix_sum, rlcs_gae, rlcs_lambda_returns,
     rlcs_retrace, rlcs_set_shape_override, rlcs_vtrace, rlcs_workspace_bytes,

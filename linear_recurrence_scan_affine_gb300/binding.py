@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "librlcs.so")
 
 RLCS_OK = 0
-RLCS_SHAPE_AUTO, RLCS_SHAPE_WARP_ROW, RLCS_SHAPE_BLOCK_CHUNK = 0, 1, 2
+RLCS_SHAPE_AUTO, RLCS_SHAPE_WARP_ROW, RLCS_SHAPE_BLOCK_CHUNK, RLCS_SHAPE_BLOCK_TILE = 0, 1, 2, 3
 
 
 class RlcsError(RuntimeError):

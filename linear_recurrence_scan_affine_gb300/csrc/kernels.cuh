@@ -32,7 +32,7 @@ constexpr int kChunkThreads = kChunkWarps * 32;
 constexpr int kRowWarps = RLCS_ROW_WARPS;  // rows (warps) per block, warp-row tier
 constexpr uint64_t kWaitLimitNs = 1ull << 30;  // ~1.07 s bound on every wait
 
-// Workspace: a 64-byte header, then one 16-byte record per chunk ticket.
+// Workspace: a 64-byte header, then one 32-byte record per chunk.
 struct WsHeader {
   uint32_t epoch;   // bumped by the last block of every chunked launch
   uint32_t ticket;  // next chunk ticket
@@ -40,14 +40,24 @@ struct WsHeader {
   uint32_t status;  // sticky device-side error (an rlcs_status code)
   uint32_t pad[12];
 };
+// A chunk record holds self-validating 64-bit words, each
+// (tag << 32) | payload with tag = (epoch tag << 2) | state: the aggregate
+// pair (m, c) in two words of state 1, the inclusive value in one word of
+// state 2. Each word is written and read with one strong 64-bit access,
+// which is single-copy atomic, so a reader that sees a matching tag has that
+// word's payload whole. No fence orders the words, and none is needed: the
+// aggregate counts only when both of its words carry the current tag.
 struct WsRecord {
-  uint32_t flag;  // (epoch tag << 2) | state
-  uint32_t m;     // chunk aggregate pair, raw bits
-  uint32_t c;
-  uint32_t inc;   // inclusive value (value at the chunk's far end), raw bits
+  uint64_t m;    // aggregate multiplier bits, state 1
+  uint64_t c;    // aggregate addend bits, state 1
+  uint64_t inc;  // inclusive value bits (value at the chunk's far end), state 2
+  uint64_t pad;
 };
-static_assert(sizeof(WsHeader) == 64 && sizeof(WsRecord) == 16, "workspace layout");
+static_assert(sizeof(WsHeader) == 64 && sizeof(WsRecord) == 32, "workspace layout");
 constexpr uint32_t kStateAgg = 1u, kStateInc = 2u;
+__device__ __forceinline__ uint64_t tagged(uint32_t tag, uint32_t payload) {
+  return ((uint64_t)tag << 32) | payload;
+}
 constexpr uint32_t kTagMask = 0x3fffffffu;
 constexpr uint32_t kStatusWorkspace = 3u, kStatusTimeout = 5u;
 
@@ -185,6 +195,11 @@ struct Strips {
   template <class Src>
   __device__ __forceinline__ void build(const Params &p, const Src &src, float boot,
                                         int64_t t_span, int64_t T, int lane) {
+    // Per-element bounds in 32-bit offsets from the span start: steps left in
+    // the row (clamped; a span is at most a few thousand steps long).
+    const int64_t left = T - t_span;
+    const int rem = left > (int64_t)(1 << 30) ? (1 << 30) : (int)left;
+    const bool at_origin = (t_span == 0);
 #pragma unroll
     for (int j = 0; j < S; ++j) {
       float4 raw[kNumSlots], nx[kNumSlots];
@@ -196,10 +211,10 @@ struct Strips {
                                                       : f4zero();
       float4 dp = f4zero();
       if (!E::kBackward) dp = prev4(raw[kD], src.preceding_d(j), lane);
-      const int64_t t0 = t_span + (int64_t)j * kStrip + 4 * lane;
+      const int o0 = j * kStrip + 4 * lane;  // offset of the lane's run in the span
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int64_t t = t0 + i;
+        const int o = o0 + i;
         StepIn s;
         s.r = f4get(raw[kR], i);
         s.v = f4get(raw[kV], i);
@@ -212,12 +227,12 @@ struct Strips {
         s.qn = f4get(nx[kQ], i);
         s.lrn = f4get(nx[kLR], i);
         s.dp = f4get(dp, i);
-        s.last = (t == T - 1);
-        s.first = (t == 0);
+        s.last = (o == rem - 1);
+        s.first = at_origin && (o == 0);
         float a0 = 0.f, a1 = 0.f;
         P e;
         E::template coeff<TRUNC>(p, s, boot, e, a0, a1);
-        if (t >= T) e = identity(P{});  // ragged tail: padding is the identity
+        if (o >= rem) e = identity(P{});  // ragged tail: padding is the identity
         el[j][i] = e;
         aux0[j][i] = a0;
         aux1[j][i] = a1;
@@ -361,8 +376,9 @@ __global__ void __launch_bounds__(kRowWarps * 32) warp_row_kernel(Params p) {
 // ---------------------------------------------------------------------------
 // Block-chunk tier
 // ---------------------------------------------------------------------------
+// Sticky device-side status: the highest code recorded wins.
 __device__ __forceinline__ void set_status(WsHeader *ws, uint32_t code) {
-  if (ws != nullptr) atomicCAS(&ws->status, 0u, code);
+  if (ws != nullptr) atomicMax(&ws->status, code);
 }
 
 // Bounded wait on phase 0 of the block's mbarrier. False on timeout.
@@ -375,84 +391,100 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar) {
   return true;
 }
 
-// Decoupled look-back for the chunk with ticket `ticket` (warp-wide call).
-// Publishes the chunk aggregate, walks predecessor tickets (nearer first, 32
-// per round) until one holds an inclusive value, composes the aggregates in
-// between, publishes this chunk's inclusive value and returns the value just
-// outside the chunk on its scan-origin side. Every wait is bounded; on
-// timeout the status word records RLCS_ERR_TIMEOUT and missing aggregates
-// count as the identity, so the launch always finishes.
+// Decoupled look-back (warp-wide call) for the chunk whose record is
+// `self`. Its predecessors in scan order are the records self - j*stride for
+// j = 1..npred (nearest first). Publishes the chunk aggregate, walks the
+// predecessors 32 per round until one holds an inclusive value, composes the
+// aggregates in between, publishes this chunk's inclusive value and returns
+// the value just outside the chunk on its scan-origin side. Every wait is
+// bounded; on timeout the status word records RLCS_ERR_TIMEOUT and missing
+// aggregates count as the identity, so the launch always finishes.
 template <class P, class V>
-__device__ V lookback(WsHeader *ws, int64_t ticket, int64_t row_first, P agg, uint32_t tag,
-                      int lane) {
+__device__ V lookback(WsHeader *ws, int64_t self, int64_t stride, int64_t npred, P agg,
+                      uint32_t tag, int lane) {
   WsRecord *rec = reinterpret_cast<WsRecord *>(ws + 1);
-  if (ticket == row_first) {  // the row's scan origin: nothing before it
-    if (lane == 0) {
-      __stcg(&rec[ticket].m, vbits(agg.m));
-      __stcg(&rec[ticket].c, vbits(agg.c));
-      __stcg(&rec[ticket].inc, vbits(apply(agg, V(0))));
-      st_release_gpu(&rec[ticket].flag, (tag << 2) | kStateInc);
-    }
+  const uint32_t tagA = (tag << 2) | kStateAgg, tagP = (tag << 2) | kStateInc;
+  if (npred == 0) {  // the row's scan origin: nothing before it
+    if (lane == 0) st_relaxed_gpu_u64(&rec[self].inc, tagged(tagP, vbits(apply(agg, V(0)))));
     return V(0);
   }
   if (lane == 0) {
-    __stcg(&rec[ticket].m, vbits(agg.m));
-    __stcg(&rec[ticket].c, vbits(agg.c));
-    st_release_gpu(&rec[ticket].flag, (tag << 2) | kStateAgg);
+    st_relaxed_gpu_u64(&rec[self].m, tagged(tagA, vbits(agg.m)));
+    st_relaxed_gpu_u64(&rec[self].c, tagged(tagA, vbits(agg.c)));
   }
   P acc = identity(P{});
   V X = V(0);
   bool timed_out = false;
-  int64_t look = ticket - 1;
+  int64_t d0 = 0;  // distance already walked
   while (true) {
-    const int64_t tk = look - lane;
-    const bool valid = tk >= row_first;
-    uint32_t f = 0;
+    const int64_t dist = d0 + lane + 1;
+    const bool valid = dist <= npred;
+    const int64_t tk = self - dist * stride;
+    uint64_t wm = 0, wc = 0, wi = 0;
+    bool isP = false, isA = false;
     uint64_t start = 0;
+    unsigned backoff = 64;
     while (true) {
-      if (valid) f = ld_acquire_gpu(&rec[tk].flag);
-      const bool ready = !valid || (((f >> 2) == tag) && (f & 3u) != 0u);
-      if (__all_sync(kFull, ready)) break;
+      if (valid) {
+        wi = ld_relaxed_gpu_u64(&rec[tk].inc);
+        wm = ld_relaxed_gpu_u64(&rec[tk].m);
+        wc = ld_relaxed_gpu_u64(&rec[tk].c);
+        isP = (uint32_t)(wi >> 32) == tagP;
+        isA = (uint32_t)(wm >> 32) == tagA && (uint32_t)(wc >> 32) == tagA;
+      }
+      if (__all_sync(kFull, !valid || isP || isA)) break;
       const uint64_t now = globaltimer_ns();
       if (start == 0) start = now;
       if (__any_sync(kFull, now - start > kWaitLimitNs)) {
         timed_out = true;
         break;
       }
-      __nanosleep(40);
+      __nanosleep(backoff);  // back off so a waiting warp leaves issue slots to others
+      if (backoff < 1024) backoff <<= 1;
     }
-    const bool ready = valid && ((f >> 2) == tag) && (f & 3u) != 0u;
-    const unsigned pm = __ballot_sync(kFull, ready && (f & 3u) == kStateInc);
+    const unsigned pm = __ballot_sync(kFull, valid && isP);
     const int firstP = pm ? __ffs(pm) - 1 : 32;
     P mine = identity(P{});
-    uint32_t inc_bits = 0;
-    if (ready && lane < firstP) {
-      vfrom(__ldcg(&rec[tk].m), mine.m);
-      vfrom(__ldcg(&rec[tk].c), mine.c);
+    if (valid && isA && lane < firstP) {
+      vfrom((uint32_t)wm, mine.m);
+      vfrom((uint32_t)wc, mine.c);
     }
-    if (lane == firstP) inc_bits = __ldcg(&rec[tk].inc);
     P win = warp_reduce_outer_first(mine);
     win = shfl_idx(win, 0);
     acc = compose(acc, win);
     if (pm) {
       V incv;
-      vfrom(__shfl_sync(kFull, inc_bits, firstP), incv);
+      vfrom(__shfl_sync(kFull, (uint32_t)wi, firstP), incv);
       X = apply(acc, incv);
       break;
     }
-    if (timed_out || look - 32 < row_first) {  // only reachable after a timeout
+    if (timed_out || d0 + 32 >= npred) {  // only reachable after a timeout
       X = apply(acc, V(0));
       timed_out = true;
       break;
     }
-    look -= 32;
+    d0 += 32;
   }
   if (lane == 0) {
     if (timed_out) set_status(ws, kStatusTimeout);
-    __stcg(&rec[ticket].inc, vbits(apply(agg, X)));
-    st_release_gpu(&rec[ticket].flag, (tag << 2) | kStateInc);
+    st_relaxed_gpu_u64(&rec[self].inc, tagged(tagP, vbits(apply(agg, X))));
   }
   return X;
+}
+
+// Marks the launch's block as finished; the last block of the launch resets
+// the counters and moves the workspace to the next epoch, so the next call
+// ignores every flag this one wrote.
+// Called by one thread per block after the block's last use of the
+// workspace (its epoch read and look-back are complete by then).
+__device__ __forceinline__ void finish_launch(WsHeader *ws, int64_t total, uint32_t epoch) {
+  const uint32_t prev = atomicAdd(&ws->done, 1u);
+  if (prev == (uint32_t)(total - 1)) {
+    ws->ticket = 0u;
+    ws->done = 0u;
+    __threadfence();
+    ws->epoch = epoch + 1u;
+  }
 }
 
 template <class E, bool TRUNC, int S>
@@ -495,14 +527,12 @@ __global__ void __launch_bounds__(kChunkThreads) block_chunk_kernel(Params p, Ch
     int ok = 1;
     if (Q > 1) {
       ticket = atomicAdd(&cs.ws->ticket, 1u);
-      epoch = ld_relaxed_gpu(&cs.ws->epoch);
       if (ticket >= cs.total_chunks) {
         set_status(cs.ws, kStatusWorkspace);
         ok = 0;
       }
     }
     s_ticket = ticket;
-    s_epoch = epoch;
     s_ok = ok;
     if (ok && vec) {
       const int64_t row = ticket / Q, kk = ticket - row * Q;
@@ -522,6 +552,8 @@ __global__ void __launch_bounds__(kChunkThreads) block_chunk_kernel(Params p, Ch
         }
       }
     }
+    if (ok && Q > 1) epoch = ld_relaxed_gpu(&cs.ws->epoch);  // after the copies are issued
+    s_epoch = epoch;
   }
   __syncthreads();
   if (!s_ok) return;  // uniform: a corrupted workspace handed out a bad ticket
@@ -597,17 +629,7 @@ __global__ void __launch_bounds__(kChunkThreads) block_chunk_kernel(Params p, Ch
     V X = V(0);
     if (Q > 1) {
       const uint32_t epoch = s_epoch;
-      X = lookback<P, V>(cs.ws, ticket, row * Q, chunk_agg, epoch & kTagMask, lane);
-      if (lane == 0) {
-        __threadfence();
-        const uint32_t prev = atomicAdd(&cs.ws->done, 1u);
-        if (prev == (uint32_t)(cs.total_chunks - 1)) {  // last block of the launch
-          cs.ws->ticket = 0u;
-          cs.ws->done = 0u;
-          __threadfence();
-          cs.ws->epoch = epoch + 1u;
-        }
-      }
+      X = lookback<P, V>(cs.ws, ticket, 1, kk, chunk_agg, epoch & kTagMask, lane);
     }
     if (lane < kChunkWarps) s_carry[lane] = apply(nb, X);
   }
@@ -623,6 +645,129 @@ __global__ void __launch_bounds__(kChunkThreads) block_chunk_kernel(Params p, Ch
       if (p.out1) store4(p.out1 + base, t, T, vec, o1[j]);
     }
   }
+  if (Q > 1 && tid == 0) finish_launch(cs.ws, cs.total_chunks, s_epoch);
+}
+
+// ---------------------------------------------------------------------------
+// Block-tile tier: one 256-thread block per row tile of 1024*S steps, inputs
+// loaded straight into registers (each warp its own span of S strips, like
+// the warp-row tier), warp aggregates composed in shared memory, tiles of a
+// row chained by decoupled look-back. No shared-memory staging and low
+// register use keep several blocks resident per SM, so one block's look-back
+// wait overlaps other blocks' loads.
+//
+// Tile order: block b handles tile round r = b / N of row b % N (row-
+// interleaved), at position q = r (forward) or Q-1-r (backward) along the
+// row. A tile's predecessor in its row is block b - N: issued N blocks
+// earlier, so with many rows its inclusive value is usually published before
+// it is needed. Blocks are dispatched in index order, so every block a tile
+// waits for has already been scheduled; the waits are bounded all the same.
+// The bulk L2 prefetch of the tile is issued before the grid-dependency wait.
+// ---------------------------------------------------------------------------
+struct TileShape {
+  WsHeader *ws;           // workspace (records indexed by block); NULL when Q == 1
+  int64_t tiles_per_row;  // Q
+  int64_t total_tiles;    // N * Q = grid size
+};
+
+// Resident blocks per SM the compiler must allow: 4096-step tiles keep more
+// state per thread and are used when the whole grid fits in about one wave
+// (2 per SM); shorter tiles are capped at 64 registers so 4 blocks share an
+// SM and one block's look-back overlaps the others' loads.
+template <int S> struct TileMinBlocks { static constexpr int value = S >= 4 ? 2 : 4; };
+
+template <class E, bool TRUNC, int S>
+__global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
+    block_tile_kernel(Params p, TileShape ts) {
+  using St = Strips<E, TRUNC, S>;
+  using P = typename St::P;
+  using V = typename St::V;
+  constexpr int C = kChunkWarps * kStrip * S;  // steps per tile
+  constexpr uint32_t kUse = St::kUse;
+
+  __shared__ P s_warp[kChunkWarps];
+  __shared__ V s_carry[kChunkWarps];
+  __shared__ uint32_t s_epoch;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool vec = p.vec != 0;
+  const int64_t N = p.N, T = p.T, Q = ts.tiles_per_row;
+  const int64_t b = blockIdx.x;
+  const int64_t r = b / N, row = b - r * N;
+  const int64_t q = E::kBackward ? (Q - 1 - r) : r;
+  const int64_t t0 = q * C;
+  const int64_t base = row * T;
+  const int span_off = warp * kStrip * S;
+  if (vec && tid == 0) {
+    const int64_t len = (T - t0 < C) ? (T - t0) : C;
+#pragma unroll
+    for (int k = 0; k < kNumSlots; ++k)
+      if (kUse & bit(k)) prefetch_l2(p.in[k] + base + t0, (uint32_t)(len * 4));
+  }
+  pdl_wait();
+
+  const int64_t t_span = t0 + span_off;
+  float4 raw[kNumSlots][S];
+#pragma unroll
+  for (int k = 0; k < kNumSlots; ++k) {
+#pragma unroll
+    for (int j = 0; j < S; ++j)
+      raw[k][j] = (kUse & bit(k)) ? load4(p.in[k] + base, t_span + (int64_t)j * kStrip + 4 * lane,
+                                          T, vec)
+                                  : f4zero();
+  }
+  float halo[kNumSlots];
+#pragma unroll
+  for (int k = 0; k < kNumSlots; ++k) {
+    const int64_t th = t_span + (int64_t)kStrip * S;  // first step after the span
+    halo[k] = (E::kBackward && (E::kNext & bit(k)) && th < T) ? __ldg(p.in[k] + base + th) : 0.f;
+  }
+  const float halo_d = (!E::kBackward && t_span > 0) ? __ldg(p.in[kD] + base + t_span - 1) : 0.f;
+  const float boot = (E::kBackward && p.boot) ? __ldg(p.boot + row) : 0.f;
+  if (tid == 0 && Q > 1) s_epoch = ld_relaxed_gpu(&ts.ws->epoch);  // after the loads issue
+  pdl_launch_dependents();
+
+  const RegSource<S> src{raw, halo, halo_d, lane};
+  St st;
+  st.build(p, src, boot, t_span, T, lane);
+  const P wagg = st.scan(lane);
+  if (lane == 0) s_warp[warp] = wagg;
+  __syncthreads();
+
+  if (warp == 0) {
+    const P w = (lane < kChunkWarps) ? s_warp[lane] : identity(P{});
+    P inc, nb, tile_agg;
+    if (E::kBackward) {
+      inc = warp_suffix_scan(w, lane);
+      tile_agg = shfl_idx(inc, 0);
+      const P x = shfl_down(inc, 1);
+      nb = (lane >= kChunkWarps - 1) ? identity(P{}) : x;
+    } else {
+      inc = warp_prefix_scan(w, lane);
+      tile_agg = shfl_idx(inc, kChunkWarps - 1);
+      const P x = shfl_up(inc, 1);
+      nb = (lane == 0) ? identity(P{}) : x;
+    }
+    V X = V(0);
+    if (Q > 1) {
+      const uint32_t epoch = s_epoch;
+      X = lookback<P, V>(ts.ws, b, N, r, tile_agg, epoch & kTagMask, lane);
+    }
+    if (lane < kChunkWarps) s_carry[lane] = apply(nb, X);
+  }
+  __syncthreads();
+
+  float4 o0[S], o1[S];
+  st.finish(s_carry[warp], o0, o1);
+#pragma unroll
+  for (int j = 0; j < S; ++j) {
+    const int64_t t = t_span + (int64_t)j * kStrip + 4 * lane;
+    store4(static_cast<float *>(p.out0) + base, t, T, vec, o0[j]);
+    if constexpr (E::kOuts > 1) {
+      if (p.out1) store4(p.out1 + base, t, T, vec, o1[j]);
+    }
+  }
+  if (Q > 1 && tid == 0) finish_launch(ts.ws, ts.total_tiles, s_epoch);
 }
 
 }  // namespace rlcs

@@ -9,7 +9,7 @@
 namespace rlcs {
 
 struct Plan {
-  int shape;       // RLCS_SHAPE_WARP_ROW or RLCS_SHAPE_BLOCK_CHUNK
+  int shape;       // RLCS_SHAPE_WARP_ROW, RLCS_SHAPE_BLOCK_CHUNK or RLCS_SHAPE_BLOCK_TILE
   int S;           // strips per warp: 1, 2 or 4
   int64_t Q;       // chunks per row (block-chunk shape)
   bool trunc;      // truncation inputs present
@@ -37,6 +37,11 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
   if (plan.shape == RLCS_SHAPE_WARP_ROW) {
     const dim3 grid((unsigned)((p.N + kRowWarps - 1) / kRowWarps));
     return launch_ex(warp_row_kernel<E, TRUNC, S>, grid, dim3(kRowWarps * 32), 0, s, plan.pdl, p);
+  }
+  if (plan.shape == RLCS_SHAPE_BLOCK_TILE) {
+    TileShape ts{plan.Q > 1 ? ws : nullptr, plan.Q, p.N * plan.Q};
+    return launch_ex(block_tile_kernel<E, TRUNC, S>, dim3((unsigned)(p.N * plan.Q)),
+                     dim3(kChunkThreads), 0, s, plan.pdl, p, ts);
   }
   constexpr uint32_t kUse = Strips<E, TRUNC, S>::kUse;
   constexpr size_t smem = (size_t)__builtin_popcount(kUse) * kChunkWarps * kStrip * S * 4;

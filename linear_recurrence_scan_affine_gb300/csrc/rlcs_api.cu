@@ -32,6 +32,17 @@ int sm_count() {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Tile/chunk length for rows longer than the warp-row limit (measured on
+// GB300): 4096 steps while the whole grid fits in about two blocks per SM,
+// where fewer and larger tiles shorten the chain of look-backs; 2048 steps
+// for larger grids, where more resident blocks overlap better; 1024 only for
+// rows that need no more.
+int64_t pick_chunk(int64_t N, int64_t T) {
+  if (T <= 1024) return 1024;
+  if (N * ceil_div(T, 4096) <= 2 * (int64_t)sm_count()) return 4096;
+  return 2048;
+}
+
 // Choose the launch shape for an [N, T] call.
 rlcs_status plan_call(int64_t N, int64_t T, bool trunc, Plan &plan) {
   plan = Plan{};
@@ -45,15 +56,9 @@ rlcs_status plan_call(int64_t N, int64_t T, bool trunc, Plan &plan) {
     plan.Q = 1;
     return RLCS_OK;
   }
-  plan.shape = RLCS_SHAPE_BLOCK_CHUNK;
+  plan.shape = (ov == RLCS_SHAPE_BLOCK_CHUNK) ? RLCS_SHAPE_BLOCK_CHUNK : RLCS_SHAPE_BLOCK_TILE;
   int64_t chunk = g_override_chunk.load(std::memory_order_relaxed);
-  if (ov != RLCS_SHAPE_BLOCK_CHUNK || chunk == 0) {
-    // Largest chunk that still gives every SM a few blocks to overlap.
-    const int64_t want_blocks = 4 * (int64_t)sm_count();
-    chunk = 4096;
-    while (chunk > kMinChunk && N * ceil_div(T, chunk) < want_blocks) chunk /= 2;
-    while (chunk > kMinChunk && chunk / 2 >= T) chunk /= 2;
-  }
+  if (ov == RLCS_SHAPE_AUTO || chunk == 0) chunk = pick_chunk(N, T);
   plan.S = (int)(chunk / kMinChunk);
   plan.Q = ceil_div(T, chunk);
   return RLCS_OK;
@@ -105,7 +110,7 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
   const rlcs_status st = plan_call(N, T, trunc != nullptr, plan);
   if (st != RLCS_OK) return st;
   WsHeader *wsh = nullptr;
-  if (plan.shape == RLCS_SHAPE_BLOCK_CHUNK) {
+  if (plan.shape != RLCS_SHAPE_WARP_ROW) {
     if (N * plan.Q >= (int64_t)UINT32_MAX) return RLCS_ERR_INVALID_ARG;
     if (plan.Q > 1) {
       if (!ws || ws_bytes < ws_bytes_for(N, plan.Q) || !aligned16(ws)) return RLCS_ERR_WORKSPACE;
@@ -187,11 +192,13 @@ const char *rlcs_status_string(rlcs_status status) {
 }
 
 rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk) {
-  if (shape != RLCS_SHAPE_AUTO && shape != RLCS_SHAPE_WARP_ROW && shape != RLCS_SHAPE_BLOCK_CHUNK)
+  if (shape != RLCS_SHAPE_AUTO && shape != RLCS_SHAPE_WARP_ROW &&
+      shape != RLCS_SHAPE_BLOCK_CHUNK && shape != RLCS_SHAPE_BLOCK_TILE)
     return RLCS_ERR_INVALID_ARG;
-  if (shape == RLCS_SHAPE_BLOCK_CHUNK && !(chunk == 0 || chunk == 1024 || chunk == 2048 || chunk == 4096))
+  const bool block = shape == RLCS_SHAPE_BLOCK_CHUNK || shape == RLCS_SHAPE_BLOCK_TILE;
+  if (block && !(chunk == 0 || chunk == 1024 || chunk == 2048 || chunk == 4096))
     return RLCS_ERR_INVALID_ARG;
-  g_override_chunk.store(shape == RLCS_SHAPE_BLOCK_CHUNK ? chunk : 0);
+  g_override_chunk.store(block ? chunk : 0);
   g_override_shape.store(shape);
   return RLCS_OK;
 }
@@ -332,7 +339,7 @@ rlcs_status rlcs_episodic_prefix_sum(const int32_t *x, const float *dones, int32
 // forbids allocating after start-up. They cannot provide the workspace that
 // long rows need, so here the look-back scratch lives in a fixed array of
 // device memory that belongs to this library: a 64-byte header plus 65536
-// chunk records of 16 bytes (about 1 MiB), held on every GPU that loads the
+// chunk records of 32 bytes (about 2 MiB), held on every GPU that loads the
 // library until the process exits.
 // ---------------------------------------------------------------------------
 namespace rlcs {

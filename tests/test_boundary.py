@@ -65,10 +65,10 @@ def test_workspace_bytes(lib):
     assert lib.rlcs_workspace_bytes(0, 10) == 0
     assert lib.rlcs_workspace_bytes(10, 0) == 0
     assert lib.rlcs_workspace_bytes(-1, 10) == 0
-    # 64-byte header + 16 bytes per 1024-step chunk of every row
-    assert lib.rlcs_workspace_bytes(4096, 128) == 64 + 16 * 4096
-    assert lib.rlcs_workspace_bytes(8, 131072) == 64 + 16 * 8 * 128
-    assert lib.rlcs_workspace_bytes(3, 1025) == 64 + 16 * 3 * 2
+    # 64-byte header + 32 bytes per 1024-step chunk of every row
+    assert lib.rlcs_workspace_bytes(4096, 128) == 64 + 32 * 4096
+    assert lib.rlcs_workspace_bytes(8, 131072) == 64 + 32 * 8 * 128
+    assert lib.rlcs_workspace_bytes(3, 1025) == 64 + 32 * 3 * 2
 
 
 FAKE = 0x7f0000000000  # 16-byte aligned fake device address, never dereferenced
@@ -138,6 +138,8 @@ def test_long_rows_need_a_workspace(lib):
 
 def test_shape_override_validation(lib):
     assert lib.rlcs_set_shape_override(7, 0) == INVALID
+    assert lib.rlcs_set_shape_override(3, 512) == INVALID
+    assert lib.rlcs_set_shape_override(3, 4096) == OK
     assert lib.rlcs_set_shape_override(2, 3000) == INVALID
     assert lib.rlcs_set_shape_override(2, 2048) == OK
     assert lib.rlcs_set_shape_override(0, 0) == OK

@@ -89,18 +89,34 @@ def test_warp_row_shape(rl, dev, T, trunc):
 
 @pytest.mark.parametrize("chunk,T", CHUNK_CASES)
 @pytest.mark.parametrize("trunc", [False, True])
-def test_block_chunk_shape(rl, dev, chunk, T, trunc):
-    rl.rlcs_set_shape_override(rl.RLCS_SHAPE_BLOCK_CHUNK, chunk)
+@pytest.mark.parametrize("shape", ["chunk", "tile"])
+def test_block_shapes(rl, dev, shape, chunk, T, trunc):
+    code = rl.RLCS_SHAPE_BLOCK_CHUNK if shape == "chunk" else rl.RLCS_SHAPE_BLOCK_TILE
+    rl.rlcs_set_shape_override(code, chunk)
     try:
         src = rollout(5, T, 3000 + T + chunk, p_term=0.01, p_trunc=0.005 if trunc else 0.0)
         check_all(rl, src, to_dev(src, dev), DEFAULT, ALL, trunc,
-                  tag=" [chunk=%d T=%d]" % (chunk, T))
+                  tag=" [%s=%d T=%d]" % (shape, chunk, T))
+    finally:
+        rl.rlcs_set_shape_override(rl.RLCS_SHAPE_AUTO, 0)
+
+
+@pytest.mark.parametrize("shape", ["chunk", "tile"])
+def test_block_shapes_many_rows(rl, dev, shape):
+    """Many rows of several tiles each: with row-interleaved tile order a
+    tile's predecessor is N blocks back."""
+    code = rl.RLCS_SHAPE_BLOCK_CHUNK if shape == "chunk" else rl.RLCS_SHAPE_BLOCK_TILE
+    rl.rlcs_set_shape_override(code, 1024)
+    try:
+        src = rollout(700, 5000, 3100, p_term=0.002, p_trunc=0.001)
+        check_all(rl, src, to_dev(src, dev), DEFAULT, ALL, True, tag=" [%s many rows]" % shape)
     finally:
         rl.rlcs_set_shape_override(rl.RLCS_SHAPE_AUTO, 0)
 
 
 @pytest.mark.parametrize("shape,chunk,T", [(1, 0, 128), (1, 0, 300), (2, 1024, 3000),
-                                           (2, 4096, 9000), (2, 2048, 2048)])
+                                           (2, 4096, 9000), (2, 2048, 2048), (3, 1024, 3000),
+                                           (3, 4096, 9000), (3, 2048, 2048)])
 def test_unaligned_rows_take_scalar_path(rl, dev, shape, chunk, T):
     rl.rlcs_set_shape_override(shape, chunk)
     try:
