@@ -89,7 +89,8 @@ rlcs_status rlcs_workspace_init(void *workspace, size_t bytes,
 
 /* Synchronise `stream`, then read and clear the device-side status that
  * calls using `workspace` recorded (RLCS_ERR_TIMEOUT when a bounded wait ran
- * out, RLCS_ERR_WORKSPACE when the workspace was not initialised). Returns
+ * out, RLCS_ERR_WORKSPACE when the workspace was not initialised; the higher
+ * code wins when both happened). Returns
  * RLCS_ERR_CUDA if the stream reported an error. workspace may be NULL, in
  * which case only the stream is checked. */
 rlcs_status rlcs_check_status(void *workspace, rlcs_stream_t stream);

@@ -120,7 +120,7 @@ struct DiscountedReturns {
 
 // ---------------------------------------------------------------------------
 // V-trace (IMPALA, lambda in the trace weight):
-//   rho = min(rho_bar, e^lr), c = lambda*min(c_bar, e^lr)
+//   rho = min(rho_bar, e^lr), c = lambda*min(c_bar, e^lr)   (e^lr by __expf)
 //   alpha = rho*(r + gamma*S - V), beta = gamma*c (0 at a cut), A = vs - V.
 // Outputs vs = V + A and pg = alpha + [not cut]*gamma*rho*A_{t+1}, which is
 // rho*(r + gamma*W - V) with W = vs_{t+1} (or S at a cut).
@@ -137,7 +137,7 @@ struct VTrace {
                                                Pair &e, float &aux0, float &aux1) {
     bool cut;
     const float S = successor<TRUNC>(s, boot, cut);
-    const float ratio = expf(s.lr);
+    const float ratio = __expf(s.lr);  // fast exponential: ~1e-6 relative error
     const float rho = fminf(p.rho_bar, ratio);
     const float c = p.lambda * fminf(p.c_bar, ratio);
     e.c = rho * (fmaf(p.gamma, S, s.r) - s.v);
@@ -175,7 +175,7 @@ struct Retrace {
       e.c = fmaf(p.gamma, S, s.r);
       e.m = 0.0f;
     } else {
-      const float c_next = p.lambda * fminf(p.c_bar, expf(s.lrn));
+      const float c_next = p.lambda * fminf(p.c_bar, __expf(s.lrn));
       e.c = fmaf(p.gamma, fmaf(-c_next, s.qn, s.vn), s.r);
       e.m = p.gamma * c_next;
     }

@@ -202,41 +202,52 @@ struct Strips {
     const bool at_origin = (t_span == 0);
 #pragma unroll
     for (int j = 0; j < S; ++j) {
-      float4 raw[kNumSlots], nx[kNumSlots];
+      // A strip wholly inside the row, and not holding the row's last step,
+      // needs no per-step bound checks (uniform across the warp).
+      if ((j + 1) * kStrip < rem && !(at_origin && j == 0))
+        build_strip<true>(p, src, boot, j, rem, false, lane);
+      else
+        build_strip<false>(p, src, boot, j, rem, at_origin, lane);
+    }
+  }
+
+  template <bool FULL, class Src>
+  __device__ __forceinline__ void build_strip(const Params &p, const Src &src, float boot, int j,
+                                              int rem, bool at_origin, int lane) {
+    float4 raw[kNumSlots], nx[kNumSlots];
 #pragma unroll
-      for (int k = 0; k < kNumSlots; ++k) raw[k] = (kUse & bit(k)) ? src.get(k, j) : f4zero();
+    for (int k = 0; k < kNumSlots; ++k) raw[k] = (kUse & bit(k)) ? src.get(k, j) : f4zero();
 #pragma unroll
-      for (int k = 0; k < kNumSlots; ++k)
-        nx[k] = (E::kBackward && (E::kNext & bit(k))) ? next4(raw[k], src.following(k, j), lane)
-                                                      : f4zero();
-      float4 dp = f4zero();
-      if (!E::kBackward) dp = prev4(raw[kD], src.preceding_d(j), lane);
-      const int o0 = j * kStrip + 4 * lane;  // offset of the lane's run in the span
+    for (int k = 0; k < kNumSlots; ++k)
+      nx[k] = (E::kBackward && (E::kNext & bit(k))) ? next4(raw[k], src.following(k, j), lane)
+                                                    : f4zero();
+    float4 dp = f4zero();
+    if (!E::kBackward) dp = prev4(raw[kD], src.preceding_d(j), lane);
+    const int o0 = j * kStrip + 4 * lane;  // offset of the lane's run in the span
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int o = o0 + i;
-        StepIn s;
-        s.r = f4get(raw[kR], i);
-        s.v = f4get(raw[kV], i);
-        s.q = f4get(raw[kQ], i);
-        s.lr = f4get(raw[kLR], i);
-        s.d = f4get(raw[kD], i);
-        s.tau = f4get(raw[kTau], i);
-        s.nv = f4get(raw[kNV], i);
-        s.vn = f4get(nx[kV], i);
-        s.qn = f4get(nx[kQ], i);
-        s.lrn = f4get(nx[kLR], i);
-        s.dp = f4get(dp, i);
-        s.last = (o == rem - 1);
-        s.first = at_origin && (o == 0);
-        float a0 = 0.f, a1 = 0.f;
-        P e;
-        E::template coeff<TRUNC>(p, s, boot, e, a0, a1);
-        if (o >= rem) e = identity(P{});  // ragged tail: padding is the identity
-        el[j][i] = e;
-        aux0[j][i] = a0;
-        aux1[j][i] = a1;
-      }
+    for (int i = 0; i < 4; ++i) {
+      const int o = o0 + i;
+      StepIn s;
+      s.r = f4get(raw[kR], i);
+      s.v = f4get(raw[kV], i);
+      s.q = f4get(raw[kQ], i);
+      s.lr = f4get(raw[kLR], i);
+      s.d = f4get(raw[kD], i);
+      s.tau = f4get(raw[kTau], i);
+      s.nv = f4get(raw[kNV], i);
+      s.vn = f4get(nx[kV], i);
+      s.qn = f4get(nx[kQ], i);
+      s.lrn = f4get(nx[kLR], i);
+      s.dp = f4get(dp, i);
+      s.last = FULL ? false : (o == rem - 1);
+      s.first = FULL ? false : (at_origin && o == 0);
+      float a0 = 0.f, a1 = 0.f;
+      P e;
+      E::template coeff<TRUNC>(p, s, boot, e, a0, a1);
+      if (!FULL && o >= rem) e = identity(P{});  // ragged tail: padding is the identity
+      el[j][i] = e;
+      aux0[j][i] = a0;
+      aux1[j][i] = a1;
     }
   }
 
