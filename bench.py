@@ -58,6 +58,20 @@ ESTIMATORS = {
 BACKWARD = ("gae", "lambda_returns", "discounted_returns", "vtrace", "retrace")
 
 
+def kernel_source_hash():
+    """Short hash of the CUDA sources, to tell whether stored ncu counters
+    still describe the kernels being timed."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "linear_recurrence_scan_affine_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "*.cu*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def bytes_per_env_step(est):
     ins, outs = ESTIMATORS[est]
     return 4 * (len(ins) + len(outs))
@@ -432,7 +446,10 @@ def run_ours(args):
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tr_path):
         with open(tr_path) as fh:
-            traffic = json.load(fh).get("%s_%dx%d" % (dom, N, T))
+            tr = json.load(fh)
+        # counters count only for the kernel sources they were taken on
+        if tr.get("kernel_source_sha256_16") == kernel_source_hash():
+            traffic = tr.get("%s_%dx%d" % (dom, N, T))
     achieved = per_est[dom]["gbs"]
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
