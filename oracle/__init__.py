@@ -19,7 +19,10 @@ _lib = None
 def _load():
     global _lib
     if _lib is None:
-        lib = ctypes.CDLL(_build.build())
+        # RLCS_ORACLE_LIB lets the mutation tests point the pins at a
+        # deliberately broken build of this oracle.
+        path = os.environ.get("RLCS_ORACLE_LIB") or _build.build()
+        lib = ctypes.CDLL(path)
         i64, dbl, ptr = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
         lib.oracle_gae.argtypes = [i64, i64] + [ptr] * 6 + [dbl, dbl, ptr]
         lib.oracle_lambda_returns.argtypes = [i64, i64] + [ptr] * 6 + [dbl, dbl, ptr]

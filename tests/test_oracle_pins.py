@@ -344,10 +344,11 @@ def test_bruteforce_random(T, trunc):
             src["x_int"][n].tolist(), L(d))
 
 
-@pytest.mark.parametrize("T", [1, 4, 7])
-def test_bruteforce_exhaustive_exact(T):
+@pytest.mark.parametrize("T,both", [(1, False), (4, False), (7, False), (2, True), (5, True)])
+def test_bruteforce_exhaustive_exact(T, both):
     """Every (terminated, truncated) pattern with small integer inputs and
-    dyadic gamma/lambda: the oracle and the explicit sums must agree exactly."""
+    dyadic gamma/lambda: the oracle and the explicit sums must agree exactly.
+    With `both`, steps may also carry both masks at once (termination wins)."""
     rng = np.random.default_rng(T)
     gamma, lam = 0.5, 0.75
     r = rng.integers(-4, 5, T).astype(np.float32)
@@ -358,10 +359,11 @@ def test_bruteforce_exhaustive_exact(T):
     xi = rng.integers(-100, 101, T).astype(np.int32)
     zero = np.zeros(T, np.float32)
     boot = 3.0
-    pats = list(itertools.product([0, 1, 2], repeat=T))  # 0 none, 1 term, 2 trunc
+    kinds = [0, 1, 2, 3] if both else [0, 1, 2]  # none, term, trunc, both
+    pats = list(itertools.product(kinds, repeat=T))
     for pat in pats:
-        d = np.array([p == 1 for p in pat], np.float32)
-        tr = np.array([p == 2 for p in pat], np.float32)
+        d = np.array([p in (1, 3) for p in pat], np.float32)
+        tr = np.array([p in (2, 3) for p in pat], np.float32)
         kw = dict(boot=boot, trunc=tr.tolist(), nv=nv.tolist())
         B = np.array([boot], np.float32)
         got = oracle.gae(r[None], v[None], d[None], gamma, lam, B, tr[None], nv[None])[0]
