@@ -57,6 +57,14 @@ ESTIMATORS = {
 }
 BACKWARD = ("gae", "lambda_returns", "discounted_returns", "vtrace", "retrace")
 
+# Entry points beyond the seven (timed alone, reported under "next_rows").
+EXTRA = {
+    "gae_and_returns": (("rewards", "values", "terminateds"), ("out", "out2")),
+    "affine_scan": (("a", "b", "reset"), ("out",)),
+}
+SPECS = dict(ESTIMATORS, **EXTRA)
+ROW_VALUE = BACKWARD + ("gae_and_returns", "affine_scan")   # read one value per row
+
 
 def kernel_source_hash():
     """Short hash of the CUDA sources, to tell whether stored ncu counters
@@ -73,12 +81,12 @@ def kernel_source_hash():
 
 
 def bytes_per_env_step(est):
-    ins, outs = ESTIMATORS[est]
+    ins, outs = SPECS[est]
     return 4 * (len(ins) + len(outs))
 
 
 def bytes_per_launch(est, N, T):
-    return bytes_per_env_step(est) * N * T + (4 * N if est in BACKWARD else 0)
+    return bytes_per_env_step(est) * N * T + (4 * N if est in ROW_VALUE else 0)
 
 
 # ---------------------------------------------------------------------------
@@ -307,6 +315,11 @@ def launch(rl, est, e, prm):
         rl.rlcs_eligibility_traces(e["x"], e["terminateds"], g, lm, out=e["out"])
     elif est == "episodic_prefix_sum":
         rl.rlcs_episodic_prefix_sum(e["x_int"], e["terminateds"], out=e["out"])
+    elif est == "gae_and_returns":
+        rl.rlcs_gae_and_returns(e["rewards"], e["values"], e["terminateds"], g, lm,
+                                e["bootstrap_value"], out=e["out"], out_returns=e["out2"])
+    elif est == "affine_scan":
+        rl.rlcs_affine_scan(e["a"], e["b"], e["reset"], e["x_init"], reverse=True, out=e["out"])
 
 
 def capture(torch, stream, fn):
@@ -469,10 +482,25 @@ def run_ours(args):
             for est in wl.estimators:
                 r_ = time_alone(torch, rl, est, src_l, dev, stream, prm_l, l2, wl.N, wl.T,
                                 seconds=0.08)
-                r_["frac_of_measured_hbm"] = r_["gbs"] * 1e9 / (peak * 1e9)
+                r_["frac_of_measured_hbm"] = r_["gbs"] / peak
                 res[est] = r_
             long_t[name] = res
             del src_l
+        rl.check_all_workspaces()
+
+    # entry points beyond the seven, alone, at the bench size and one long size
+    next_rows = {}
+    if not args.no_long_t:
+        from synthetic_rollouts import affine_inputs
+        for (nN, nT, seed) in ((N, T, w.seed), (256, 16384, 1004)):
+            srcn = dict(rollout(nN, nT, seed, w.p_term), **affine_inputs(nN, nT, seed + 7))
+            res = {}
+            for est in EXTRA:
+                r_ = time_alone(torch, rl, est, srcn, dev, stream, prm, l2, nN, nT, seconds=0.08)
+                r_["frac_of_measured_hbm"] = r_["gbs"] / peak
+                res[est] = r_
+            next_rows["%dx%d" % (nN, nT)] = res
+            del srcn
         rl.check_all_workspaces()
 
     e2e = run_e2e(torch, rl, src, dev, stream, prm, order, max(32, min(K, 512)), N, T)
@@ -504,7 +532,7 @@ def run_ours(args):
             "hbm_frac_of_measured": step_gbs / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 7 * K, "clocks": clocks, "per_estimator": per_est,
-            "long_t_sweep": long_t,
+            "long_t_sweep": long_t, "next_rows": next_rows,
         }
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -514,12 +542,13 @@ def run_ours(args):
 
 
 def time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T, seconds=0.15):
-    ins, outs = ESTIMATORS[est]
+    ins, outs = SPECS[est]
+    row_key = "x_init" if est == "affine_scan" else "bootstrap_value"
     set_bytes = bytes_per_launch(est, N, T)
     nsets = int(min(256, max(8, -(-3 * l2 // set_bytes))))
     sets = []
     for _ in range(nsets):
-        e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + ("bootstrap_value",)}
+        e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + (row_key,)}
         for o in outs:
             e[o] = torch.empty_like(e[ins[0]])
         sets.append(e)
@@ -541,47 +570,107 @@ def time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T, seconds=0.15):
             "footprint_over_l2": nsets * set_bytes / l2}
 
 
-def run_e2e(torch, rl, src, dev, stream, prm, order, steps, N, T):
-    """Whole step through the public API from pinned host buffers: copy every
-    estimator's inputs in, run the seven kernels, copy every output back."""
-    host_in, dev_set = {}, {}
-    h2d = d2h = 0
-    for est in order:
-        ins, outs = ESTIMATORS[est]
-        e, h = {}, {}
-        for k in ins + ("bootstrap_value",):
-            h[k] = torch.from_numpy(src[k]).pin_memory()
-            e[k] = torch.empty_like(h[k], device=dev)
-            h2d += h[k].numel() * h[k].element_size()
-        for o in outs:
-            e[o] = torch.empty_like(e[ins[0]])
-            h[o] = torch.empty_like(h[ins[0]]).pin_memory()
-            d2h += h[o].numel() * h[o].element_size()
-        host_in[est], dev_set[est] = h, e
+def run_e2e(torch, rl, src, dev, stream, prm, order, steps, N, T, depth=2, block=16):
+    """Whole steps through the public API from pinned host memory.
 
-    def step():
+    Like a rollout buffer, one step's inputs for all seven estimators sit in
+    one contiguous pinned host buffer and its outputs come back into another;
+    each step copies its inputs in with one host-to-device copy, runs the
+    seven rlcs_* calls, and copies every output back with one device-to-host
+    copy. Steps are pipelined over `depth` device buffer slots on separate
+    copy-in, compute and copy-out streams, so step i+1's copy-in overlaps step
+    i's kernels and step i-1's copy-out."""
+    def layout(kind):
+        off, fields = 0, []
         for est in order:
             ins, outs = ESTIMATORS[est]
-            for k in ins + ("bootstrap_value",):
-                dev_set[est][k].copy_(host_in[est][k], non_blocking=True)
+            names = ins + ("bootstrap_value",) if kind == "in" else outs
+            for k in names:
+                ref = src[k] if kind == "in" else src["rewards"]
+                nbytes = ref.size * ref.itemsize
+                fields.append((est, k, off, ref.shape, ref.dtype))
+                off += (nbytes + 255) // 256 * 256
+        return fields, off
+
+    in_fields, in_bytes = layout("in")
+    out_fields, out_bytes = layout("out")
+    h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    for est, k, off, shp, dt in in_fields:
+        a = src[k]
+        h_in[off:off + a.size * a.itemsize].copy_(torch.from_numpy(a.view(np.uint8).reshape(-1)))
+    h_out = [torch.empty(out_bytes, dtype=torch.uint8).pin_memory() for _ in range(depth)]
+    d_in = [torch.empty(in_bytes, dtype=torch.uint8, device=dev) for _ in range(depth)]
+    d_out = [torch.empty(out_bytes, dtype=torch.uint8, device=dev) for _ in range(depth)]
+    tdt = {np.dtype(np.float32): torch.float32, np.dtype(np.int32): torch.int32}
+
+    def views(buf_in, buf_out):
+        sets = {est: {} for est in order}
+        for est, k, off, shp, dt in in_fields:
+            n = int(np.prod(shp))
+            sets[est][k] = buf_in[off:off + n * 4].view(tdt[dt]).view(*shp)
+        for est, k, off, shp, dt in out_fields:
+            n = int(np.prod(shp))
+            ref_dt = tdt[src[ESTIMATORS[est][0][0]].dtype]
+            sets[est][k] = buf_out[off:off + n * 4].view(ref_dt).view(*shp)
+        return sets
+
+    slot_sets = [views(d_in[i], d_out[i]) for i in range(depth)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    side = {est: torch.cuda.Stream(dev) for est in order}
+
+    def step(i, slot, ev):
+        # copy-in may reuse the slot once the kernels of step i - depth are done
+        if ev["comp"][slot] is not None:
+            s_in.wait_event(ev["comp"][slot])
+        with torch.cuda.stream(s_in):
+            d_in[slot].copy_(h_in, non_blocking=True)
+        e_in = torch.cuda.Event()
+        e_in.record(s_in)
+        joins = []
         for est in order:
-            launch(rl, est, dev_set[est], prm)
-        for est in order:
-            for o in ESTIMATORS[est][1]:
-                host_in[est][o].copy_(dev_set[est][o], non_blocking=True)
+            st = side[est]
+            st.wait_event(e_in)
+            if ev["out"][slot] is not None:   # outputs of step i - depth copied out
+                st.wait_event(ev["out"][slot])
+            with torch.cuda.stream(st):
+                launch(rl, est, slot_sets[slot][est], prm)
+            e = torch.cuda.Event()
+            e.record(st)
+            joins.append(e)
+        for e in joins:
+            s_out.wait_event(e)
+        e_comp = torch.cuda.Event()
+        e_comp.record(s_out)
+        with torch.cuda.stream(s_out):
+            h_out[slot].copy_(d_out[slot], non_blocking=True)
+        e_out = torch.cuda.Event()
+        e_out.record(s_out)
+        ev["comp"][slot], ev["out"][slot] = e_comp, e_out
+
+    def block_fn():
+        ev = {"comp": [None] * depth, "out": [None] * depth}
+        for s_ in [s_in, s_out] + list(side.values()):
+            s_.wait_stream(stream)
+        for i in range(block):
+            step(i, i % depth, ev)
+        for s_ in [s_in, s_out] + list(side.values()):
+            stream.wait_stream(s_)
 
     with torch.cuda.stream(stream):
-        step()
+        block_fn()  # eager warm-up: workspaces allocated outside capture
     torch.cuda.synchronize()
-    g = capture(torch, stream, step)
+    g = capture(torch, stream, block_fn)
     with torch.cuda.stream(stream):
-        for _ in range(3):
+        for _ in range(2):
             g.replay()
-    sec = time_graph(torch, stream, g, steps) / steps
-    return {"value": N * T / sec, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": sec * 1e3,
-            "path": "pinned host -> device copies, seven rlcs_* calls, device -> pinned host "
-                    "copies, one CUDA graph per step"}
+    reps = max(2, -(-steps // block))
+    sec = time_graph(torch, stream, g, reps) / (reps * block)
+    return {"value": N * T / sec, "unit": UNIT, "h2d_bytes_per_step": in_bytes,
+            "d2h_bytes_per_step": out_bytes, "ms_per_step": sec * 1e3,
+            "path": "one pinned host->device copy of all seven estimators' inputs, seven rlcs_* "
+                    "calls on seven streams, one device->pinned host copy of all outputs, per "
+                    "step; %d-slot pipeline over copy-in / compute / copy-out streams, CUDA "
+                    "graph of %d steps" % (depth, block)}
 
 
 def run_profile(args):

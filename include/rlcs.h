@@ -198,6 +198,34 @@ rlcs_status rlcs_episodic_prefix_sum(const int32_t *x, const float *dones,
                                      void *workspace, size_t workspace_bytes,
                                      rlcs_stream_t stream);
 
+/* GAE advantages and TD(lambda) returns in one pass.
+ * README Kernels table, compute_gae and compute_lambda_returns; the two share
+ * their coefficients, and TD(lambda) returns = GAE + values. Same inputs and
+ * conventions as rlcs_gae; writes advantages [N,T] and returns [N,T] from a
+ * single read of the inputs (20 bytes per step instead of 32 for two calls).
+ * The outputs must not overlap each other or any input. */
+rlcs_status rlcs_gae_and_returns(const float *rewards, const float *values,
+                                 const float *terminateds, const float *truncateds,
+                                 const float *next_values, const float *bootstrap_value,
+                                 float *advantages, float *returns, int64_t N, int64_t T,
+                                 float gamma, float lambda, void *workspace,
+                                 size_t workspace_bytes, rlcs_stream_t stream);
+
+/* Generic segmented first-order affine recurrence on raw coefficients.
+ * The recurrence of the technical summary, Methodology 1, with a and b given
+ * directly (its Significance section points to other segmented affine
+ * recurrences):
+ *   reverse = 0:  x_t = a_t * x_{t-1} + b_t,   x_{-1} = x_init[n]
+ *   reverse = 1:  x_t = a_t * x_{t+1} + b_t,   x_T    = x_init[n]
+ * a, b, x are [N,T] float32; reset [N,T] is optional (NULL: no resets) and
+ * where it is nonzero the step does not depend on its neighbour (x_t = b_t);
+ * x_init [N] is optional (NULL: 0). Same layout, stream, workspace and error
+ * conventions as the estimators. */
+rlcs_status rlcs_affine_scan(const float *a, const float *b, const float *reset,
+                             const float *x_init, float *x, int64_t N, int64_t T,
+                             int reverse, void *workspace, size_t workspace_bytes,
+                             rlcs_stream_t stream);
+
 /* GAE for callers that cannot allocate device memory.
  * The paper has no counterpart: this is a library convenience. Some callers
  * cannot call cudaMalloc, such as a plugin inside a host program that owns

@@ -46,6 +46,8 @@ def _load():
         "rlcs_retrace": ([P] * 9 + [I64, I64, F, F, F, P, SZ, P], ctypes.c_int),
         "rlcs_eligibility_traces": ([P] * 3 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
         "rlcs_episodic_prefix_sum": ([P] * 3 + [I64, I64, P, SZ, P], ctypes.c_int),
+        "rlcs_gae_and_returns": ([P] * 8 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_affine_scan": ([P] * 5 + [I64, I64, ctypes.c_int, P, SZ, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -58,7 +60,8 @@ _lib = _load()
 EXPORTED = ("rlcs_workspace_bytes", "rlcs_workspace_init", "rlcs_check_status",
             "rlcs_status_string", "rlcs_set_shape_override", "rlcs_gae",
             "rlcs_lambda_returns", "rlcs_discounted_returns", "rlcs_vtrace",
-            "rlcs_retrace", "rlcs_eligibility_traces", "rlcs_episodic_prefix_sum")
+            "rlcs_retrace", "rlcs_eligibility_traces", "rlcs_episodic_prefix_sum",
+            "rlcs_gae_and_returns", "rlcs_affine_scan")
 
 
 def lib():
@@ -240,6 +243,40 @@ def rlcs_episodic_prefix_sum(x, dones, out=None, stream=None):
     _check(_lib.rlcs_episodic_prefix_sum(_ptr(xx), _ptr(d), _ptr(o), N, T, _ptr(ws), wsb,
                                          _stream(stream)), "rlcs_episodic_prefix_sum")
     return _finish(o, x)
+
+
+def rlcs_gae_and_returns(rewards, values, terminateds, gamma=0.99, lambda_=0.95,
+                         bootstrap_value=None, truncateds=None, next_values=None, out=None,
+                         out_returns=None, stream=None):
+    """Returns (advantages, returns) from one pass over the inputs."""
+    N, T, (r, v, d) = _prep(rewards, [(values, "values"), (terminateds, "terminateds")])
+    tr, nv = _opt(truncateds, "truncateds", N, T), _opt(next_values, "next_values", N, T)
+    b = _boot(bootstrap_value, N)
+    adv = torch.empty_like(r) if out is None else out
+    ret = torch.empty_like(r) if out_returns is None else out_returns
+    ws, wsb = workspace_for(N, T, r.device, stream)
+    _check(_lib.rlcs_gae_and_returns(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
+                                     _ptr(adv), _ptr(ret), N, T, gamma, lambda_, _ptr(ws), wsb,
+                                     _stream(stream)), "rlcs_gae_and_returns")
+    return _finish(adv, rewards), _finish(ret, rewards)
+
+
+def rlcs_affine_scan(a, b, reset=None, x_init=None, reverse=False, out=None, stream=None):
+    """x_t = a_t*x_{t-1} + b_t (reverse: x_t = a_t*x_{t+1} + b_t) per row."""
+    N, T, (aa, bb) = _prep(a, [(b, "b")], rewards_name="a")
+    rr = _opt(reset, "reset", N, T)
+    x0 = None
+    if x_init is not None:
+        x0 = x_init.reshape(-1)
+        if not x0.is_cuda or x0.dtype != torch.float32 or x0.numel() != N:
+            raise ValueError("x_init must be a float32 CUDA tensor of %d values" % N)
+        x0 = x0.contiguous()
+    o = torch.empty_like(aa) if out is None else out
+    ws, wsb = workspace_for(N, T, aa.device, stream)
+    _check(_lib.rlcs_affine_scan(_ptr(aa), _ptr(bb), _ptr(rr), _ptr(x0), _ptr(o), N, T,
+                                 1 if reverse else 0, _ptr(ws), wsb, _stream(stream)),
+           "rlcs_affine_scan")
+    return _finish(o, a)
 
 
 def rlcs_check_status(workspace=None, stream=None):

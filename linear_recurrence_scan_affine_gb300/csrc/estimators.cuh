@@ -52,6 +52,9 @@ constexpr uint32_t kTruncSlots = bit(kTau) | bit(kNV);
 // GAE: alpha = r + gamma*S - V, beta = gamma*lambda (0 at a cut). Out: A.
 // ---------------------------------------------------------------------------
 struct Gae {
+  static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
+  static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
+  static constexpr bool kPrevD = false;         // reads the done mask at t-1
   static constexpr bool kBackward = true;
   static constexpr uint32_t kSlots = bit(kR) | bit(kV) | bit(kD);
   static constexpr uint32_t kNext = bit(kV);
@@ -75,6 +78,9 @@ struct Gae {
 // at a cut alpha = r + gamma*S, beta = 0. Out: G.
 // ---------------------------------------------------------------------------
 struct LambdaReturns {
+  static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
+  static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
+  static constexpr bool kPrevD = false;         // reads the done mask at t-1
   static constexpr bool kBackward = true;
   static constexpr uint32_t kSlots = bit(kR) | bit(kV) | bit(kD);
   static constexpr uint32_t kNext = bit(kV);
@@ -98,6 +104,9 @@ struct LambdaReturns {
 // Discounted returns: alpha = r (+ gamma*S at a cut), beta = gamma (0 at a cut).
 // ---------------------------------------------------------------------------
 struct DiscountedReturns {
+  static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
+  static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
+  static constexpr bool kPrevD = false;         // reads the done mask at t-1
   static constexpr bool kBackward = true;
   static constexpr uint32_t kSlots = bit(kR) | bit(kD);
   static constexpr uint32_t kNext = 0;
@@ -127,6 +136,9 @@ struct DiscountedReturns {
 // aux0 = gamma*rho (0 at a cut), aux1 = V.
 // ---------------------------------------------------------------------------
 struct VTrace {
+  static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
+  static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
+  static constexpr bool kPrevD = false;         // reads the done mask at t-1
   static constexpr bool kBackward = true;
   static constexpr uint32_t kSlots = bit(kR) | bit(kV) | bit(kLR) | bit(kD);
   static constexpr uint32_t kNext = bit(kV);
@@ -161,6 +173,9 @@ struct VTrace {
 //   at a cut alpha = r + gamma*S, beta = 0. Out: Q^ret.
 // ---------------------------------------------------------------------------
 struct Retrace {
+  static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
+  static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
+  static constexpr bool kPrevD = false;         // reads the done mask at t-1
   static constexpr bool kBackward = true;
   static constexpr uint32_t kSlots = bit(kR) | bit(kV) | bit(kQ) | bit(kLR) | bit(kD);
   static constexpr uint32_t kNext = bit(kV) | bit(kQ) | bit(kLR);
@@ -190,6 +205,9 @@ struct Retrace {
 // beta_0 = 0 (e_{-1} = 0). Out: e.
 // ---------------------------------------------------------------------------
 struct EligibilityTraces {
+  static constexpr uint32_t kOptSlots = 0u;  // slots added when the optional input is given
+  static constexpr bool kUsesRowValue = false;  // reads bootstrap_value[n]
+  static constexpr bool kPrevD = true;         // reads the done mask at t-1
   static constexpr bool kBackward = false;
   static constexpr uint32_t kSlots = bit(kR) | bit(kD);
   static constexpr uint32_t kNext = 0;
@@ -211,6 +229,9 @@ struct EligibilityTraces {
 // m = (1 - d_{t-1}), m_0 = 0. The int32 input travels in slot R as raw bits.
 // ---------------------------------------------------------------------------
 struct EpisodicPrefixSum {
+  static constexpr uint32_t kOptSlots = 0u;  // slots added when the optional input is given
+  static constexpr bool kUsesRowValue = false;  // reads bootstrap_value[n]
+  static constexpr bool kPrevD = true;         // reads the done mask at t-1
   static constexpr bool kBackward = false;
   static constexpr uint32_t kSlots = bit(kR) | bit(kD);
   static constexpr uint32_t kNext = 0;
@@ -221,6 +242,65 @@ struct EpisodicPrefixSum {
                                                float &, float &) {
     e.c = __float_as_uint(s.r);
     e.m = (s.first || s.dp != 0.0f) ? 0u : 1u;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// GAE and TD(lambda) returns in one pass: the GAE pairs, with outputs
+// A_t and G_t = A_t + V_t (the identity TD(lambda) = GAE + V).
+// ---------------------------------------------------------------------------
+struct GaeAndReturns {
+  static constexpr uint32_t kOptSlots = kTruncSlots;
+  static constexpr bool kUsesRowValue = true;
+  static constexpr bool kPrevD = false;
+  static constexpr bool kBackward = true;
+  static constexpr uint32_t kSlots = bit(kR) | bit(kV) | bit(kD);
+  static constexpr uint32_t kNext = bit(kV);
+  static constexpr int kOuts = 2;
+  using Pair = FPair;
+  template <bool TRUNC>
+  __device__ static __forceinline__ void coeff(const Params &p, const StepIn &s, float boot,
+                                               Pair &e, float &, float &aux1) {
+    Gae::coeff<TRUNC>(p, s, boot, e, aux1, aux1);
+    aux1 = s.v;
+  }
+  __device__ static __forceinline__ float out0(float A, float, const Pair &, float, float) {
+    return A;
+  }
+  __device__ static __forceinline__ float out1(float A, float, const Pair &, float, float v) {
+    return v + A;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Generic first-order affine recurrence on raw coefficients (the segmented
+// affine scan the technical summary's Significance section points to):
+//   forward   x_t = a_t * x_{t-1} + b_t,   x_{-1} = x_init[n]
+//   backward  x_t = a_t * x_{t+1} + b_t,   x_T    = x_init[n]
+// b travels in slot R, a in slot Q, the optional reset mask in slot D. Where
+// reset[t] is set the step does not depend on its neighbour: x_t = b_t. The
+// step at the scan origin folds x_init into its addend.
+// ---------------------------------------------------------------------------
+template <bool BACKWARD>
+struct Affine {
+  static constexpr uint32_t kOptSlots = bit(kD);
+  static constexpr bool kUsesRowValue = true;
+  static constexpr bool kPrevD = false;
+  static constexpr bool kBackward = BACKWARD;
+  static constexpr uint32_t kSlots = bit(kR) | bit(kQ);
+  static constexpr uint32_t kNext = 0;
+  static constexpr int kOuts = 1;
+  using Pair = FPair;
+  template <bool RESET>
+  __device__ static __forceinline__ void coeff(const Params &, const StepIn &s, float x_init,
+                                               Pair &e, float &, float &) {
+    const bool cut = RESET && s.d != 0.0f;
+    const bool origin = BACKWARD ? s.last : s.first;
+    e.m = (cut || origin) ? 0.0f : s.q;
+    e.c = (origin && !cut) ? fmaf(s.q, x_init, s.r) : s.r;
+  }
+  __device__ static __forceinline__ float out0(float A, float, const Pair &, float, float) {
+    return A;
   }
 };
 

@@ -185,7 +185,7 @@ template <class E, bool TRUNC, int S>
 struct Strips {
   using P = typename E::Pair;
   using V = typename ValueOf<P>::type;
-  static constexpr uint32_t kUse = E::kSlots | ((TRUNC && E::kBackward) ? kTruncSlots : 0u);
+  static constexpr uint32_t kUse = E::kSlots | (TRUNC ? E::kOptSlots : 0u);
 
   P el[S][4];
   float aux0[S][4], aux1[S][4];
@@ -222,7 +222,7 @@ struct Strips {
       nx[k] = (E::kBackward && (E::kNext & bit(k))) ? next4(raw[k], src.following(k, j), lane)
                                                     : f4zero();
     float4 dp = f4zero();
-    if (!E::kBackward) dp = prev4(raw[kD], src.preceding_d(j), lane);
+    if (E::kPrevD) dp = prev4(raw[kD], src.preceding_d(j), lane);
     const int o0 = j * kStrip + 4 * lane;  // offset of the lane's run in the span
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -362,7 +362,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) warp_row_kernel(Params p) {
       raw[k][j] = (St::kUse & bit(k)) ? load4(p.in[k] + base, (int64_t)j * kStrip + 4 * lane, T, vec)
                                       : f4zero();
   }
-  const float boot = (E::kBackward && p.boot) ? __ldg(p.boot + row) : 0.f;
+  const float boot = (E::kUsesRowValue && p.boot) ? __ldg(p.boot + row) : 0.f;
   pdl_launch_dependents();
 
   float halo[kNumSlots];
@@ -596,9 +596,9 @@ __global__ void __launch_bounds__(kChunkThreads) block_chunk_kernel(Params p, Ch
     if (E::kBackward && (E::kNext & bit(k)) && warp == kChunkWarps - 1 && t0 + C < T)
       halo[k] = __ldg(p.in[k] + base + t0 + C);
   }
-  const float halo_d = (!E::kBackward && warp == 0 && t0 > 0) ? __ldg(p.in[kD] + base + t0 - 1)
-                                                              : 0.f;
-  const float boot = (E::kBackward && p.boot) ? __ldg(p.boot + row) : 0.f;
+  const float halo_d = (E::kPrevD && warp == 0 && t0 > 0) ? __ldg(p.in[kD] + base + t0 - 1)
+                                                          : 0.f;
+  const float boot = (E::kUsesRowValue && p.boot) ? __ldg(p.boot + row) : 0.f;
 
   if (vec) {
     if (!wait_bar(&bar)) set_status(cs.ws, kStatusTimeout);
@@ -733,8 +733,8 @@ __global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
     const int64_t th = t_span + (int64_t)kStrip * S;  // first step after the span
     halo[k] = (E::kBackward && (E::kNext & bit(k)) && th < T) ? __ldg(p.in[k] + base + th) : 0.f;
   }
-  const float halo_d = (!E::kBackward && t_span > 0) ? __ldg(p.in[kD] + base + t_span - 1) : 0.f;
-  const float boot = (E::kBackward && p.boot) ? __ldg(p.boot + row) : 0.f;
+  const float halo_d = (E::kPrevD && t_span > 0) ? __ldg(p.in[kD] + base + t_span - 1) : 0.f;
+  const float boot = (E::kUsesRowValue && p.boot) ? __ldg(p.boot + row) : 0.f;
   if (tid == 0 && Q > 1) s_epoch = ld_relaxed_gpu(&ts.ws->epoch);  // after the loads issue
   pdl_launch_dependents();
 

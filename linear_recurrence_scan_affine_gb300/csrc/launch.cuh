@@ -12,7 +12,8 @@ struct Plan {
   int shape;       // RLCS_SHAPE_WARP_ROW, RLCS_SHAPE_BLOCK_CHUNK or RLCS_SHAPE_BLOCK_TILE
   int S;           // strips per warp: 1, 2 or 4
   int64_t Q;       // chunks per row (block-chunk shape)
-  bool trunc;      // truncation inputs present
+  bool trunc;      // the estimator's optional inputs are present (truncation,
+                   // or the affine scan's reset mask)
   bool pdl;        // launch with programmatic stream serialization
 };
 
@@ -70,7 +71,9 @@ inline cudaError_t launch_trunc(const Params &p, const Plan &plan, WsHeader *ws,
 template <class E>
 inline cudaError_t launch_estimator(const Params &p, const Plan &plan, WsHeader *ws,
                                     cudaStream_t s) {
-  if (E::kBackward && plan.trunc) return launch_trunc<E, true>(p, plan, ws, s);
+  if constexpr (E::kOptSlots != 0u) {
+    if (plan.trunc) return launch_trunc<E, true>(p, plan, ws, s);
+  }
   return launch_trunc<E, false>(p, plan, ws, s);
 }
 
@@ -82,5 +85,8 @@ cudaError_t launch_vtrace(const Params &, const Plan &, WsHeader *, cudaStream_t
 cudaError_t launch_retrace(const Params &, const Plan &, WsHeader *, cudaStream_t);
 cudaError_t launch_eligibility_traces(const Params &, const Plan &, WsHeader *, cudaStream_t);
 cudaError_t launch_episodic_prefix_sum(const Params &, const Plan &, WsHeader *, cudaStream_t);
+cudaError_t launch_gae_and_returns(const Params &, const Plan &, WsHeader *, cudaStream_t);
+cudaError_t launch_affine_forward(const Params &, const Plan &, WsHeader *, cudaStream_t);
+cudaError_t launch_affine_backward(const Params &, const Plan &, WsHeader *, cudaStream_t);
 
 }  // namespace rlcs

@@ -81,9 +81,12 @@ bool overlaps(const Buf &a, const Buf &b) {
 }
 
 // Shared tail of every entry point.
+// `opt`: the estimator's optional inputs are present (the truncation pair,
+// or the affine scan's reset mask already placed in p.in).
 template <class Launch>
 rlcs_status run(Params &p, const float *trunc, const float *next_values, void *const *outs,
-                int n_outs, void *ws, size_t ws_bytes, cudaStream_t stream, Launch launch) {
+                int n_outs, void *ws, size_t ws_bytes, cudaStream_t stream, Launch launch,
+                bool opt) {
   const int64_t N = p.N, T = p.T;
   if (N <= 0 || T <= 0) return RLCS_ERR_INVALID_ARG;
   if (N > (int64_t)(INT64_MAX / 4) / T) return RLCS_ERR_INVALID_ARG;
@@ -107,7 +110,7 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
   p.vec = vec ? 1 : 0;
 
   Plan plan;
-  const rlcs_status st = plan_call(N, T, trunc != nullptr, plan);
+  const rlcs_status st = plan_call(N, T, opt, plan);
   if (st != RLCS_OK) return st;
   WsHeader *wsh = nullptr;
   if (plan.shape != RLCS_SHAPE_WARP_ROW) {
@@ -218,7 +221,7 @@ rlcs_status rlcs_gae(const float *rewards, const float *values, const float *ter
   p.lambda = lambda;
   void *outs[1] = {advantages};
   return run(p, truncateds, next_values, outs, 1, workspace, workspace_bytes,
-             reinterpret_cast<cudaStream_t>(stream), launch_gae);
+             reinterpret_cast<cudaStream_t>(stream), launch_gae, truncateds != nullptr);
 }
 
 rlcs_status rlcs_lambda_returns(const float *rewards, const float *values,
@@ -236,7 +239,7 @@ rlcs_status rlcs_lambda_returns(const float *rewards, const float *values,
   p.lambda = lambda;
   void *outs[1] = {returns};
   return run(p, truncateds, next_values, outs, 1, workspace, workspace_bytes,
-             reinterpret_cast<cudaStream_t>(stream), launch_lambda_returns);
+             reinterpret_cast<cudaStream_t>(stream), launch_lambda_returns, truncateds != nullptr);
 }
 
 rlcs_status rlcs_discounted_returns(const float *rewards, const float *terminateds,
@@ -252,7 +255,7 @@ rlcs_status rlcs_discounted_returns(const float *rewards, const float *terminate
   p.gamma = gamma;
   void *outs[1] = {returns};
   return run(p, truncateds, next_values, outs, 1, workspace, workspace_bytes,
-             reinterpret_cast<cudaStream_t>(stream), launch_discounted_returns);
+             reinterpret_cast<cudaStream_t>(stream), launch_discounted_returns, truncateds != nullptr);
 }
 
 rlcs_status rlcs_vtrace(const float *rewards, const float *values, const float *log_rhos,
@@ -275,7 +278,7 @@ rlcs_status rlcs_vtrace(const float *rewards, const float *values, const float *
   p.c_bar = c_bar;
   void *outs[2] = {vs, pg_advantages};
   return run(p, truncateds, next_values, outs, 2, workspace, workspace_bytes,
-             reinterpret_cast<cudaStream_t>(stream), launch_vtrace);
+             reinterpret_cast<cudaStream_t>(stream), launch_vtrace, truncateds != nullptr);
 }
 
 rlcs_status rlcs_retrace(const float *rewards, const float *values, const float *q_values,
@@ -298,7 +301,7 @@ rlcs_status rlcs_retrace(const float *rewards, const float *values, const float 
   p.c_bar = c_bar;
   void *outs[1] = {q_ret};
   return run(p, truncateds, next_values, outs, 1, workspace, workspace_bytes,
-             reinterpret_cast<cudaStream_t>(stream), launch_retrace);
+             reinterpret_cast<cudaStream_t>(stream), launch_retrace, truncateds != nullptr);
 }
 
 rlcs_status rlcs_eligibility_traces(const float *x, const float *dones, float *traces, int64_t N,
@@ -313,7 +316,7 @@ rlcs_status rlcs_eligibility_traces(const float *x, const float *dones, float *t
   p.lambda = lambda;
   void *outs[1] = {traces};
   return run(p, nullptr, nullptr, outs, 1, workspace, workspace_bytes,
-             reinterpret_cast<cudaStream_t>(stream), launch_eligibility_traces);
+             reinterpret_cast<cudaStream_t>(stream), launch_eligibility_traces, false);
 }
 
 rlcs_status rlcs_episodic_prefix_sum(const int32_t *x, const float *dones, int32_t *out,
@@ -326,10 +329,48 @@ rlcs_status rlcs_episodic_prefix_sum(const int32_t *x, const float *dones, int32
   p.out0 = out;
   void *outs[1] = {out};
   return run(p, nullptr, nullptr, outs, 1, workspace, workspace_bytes,
-             reinterpret_cast<cudaStream_t>(stream), launch_episodic_prefix_sum);
+             reinterpret_cast<cudaStream_t>(stream), launch_episodic_prefix_sum, false);
 }
 
 }  // extern "C"
+
+extern "C" rlcs_status rlcs_gae_and_returns(const float *rewards, const float *values,
+                                            const float *terminateds, const float *truncateds,
+                                            const float *next_values,
+                                            const float *bootstrap_value, float *advantages,
+                                            float *returns, int64_t N, int64_t T, float gamma,
+                                            float lambda, void *workspace,
+                                            size_t workspace_bytes, rlcs_stream_t stream) {
+  if (!rewards || !values || !terminateds || !advantages || !returns) return RLCS_ERR_INVALID_ARG;
+  Params p = base_params(N, T, bootstrap_value);
+  p.in[kR] = rewards;
+  p.in[kV] = values;
+  p.in[kD] = terminateds;
+  p.out0 = advantages;
+  p.out1 = returns;
+  p.gamma = gamma;
+  p.lambda = lambda;
+  void *outs[2] = {advantages, returns};
+  return run(p, truncateds, next_values, outs, 2, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), launch_gae_and_returns,
+             truncateds != nullptr);
+}
+
+extern "C" rlcs_status rlcs_affine_scan(const float *a, const float *b, const float *reset,
+                                        const float *x_init, float *x, int64_t N, int64_t T,
+                                        int reverse, void *workspace, size_t workspace_bytes,
+                                        rlcs_stream_t stream) {
+  if (!a || !b || !x) return RLCS_ERR_INVALID_ARG;
+  Params p = base_params(N, T, x_init);
+  p.in[kR] = b;
+  p.in[kQ] = a;
+  p.in[kD] = reset;
+  p.out0 = x;
+  void *outs[1] = {x};
+  return run(p, nullptr, nullptr, outs, 1, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream),
+             reverse ? launch_affine_backward : launch_affine_forward, reset != nullptr);
+}
 
 // ---------------------------------------------------------------------------
 // GAE for callers that cannot allocate device memory.

@@ -31,10 +31,11 @@ def _load():
         lib.oracle_retrace.argtypes = [i64, i64] + [ptr] * 8 + [dbl] * 3 + [ptr]
         lib.oracle_eligibility_traces.argtypes = [i64, i64, ptr, ptr, dbl, dbl, ptr]
         lib.oracle_episodic_prefix_sum.argtypes = [i64, i64, ptr, ptr, ptr]
+        lib.oracle_affine_scan.argtypes = [i64, i64, ptr, ptr, ptr, ptr, ctypes.c_int, ptr]
         for f in (lib.oracle_gae, lib.oracle_lambda_returns,
                   lib.oracle_discounted_returns, lib.oracle_vtrace,
                   lib.oracle_retrace, lib.oracle_eligibility_traces,
-                  lib.oracle_episodic_prefix_sum):
+                  lib.oracle_episodic_prefix_sum, lib.oracle_affine_scan):
             f.restype = None
         _lib = lib
     return _lib
@@ -153,3 +154,14 @@ def episodic_prefix_sum(x, dones):
     out = np.empty((N, T), dtype=np.int32)
     _load().oracle_episodic_prefix_sum(N, T, _p(xx), _p(d), _p(out))
     return out.reshape(np.shape(x))
+
+
+def affine_scan(a, b, reset=None, x_init=None, reverse=False):
+    """x_t = a_t*x_{t-1} + b_t (or the reverse-time mirror), float64."""
+    N, T = _shape(a)
+    aa, bb, rr = _f32(a), _f32(b), _f32(reset)
+    x0 = _boot(x_init, N)
+    out = np.empty((N, T), dtype=np.float64)
+    _load().oracle_affine_scan(N, T, _p(aa), _p(bb), _p(rr), _p(x0), 1 if reverse else 0,
+                               _p(out))
+    return out.reshape(np.shape(a))

@@ -274,3 +274,29 @@ void oracle_episodic_prefix_sum(int64_t N, int64_t T, const int32_t *x,
     }
   }
 }
+
+/* Generic segmented first-order affine recurrence on raw coefficients
+ * (technical summary, Methodology 1: A_t = alpha_t + beta_t*A_{t+1} and its
+ * forward mirror, here with the multiplier a and addend b given directly;
+ * the Significance section points to other segmented affine recurrences):
+ *   reverse = 0:  x_t = a_t*x_{t-1} + b_t,  x_{-1} = x_init[n]
+ *   reverse = 1:  x_t = a_t*x_{t+1} + b_t,  x_T    = x_init[n]
+ * Where reset[t] is set the neighbour term is dropped: x_t = b_t.
+ * reset and x_init may be NULL (no resets, x_init = 0). */
+void oracle_affine_scan(int64_t N, int64_t T, const float *a, const float *b,
+                        const float *reset, const float *x_init, int reverse,
+                        double *x) {
+  for (int64_t n = 0; n < N; ++n) {
+    const float *ar = a + n * T, *br = b + n * T;
+    const float *rr = reset ? reset + n * T : NULL;
+    double *out = x + n * T;
+    double prev = x_init ? (double)x_init[n] : 0.0;
+    for (int64_t i = 0; i < T; ++i) {
+      int64_t t = reverse ? T - 1 - i : i;
+      double v = (double)br[t];
+      if (rr == NULL || !SET(rr, t)) v += (double)ar[t] * prev;
+      out[t] = v;
+      prev = v;
+    }
+  }
+}

@@ -105,3 +105,19 @@ def workload_inputs(w: Workload, N: int = None, T: int = None,
     return rollout(w.N if N is None else N, w.T if T is None else T,
                    w.seed if seed is None else seed, w.p_term, w.p_trunc,
                    w.log_rho_std)
+
+
+def affine_inputs(N: int, T: int, seed: int, p_reset: float = 0.01,
+                  a_max: float = 0.99) -> Dict[str, np.ndarray]:
+    """Raw coefficients for the generic affine scan: a ~ U(-a_max, a_max),
+    b ~ N(0, 1), reset ~ Bernoulli(p_reset) as 0/1 float32, x_init ~ N(0, 1)
+    per row. |a| < 1 keeps every partial sum bounded."""
+    children = np.random.SeedSequence(seed).spawn(4)
+    g = [np.random.Generator(np.random.PCG64(c)) for c in children]
+    f32 = np.float32
+    return {
+        "a": g[0].uniform(-a_max, a_max, (N, T)).astype(f32),
+        "b": g[1].standard_normal((N, T), dtype=f32),
+        "reset": (g[2].random((N, T)) < p_reset).astype(f32),
+        "x_init": g[3].standard_normal((N,), dtype=f32),
+    }

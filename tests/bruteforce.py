@@ -167,3 +167,34 @@ def episodic_prefix_sum(x, dones):
         total = (total + 2 ** 31) % 2 ** 32 - 2 ** 31
         out.append(total)
     return out
+
+
+def affine_scan(a, b, reset=None, x0=0, reverse=False):
+    """Explicit form: x_t = sum over k in the segment up to t of
+    (product of a_j for j in (k, t]) * b_k, plus the product of every a in
+    the segment times x0 when the segment reaches the origin."""
+    T = len(a)
+    order = list(range(T - 1, -1, -1)) if reverse else list(range(T))
+    pos = {t: i for i, t in enumerate(order)}   # position along the scan
+    out = [0] * T
+    for t in range(T):
+        total = 0
+        i = pos[t]
+        k = i
+        while True:
+            tk = order[k]
+            prod = 1
+            for m in range(k + 1, i + 1):
+                prod *= a[order[m]]
+            total += prod * b[tk]
+            if reset is not None and reset[tk] != 0:
+                break
+            if k == 0:
+                prod0 = 1
+                for m in range(0, i + 1):
+                    prod0 *= a[order[m]]
+                total += prod0 * x0
+                break
+            k -= 1
+        out[t] = total
+    return out

@@ -40,6 +40,9 @@ MUTANTS = {
     "elig_reset_same_step": ("if (t > 0 && !SET(d, t - 1)) e += gamma * lambda * e_prev;",
                              "if (!SET(d, t)) e += gamma * lambda * e_prev;"),
     "psum_no_reset": ("if (t > 0 && !SET(d, t - 1)) s += s_prev;", "if (t > 0) s += s_prev;"),
+    "affine_reset_ignored": ("if (rr == NULL || !SET(rr, t)) v += (double)ar[t] * prev;",
+                             "v += (double)ar[t] * prev;"),
+    "affine_init_dropped": ("double prev = x_init ? (double)x_init[n] : 0.0;", "double prev = 0.0;"),
     "psum_reset_same_step": ("if (t > 0 && !SET(d, t - 1)) s += s_prev;",
                              "if (t > 0 && !SET(d, t)) s += s_prev;"),
 }

@@ -491,3 +491,74 @@ def test_golden_worked_examples(fname):
         raise AssertionError(est)
     for k, want in case["expected"].items():
         assert close(got[k][0], want, 1e-12), (fname, k, got[k][0], want)
+
+
+# --------------------------------------------------------------------------
+# Generic affine scan (the recurrence itself, on raw coefficients)
+# --------------------------------------------------------------------------
+
+def test_affine_closed_form():
+    T, av, bv, x0 = 200, 0.97, 0.5, 3.0
+    a = np.full((1, T), av, np.float32)
+    b = np.full((1, T), bv, np.float32)
+    x = oracle.affine_scan(a, b, x_init=np.array([x0], np.float32))[0]
+    t = np.arange(T)
+    af = float(np.float32(av))
+    expect = af ** (t + 1) * x0 + bv * (1 - af ** (t + 1)) / (1 - af)
+    assert close(x, expect, 1e-12)
+
+
+def test_affine_reverse_is_mirrored_forward():
+    rng = np.random.default_rng(30)
+    a = rng.uniform(-1, 1, (3, 90)).astype(np.float32)
+    b = rng.standard_normal((3, 90)).astype(np.float32)
+    r = (rng.random((3, 90)) < 0.05).astype(np.float32)
+    x0 = rng.standard_normal(3).astype(np.float32)
+    fwd = oracle.affine_scan(a[:, ::-1], b[:, ::-1], r[:, ::-1], x0)
+    rev = oracle.affine_scan(a, b, r, x0, reverse=True)
+    assert np.array_equal(rev, fwd[:, ::-1])
+
+
+def test_affine_reset_everywhere_is_b():
+    rng = np.random.default_rng(31)
+    a = rng.standard_normal((2, 40)).astype(np.float32)
+    b = rng.standard_normal((2, 40)).astype(np.float32)
+    for rev in (False, True):
+        x = oracle.affine_scan(a, b, np.ones_like(a), np.ones(2, np.float32), reverse=rev)
+        assert np.array_equal(x, b.astype(np.float64))
+
+
+def test_affine_reproduces_gae_and_traces():
+    """The estimators are instances of the recurrence (Methodology 1): GAE's
+    coefficients in the reverse scan give the pinned GAE oracle; the traces'
+    coefficients in the forward scan give the pinned traces oracle."""
+    src = inputs(4, 70, 32, p_term=0.05, p_trunc=0.05)
+    r, v, d, B = src["rewards"], src["values"], src["terminateds"], src["bootstrap_value"]
+    tr, nv = src["truncateds"], src["next_values"]
+    g, lam = 0.5, 0.75                      # dyadic: the coefficients are exact
+    delta = oracle.gae(r, v, d, g, 0.0, B, tr, nv)        # = r + g*S - V
+    cut = (d != 0) | (tr != 0)
+    cut[:, -1] = True
+    a = np.where(cut, 0.0, g * lam).astype(np.float32)
+    want = oracle.gae(r, v, d, g, lam, B, tr, nv)
+    got = oracle.affine_scan(a, delta.astype(np.float32), reverse=True)
+    # delta was rounded to fp32 to feed the scan: compare at fp32 precision
+    assert close(got, want, 1e-6)
+    x = src["x"]
+    a2 = np.zeros_like(x)
+    a2[:, 1:] = np.where(d[:, :-1] != 0, 0.0, g * lam)
+    assert np.array_equal(oracle.affine_scan(a2, x), oracle.eligibility_traces(x, d, g, lam))
+
+
+@pytest.mark.parametrize("T", [1, 2, 5])
+def test_affine_bruteforce_exhaustive(T):
+    rng = np.random.default_rng(33 + T)
+    a = (rng.integers(-4, 5, T) / 4).astype(np.float32)
+    b = rng.integers(-4, 5, T).astype(np.float32)
+    for pat in itertools.product([0, 1], repeat=T):
+        rs = np.array(pat, np.float32)
+        for rev in (False, True):
+            got = oracle.affine_scan(a[None], b[None], rs[None], np.array([2.0], np.float32),
+                                     reverse=rev)[0]
+            want = bf.affine_scan(a.tolist(), b.tolist(), rs.tolist(), 2.0, rev)
+            assert got.tolist() == want
