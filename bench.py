@@ -61,9 +61,11 @@ BACKWARD = ("gae", "lambda_returns", "discounted_returns", "vtrace", "retrace")
 EXTRA = {
     "gae_and_returns": (("rewards", "values", "terminateds"), ("out", "out2")),
     "affine_scan": (("a", "b", "reset"), ("out",)),
+    "gae_compact": (("rewards_bf16", "values_bf16", "terminateds_u8"), ("out",)),
 }
+ELEM_BYTES = {"rewards_bf16": 2, "values_bf16": 2, "terminateds_u8": 1}   # others: 4
 SPECS = dict(ESTIMATORS, **EXTRA)
-ROW_VALUE = BACKWARD + ("gae_and_returns", "affine_scan")   # read one value per row
+ROW_VALUE = BACKWARD + ("gae_and_returns", "affine_scan", "gae_compact")  # one value per row
 
 
 def kernel_source_hash():
@@ -82,7 +84,7 @@ def kernel_source_hash():
 
 def bytes_per_env_step(est):
     ins, outs = SPECS[est]
-    return 4 * (len(ins) + len(outs))
+    return sum(ELEM_BYTES.get(k, 4) for k in ins) + 4 * len(outs)
 
 
 def bytes_per_launch(est, N, T):
@@ -320,6 +322,9 @@ def launch(rl, est, e, prm):
                                 e["bootstrap_value"], out=e["out"], out_returns=e["out2"])
     elif est == "affine_scan":
         rl.rlcs_affine_scan(e["a"], e["b"], e["reset"], e["x_init"], reverse=True, out=e["out"])
+    elif est == "gae_compact":
+        rl.rlcs_gae_compact(e["rewards_bf16"], e["values_bf16"], e["terminateds_u8"], g, lm,
+                            e["bootstrap_value"], out=e["out"])
 
 
 def capture(torch, stream, fn):
@@ -491,9 +496,12 @@ def run_ours(args):
     # entry points beyond the seven, alone, at the bench size and one long size
     next_rows = {}
     if not args.no_long_t:
-        from synthetic_rollouts import affine_inputs
+        from synthetic_rollouts import affine_inputs, compact_rollout
         for (nN, nT, seed) in ((N, T, w.seed), (256, 16384, 1004)):
             srcn = dict(rollout(nN, nT, seed, w.p_term), **affine_inputs(nN, nT, seed + 7))
+            comp, _ = compact_rollout(nN, nT, seed + 9, w.p_term)
+            srcn.update(rewards_bf16=comp["rewards"], values_bf16=comp["values"],
+                        terminateds_u8=comp["terminateds"])
             res = {}
             for est in EXTRA:
                 r_ = time_alone(torch, rl, est, srcn, dev, stream, prm, l2, nN, nT, seconds=0.08)
@@ -549,8 +557,9 @@ def time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T, seconds=0.15):
     sets = []
     for _ in range(nsets):
         e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + (row_key,)}
+        odt = torch.int32 if est == "episodic_prefix_sum" else torch.float32
         for o in outs:
-            e[o] = torch.empty_like(e[ins[0]])
+            e[o] = torch.empty(e[ins[0]].shape, dtype=odt, device=dev)
         sets.append(e)
     with torch.cuda.stream(stream):
         for e in sets:

@@ -211,6 +211,20 @@ rlcs_status rlcs_gae_and_returns(const float *rewards, const float *values,
                                  float gamma, float lambda, void *workspace,
                                  size_t workspace_bytes, rlcs_stream_t stream);
 
+/* GAE on compact inputs: the same estimator, conventions and fp32 output as
+ * rlcs_gae, reading rewards, values and next_values as bf16 (raw bf16 bit
+ * patterns, 2 bytes each) and terminateds and truncateds as uint8 masks (a
+ * byte counts as set when nonzero): 9 bytes per step read and written
+ * instead of 16 (13 instead of 24 with truncation). bootstrap_value stays
+ * float32 [N]. bf16 to fp32 conversion is exact; the arithmetic is fp32.
+ * Long rows always use the register-tile shape. */
+rlcs_status rlcs_gae_compact(const uint16_t *rewards, const uint16_t *values,
+                             const uint8_t *terminateds, const uint8_t *truncateds,
+                             const uint16_t *next_values, const float *bootstrap_value,
+                             float *advantages, int64_t N, int64_t T, float gamma,
+                             float lambda, void *workspace, size_t workspace_bytes,
+                             rlcs_stream_t stream);
+
 /* Generic segmented first-order affine recurrence on raw coefficients.
  * The recurrence of the technical summary, Methodology 1, with a and b given
  * directly (its Significance section points to other segmented affine

@@ -48,6 +48,7 @@ def _load():
         "rlcs_episodic_prefix_sum": ([P] * 3 + [I64, I64, P, SZ, P], ctypes.c_int),
         "rlcs_gae_and_returns": ([P] * 8 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
         "rlcs_affine_scan": ([P] * 5 + [I64, I64, ctypes.c_int, P, SZ, P], ctypes.c_int),
+        "rlcs_gae_compact": ([P] * 7 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -61,7 +62,7 @@ EXPORTED = ("rlcs_workspace_bytes", "rlcs_workspace_init", "rlcs_check_status",
             "rlcs_status_string", "rlcs_set_shape_override", "rlcs_gae",
             "rlcs_lambda_returns", "rlcs_discounted_returns", "rlcs_vtrace",
             "rlcs_retrace", "rlcs_eligibility_traces", "rlcs_episodic_prefix_sum",
-            "rlcs_gae_and_returns", "rlcs_affine_scan")
+            "rlcs_gae_and_returns", "rlcs_affine_scan", "rlcs_gae_compact")
 
 
 def lib():
@@ -277,6 +278,44 @@ def rlcs_affine_scan(a, b, reset=None, x_init=None, reverse=False, out=None, str
                                  1 if reverse else 0, _ptr(ws), wsb, _stream(stream)),
            "rlcs_affine_scan")
     return _finish(o, a)
+
+
+def rlcs_gae_compact(rewards, values, terminateds, gamma=0.99, lambda_=0.95,
+                     bootstrap_value=None, truncateds=None, next_values=None, out=None,
+                     stream=None):
+    """GAE from compact inputs: rewards, values, next_values as bf16 bit patterns
+    (torch.int16/uint16 or torch.bfloat16 tensors), masks as uint8 (or bool).
+    Returns float32 advantages."""
+    def bits16(t, name):
+        if t is None:
+            return None
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)
+        if t.dtype not in (torch.int16, torch.uint16):
+            raise TypeError("%s must hold bf16 bit patterns (bfloat16, int16 or uint16)" % name)
+        return _rows(t, name, dtype=t.dtype)
+
+    def mask8(t, name):
+        if t is None:
+            return None
+        if t.dtype == torch.bool:
+            t = t.view(torch.uint8)
+        return _rows(t, name, dtype=torch.uint8)
+
+    r, v = bits16(rewards, "rewards"), bits16(values, "values")
+    d = mask8(terminateds, "terminateds")
+    N, T = r.shape
+    for x, name in ((v, "values"), (d, "terminateds")):
+        if x.shape != (N, T):
+            raise ValueError("%s must have shape (%d, %d)" % (name, N, T))
+    tr, nv = mask8(truncateds, "truncateds"), bits16(next_values, "next_values")
+    b = _boot(bootstrap_value, N)
+    o = torch.empty((N, T), dtype=torch.float32, device=r.device) if out is None else out
+    ws, wsb = workspace_for(N, T, r.device, stream)
+    _check(_lib.rlcs_gae_compact(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b), _ptr(o),
+                                 N, T, gamma, lambda_, _ptr(ws), wsb, _stream(stream)),
+           "rlcs_gae_compact")
+    return o.reshape(rewards.shape)
 
 
 def rlcs_check_status(workspace=None, stream=None):

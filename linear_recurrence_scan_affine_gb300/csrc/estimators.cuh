@@ -48,10 +48,18 @@ __device__ __forceinline__ float successor(const StepIn &s, float boot, bool &cu
 
 constexpr uint32_t kTruncSlots = bit(kTau) | bit(kNV);
 
+// Element formats of the input slots. By default every slot is float32; a
+// functor that takes compact inputs names its bf16 slots (raw bf16 bits) and
+// its uint8 slots (0/1 masks), and the kernels convert them on load.
+struct F32Slots {
+  static constexpr uint32_t kBF16Slots = 0u;
+  static constexpr uint32_t kU8Slots = 0u;
+};
+
 // ---------------------------------------------------------------------------
 // GAE: alpha = r + gamma*S - V, beta = gamma*lambda (0 at a cut). Out: A.
 // ---------------------------------------------------------------------------
-struct Gae {
+struct Gae : F32Slots {
   static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
   static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
   static constexpr bool kPrevD = false;         // reads the done mask at t-1
@@ -77,7 +85,7 @@ struct Gae {
 // TD(lambda) returns: alpha = r + gamma*(1-lambda)*V_{t+1}, beta = gamma*lambda;
 // at a cut alpha = r + gamma*S, beta = 0. Out: G.
 // ---------------------------------------------------------------------------
-struct LambdaReturns {
+struct LambdaReturns : F32Slots {
   static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
   static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
   static constexpr bool kPrevD = false;         // reads the done mask at t-1
@@ -103,7 +111,7 @@ struct LambdaReturns {
 // ---------------------------------------------------------------------------
 // Discounted returns: alpha = r (+ gamma*S at a cut), beta = gamma (0 at a cut).
 // ---------------------------------------------------------------------------
-struct DiscountedReturns {
+struct DiscountedReturns : F32Slots {
   static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
   static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
   static constexpr bool kPrevD = false;         // reads the done mask at t-1
@@ -135,7 +143,7 @@ struct DiscountedReturns {
 // rho*(r + gamma*W - V) with W = vs_{t+1} (or S at a cut).
 // aux0 = gamma*rho (0 at a cut), aux1 = V.
 // ---------------------------------------------------------------------------
-struct VTrace {
+struct VTrace : F32Slots {
   static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
   static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
   static constexpr bool kPrevD = false;         // reads the done mask at t-1
@@ -172,7 +180,7 @@ struct VTrace {
 //   alpha = r + gamma*(V_{t+1} - c_{t+1}*Q_{t+1}), beta = gamma*c_{t+1};
 //   at a cut alpha = r + gamma*S, beta = 0. Out: Q^ret.
 // ---------------------------------------------------------------------------
-struct Retrace {
+struct Retrace : F32Slots {
   static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
   static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
   static constexpr bool kPrevD = false;         // reads the done mask at t-1
@@ -204,7 +212,7 @@ struct Retrace {
 // Eligibility traces (forward): alpha = x, beta = gamma*lambda*(1 - d_{t-1}),
 // beta_0 = 0 (e_{-1} = 0). Out: e.
 // ---------------------------------------------------------------------------
-struct EligibilityTraces {
+struct EligibilityTraces : F32Slots {
   static constexpr uint32_t kOptSlots = 0u;  // slots added when the optional input is given
   static constexpr bool kUsesRowValue = false;  // reads bootstrap_value[n]
   static constexpr bool kPrevD = true;         // reads the done mask at t-1
@@ -228,7 +236,7 @@ struct EligibilityTraces {
 // Episodic prefix sum (forward, int32 modulo 2^32): alpha = x, carry flag
 // m = (1 - d_{t-1}), m_0 = 0. The int32 input travels in slot R as raw bits.
 // ---------------------------------------------------------------------------
-struct EpisodicPrefixSum {
+struct EpisodicPrefixSum : F32Slots {
   static constexpr uint32_t kOptSlots = 0u;  // slots added when the optional input is given
   static constexpr bool kUsesRowValue = false;  // reads bootstrap_value[n]
   static constexpr bool kPrevD = true;         // reads the done mask at t-1
@@ -249,7 +257,7 @@ struct EpisodicPrefixSum {
 // GAE and TD(lambda) returns in one pass: the GAE pairs, with outputs
 // A_t and G_t = A_t + V_t (the identity TD(lambda) = GAE + V).
 // ---------------------------------------------------------------------------
-struct GaeAndReturns {
+struct GaeAndReturns : F32Slots {
   static constexpr uint32_t kOptSlots = kTruncSlots;
   static constexpr bool kUsesRowValue = true;
   static constexpr bool kPrevD = false;
@@ -282,7 +290,7 @@ struct GaeAndReturns {
 // step at the scan origin folds x_init into its addend.
 // ---------------------------------------------------------------------------
 template <bool BACKWARD>
-struct Affine {
+struct Affine : F32Slots {
   static constexpr uint32_t kOptSlots = bit(kD);
   static constexpr bool kUsesRowValue = true;
   static constexpr bool kPrevD = false;
@@ -302,6 +310,17 @@ struct Affine {
   __device__ static __forceinline__ float out0(float A, float, const Pair &, float, float) {
     return A;
   }
+};
+
+// ---------------------------------------------------------------------------
+// GAE on compact inputs: rewards, values and next_values as bf16, terminated
+// and truncated masks as uint8 (9 bytes per step read+written instead of 16
+// without truncation). The arithmetic is GAE's, in fp32, on the converted
+// values (bf16 -> fp32 is exact; a mask byte counts as set when nonzero).
+// ---------------------------------------------------------------------------
+struct GaeCompact : Gae {
+  static constexpr uint32_t kBF16Slots = bit(kR) | bit(kV) | bit(kNV);
+  static constexpr uint32_t kU8Slots = bit(kD) | bit(kTau);
 };
 
 }  // namespace rlcs

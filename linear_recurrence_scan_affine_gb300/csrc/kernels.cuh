@@ -101,6 +101,73 @@ __device__ __forceinline__ void store4(float *row, int64_t t, int64_t T, bool ve
     if (t + i < T) row[t + i] = f4get(v, i);
 }
 
+// Typed access to input slot k of estimator E (float32, bf16 bits or uint8
+// masks), converting to float. `off` counts elements from the slot's start.
+template <class E>
+__host__ __device__ constexpr int slot_bytes(int k) {
+  return (E::kBF16Slots & bit(k)) ? 2 : ((E::kU8Slots & bit(k)) ? 1 : 4);
+}
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t h) { return __uint_as_float(h << 16); }
+__device__ __forceinline__ float mask_byte(uint32_t b) { return (b & 0xffu) ? 1.0f : 0.0f; }
+
+// Four consecutive steps starting at row + t (t % 4 == 0); steps past T read 0.
+template <class E>
+__device__ __forceinline__ float4 load_slot4(const Params &p, int k, int64_t row, int64_t t,
+                                             int64_t T, bool vec) {
+  if (E::kBF16Slots & bit(k)) {
+    const uint16_t *r = reinterpret_cast<const uint16_t *>(p.in[k]) + row;
+    float4 v = f4zero();
+    if (vec) {
+      if (t < T) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2 *>(r + t));
+        v = make_float4(bf16_bits_to_float(u.x & 0xffffu), bf16_bits_to_float(u.x >> 16),
+                        bf16_bits_to_float(u.y & 0xffffu), bf16_bits_to_float(u.y >> 16));
+      }
+      return v;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (t + i < T) f4set(v, i, bf16_bits_to_float(__ldg(r + t + i)));
+    return v;
+  }
+  if (E::kU8Slots & bit(k)) {
+    const uint8_t *r = reinterpret_cast<const uint8_t *>(p.in[k]) + row;
+    float4 v = f4zero();
+    if (vec) {
+      if (t < T) {
+        const uint32_t u = __ldg(reinterpret_cast<const unsigned int *>(r + t));
+        v = make_float4(mask_byte(u), mask_byte(u >> 8), mask_byte(u >> 16), mask_byte(u >> 24));
+      }
+      return v;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (t + i < T) f4set(v, i, mask_byte(__ldg(r + t + i)));
+    return v;
+  }
+  return load4(p.in[k] + row, t, T, vec);
+}
+
+// One step of slot k at element offset `off` from the slot's start.
+template <class E>
+__device__ __forceinline__ float load_slot1(const Params &p, int k, int64_t off) {
+  if (E::kBF16Slots & bit(k))
+    return bf16_bits_to_float(__ldg(reinterpret_cast<const uint16_t *>(p.in[k]) + off));
+  if (E::kU8Slots & bit(k))
+    return mask_byte(__ldg(reinterpret_cast<const uint8_t *>(p.in[k]) + off));
+  return __ldg(p.in[k] + off);
+}
+
+// L2 bulk prefetch of n elements of slot k from element offset `off`, when
+// the range is 16-byte aligned in start and length (a hint: skipped if not).
+template <class E>
+__device__ __forceinline__ void prefetch_slot(const Params &p, int k, int64_t off, int64_t n) {
+  const char *a = reinterpret_cast<const char *>(p.in[k]) + off * slot_bytes<E>(k);
+  const int64_t bytes = n * slot_bytes<E>(k);
+  if (((reinterpret_cast<uintptr_t>(a) | (uintptr_t)bytes) & 15u) == 0 && bytes > 0)
+    prefetch_l2(a, (uint32_t)bytes);
+}
+
 // The step after each of a lane's four steps: lanes pass their first element
 // down; lane 31 takes `following` (first step after the strip).
 __device__ __forceinline__ float4 next4(const float4 &a, float following, int lane) {
@@ -349,7 +416,7 @@ __global__ void __launch_bounds__(kRowWarps * 32) warp_row_kernel(Params p) {
   if (vec && lane == 0 && row < p.N) {
 #pragma unroll
     for (int k = 0; k < kNumSlots; ++k)
-      if (St::kUse & bit(k)) prefetch_l2(p.in[k] + base, (uint32_t)(T * 4));
+      if (St::kUse & bit(k)) prefetch_slot<E>(p, k, base, T);
   }
   pdl_wait();
   if (row >= p.N) return;  // whole warp leaves together
@@ -359,7 +426,8 @@ __global__ void __launch_bounds__(kRowWarps * 32) warp_row_kernel(Params p) {
   for (int k = 0; k < kNumSlots; ++k) {
 #pragma unroll
     for (int j = 0; j < S; ++j)
-      raw[k][j] = (St::kUse & bit(k)) ? load4(p.in[k] + base, (int64_t)j * kStrip + 4 * lane, T, vec)
+      raw[k][j] = (St::kUse & bit(k)) ? load_slot4<E>(p, k, base, (int64_t)j * kStrip + 4 * lane,
+                                                      T, vec)
                                       : f4zero();
   }
   const float boot = (E::kUsesRowValue && p.boot) ? __ldg(p.boot + row) : 0.f;
@@ -681,11 +749,12 @@ struct TileShape {
   int64_t total_tiles;    // N * Q = grid size
 };
 
-// Resident blocks per SM the compiler must allow: 4096-step tiles keep more
-// state per thread and are used when the whole grid fits in about one wave
-// (2 per SM); shorter tiles are capped at 64 registers so 4 blocks share an
-// SM and one block's look-back overlaps the others' loads.
-template <int S> struct TileMinBlocks { static constexpr int value = S >= 4 ? 2 : 4; };
+// Resident blocks per SM the compiler must allow (measured on GB300):
+// 4096-step tiles keep more state per thread and are used when the whole
+// grid fits in about one wave (2 per SM); 2048-step tiles are capped at 64
+// registers (4 per SM) and 1024-step tiles at 40 (6 per SM), so one block's
+// look-back overlaps the others' loads.
+template <int S> struct TileMinBlocks { static constexpr int value = S >= 4 ? 2 : (S == 2 ? 4 : 6); };
 
 template <class E, bool TRUNC, int S>
 __global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
@@ -713,7 +782,7 @@ __global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
     const int64_t len = (T - t0 < C) ? (T - t0) : C;
 #pragma unroll
     for (int k = 0; k < kNumSlots; ++k)
-      if (kUse & bit(k)) prefetch_l2(p.in[k] + base + t0, (uint32_t)(len * 4));
+      if (kUse & bit(k)) prefetch_slot<E>(p, k, base + t0, len);
   }
   pdl_wait();
 
@@ -723,17 +792,17 @@ __global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
   for (int k = 0; k < kNumSlots; ++k) {
 #pragma unroll
     for (int j = 0; j < S; ++j)
-      raw[k][j] = (kUse & bit(k)) ? load4(p.in[k] + base, t_span + (int64_t)j * kStrip + 4 * lane,
-                                          T, vec)
+      raw[k][j] = (kUse & bit(k)) ? load_slot4<E>(p, k, base,
+                                                  t_span + (int64_t)j * kStrip + 4 * lane, T, vec)
                                   : f4zero();
   }
   float halo[kNumSlots];
 #pragma unroll
   for (int k = 0; k < kNumSlots; ++k) {
     const int64_t th = t_span + (int64_t)kStrip * S;  // first step after the span
-    halo[k] = (E::kBackward && (E::kNext & bit(k)) && th < T) ? __ldg(p.in[k] + base + th) : 0.f;
+    halo[k] = (E::kBackward && (E::kNext & bit(k)) && th < T) ? load_slot1<E>(p, k, base + th) : 0.f;
   }
-  const float halo_d = (E::kPrevD && t_span > 0) ? __ldg(p.in[kD] + base + t_span - 1) : 0.f;
+  const float halo_d = (E::kPrevD && t_span > 0) ? load_slot1<E>(p, kD, base + t_span - 1) : 0.f;
   const float boot = (E::kUsesRowValue && p.boot) ? __ldg(p.boot + row) : 0.f;
   if (tid == 0 && Q > 1) s_epoch = ld_relaxed_gpu(&ts.ws->epoch);  // after the loads issue
   pdl_launch_dependents();

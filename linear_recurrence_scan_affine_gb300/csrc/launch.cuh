@@ -39,23 +39,31 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
     const dim3 grid((unsigned)((p.N + kRowWarps - 1) / kRowWarps));
     return launch_ex(warp_row_kernel<E, TRUNC, S>, grid, dim3(kRowWarps * 32), 0, s, plan.pdl, p);
   }
-  if (plan.shape == RLCS_SHAPE_BLOCK_TILE) {
+  if constexpr ((E::kBF16Slots | E::kU8Slots) != 0u) {
+    // compact inputs are never staged through shared memory: the tile shape
+    // serves every long-row plan
     TileShape ts{plan.Q > 1 ? ws : nullptr, plan.Q, p.N * plan.Q};
     return launch_ex(block_tile_kernel<E, TRUNC, S>, dim3((unsigned)(p.N * plan.Q)),
                      dim3(kChunkThreads), 0, s, plan.pdl, p, ts);
+  } else {
+    if (plan.shape == RLCS_SHAPE_BLOCK_TILE) {
+      TileShape ts{plan.Q > 1 ? ws : nullptr, plan.Q, p.N * plan.Q};
+      return launch_ex(block_tile_kernel<E, TRUNC, S>, dim3((unsigned)(p.N * plan.Q)),
+                       dim3(kChunkThreads), 0, s, plan.pdl, p, ts);
+    }
+    constexpr uint32_t kUse = Strips<E, TRUNC, S>::kUse;
+    constexpr size_t smem = (size_t)__builtin_popcount(kUse) * kChunkWarps * kStrip * S * 4;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+      attr_err = cudaFuncSetAttribute(block_chunk_kernel<E, TRUNC, S>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    ChunkShape cs{ws, plan.Q, p.N * plan.Q};
+    return launch_ex(block_chunk_kernel<E, TRUNC, S>, dim3((unsigned)(p.N * plan.Q)),
+                     dim3(kChunkThreads), smem, s, plan.pdl, p, cs);
   }
-  constexpr uint32_t kUse = Strips<E, TRUNC, S>::kUse;
-  constexpr size_t smem = (size_t)__builtin_popcount(kUse) * kChunkWarps * kStrip * S * 4;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(block_chunk_kernel<E, TRUNC, S>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
-  ChunkShape cs{ws, plan.Q, p.N * plan.Q};
-  return launch_ex(block_chunk_kernel<E, TRUNC, S>, dim3((unsigned)(p.N * plan.Q)),
-                   dim3(kChunkThreads), smem, s, plan.pdl, p, cs);
 }
 
 template <class E, bool TRUNC>
@@ -86,6 +94,7 @@ cudaError_t launch_retrace(const Params &, const Plan &, WsHeader *, cudaStream_
 cudaError_t launch_eligibility_traces(const Params &, const Plan &, WsHeader *, cudaStream_t);
 cudaError_t launch_episodic_prefix_sum(const Params &, const Plan &, WsHeader *, cudaStream_t);
 cudaError_t launch_gae_and_returns(const Params &, const Plan &, WsHeader *, cudaStream_t);
+cudaError_t launch_gae_compact(const Params &, const Plan &, WsHeader *, cudaStream_t);
 cudaError_t launch_affine_forward(const Params &, const Plan &, WsHeader *, cudaStream_t);
 cudaError_t launch_affine_backward(const Params &, const Plan &, WsHeader *, cudaStream_t);
 

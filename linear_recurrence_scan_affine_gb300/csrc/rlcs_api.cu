@@ -83,10 +83,11 @@ bool overlaps(const Buf &a, const Buf &b) {
 // Shared tail of every entry point.
 // `opt`: the estimator's optional inputs are present (the truncation pair,
 // or the affine scan's reset mask already placed in p.in).
+// `esize`: bytes per element of each input slot (NULL: all float32).
 template <class Launch>
 rlcs_status run(Params &p, const float *trunc, const float *next_values, void *const *outs,
                 int n_outs, void *ws, size_t ws_bytes, cudaStream_t stream, Launch launch,
-                bool opt) {
+                bool opt, const int *esize = nullptr) {
   const int64_t N = p.N, T = p.T;
   if (N <= 0 || T <= 0) return RLCS_ERR_INVALID_ARG;
   if (N > (int64_t)(INT64_MAX / 4) / T) return RLCS_ERR_INVALID_ARG;
@@ -101,8 +102,10 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
     if (!outs[o]) continue;
     if (!aligned16(outs[o])) vec = false;
     const Buf ob{outs[o], plane};
-    for (int k = 0; k < kNumSlots; ++k)
-      if (overlaps(ob, Buf{p.in[k], plane})) return RLCS_ERR_INVALID_ARG;
+    for (int k = 0; k < kNumSlots; ++k) {
+      const size_t in_plane = (size_t)N * (size_t)T * (size_t)(esize ? esize[k] : 4);
+      if (overlaps(ob, Buf{p.in[k], in_plane})) return RLCS_ERR_INVALID_ARG;
+    }
     if (overlaps(ob, Buf{p.boot, (size_t)N * 4u})) return RLCS_ERR_INVALID_ARG;
     for (int o2 = o + 1; o2 < n_outs; ++o2)
       if (overlaps(ob, Buf{outs[o2], plane})) return RLCS_ERR_INVALID_ARG;
@@ -119,9 +122,10 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
       if (!ws || ws_bytes < ws_bytes_for(N, plan.Q) || !aligned16(ws)) return RLCS_ERR_WORKSPACE;
     }
     if (ws && ws_bytes >= sizeof(WsHeader) && aligned16(ws)) wsh = static_cast<WsHeader *>(ws);
-    for (const Buf &b : {Buf{ws, ws_bytes}})
-      for (int k = 0; k < kNumSlots; ++k)
-        if (overlaps(b, Buf{p.in[k], plane})) return RLCS_ERR_INVALID_ARG;
+    for (int k = 0; k < kNumSlots; ++k) {
+      const size_t in_plane = (size_t)N * (size_t)T * (size_t)(esize ? esize[k] : 4);
+      if (overlaps(Buf{ws, ws_bytes}, Buf{p.in[k], in_plane})) return RLCS_ERR_INVALID_ARG;
+    }
   }
   const cudaError_t err = launch(p, plan, wsh, stream);
   if (err != cudaSuccess) {
@@ -354,6 +358,29 @@ extern "C" rlcs_status rlcs_gae_and_returns(const float *rewards, const float *v
   return run(p, truncateds, next_values, outs, 2, workspace, workspace_bytes,
              reinterpret_cast<cudaStream_t>(stream), launch_gae_and_returns,
              truncateds != nullptr);
+}
+
+extern "C" rlcs_status rlcs_gae_compact(const uint16_t *rewards, const uint16_t *values,
+                                        const uint8_t *terminateds, const uint8_t *truncateds,
+                                        const uint16_t *next_values,
+                                        const float *bootstrap_value, float *advantages,
+                                        int64_t N, int64_t T, float gamma, float lambda,
+                                        void *workspace, size_t workspace_bytes,
+                                        rlcs_stream_t stream) {
+  if (!rewards || !values || !terminateds || !advantages) return RLCS_ERR_INVALID_ARG;
+  Params p = base_params(N, T, bootstrap_value);
+  p.in[kR] = reinterpret_cast<const float *>(rewards);
+  p.in[kV] = reinterpret_cast<const float *>(values);
+  p.in[kD] = reinterpret_cast<const float *>(terminateds);
+  p.out0 = advantages;
+  p.gamma = gamma;
+  p.lambda = lambda;
+  void *outs[1] = {advantages};
+  static const int esize[kNumSlots] = {2, 2, 4, 4, 1, 1, 2};  // R V Q LR D Tau NV
+  return run(p, reinterpret_cast<const float *>(truncateds),
+             reinterpret_cast<const float *>(next_values), outs, 1, workspace, workspace_bytes,
+             reinterpret_cast<cudaStream_t>(stream), launch_gae_compact, truncateds != nullptr,
+             esize);
 }
 
 extern "C" rlcs_status rlcs_affine_scan(const float *a, const float *b, const float *reset,

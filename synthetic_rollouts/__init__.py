@@ -121,3 +121,35 @@ def affine_inputs(N: int, T: int, seed: int, p_reset: float = 0.01,
         "reset": (g[2].random((N, T)) < p_reset).astype(f32),
         "x_init": g[3].standard_normal((N,), dtype=f32),
     }
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bf16 bit patterns (uint16), round to nearest even."""
+    b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((b + 0x7FFF + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> float32, exact."""
+    return (np.ascontiguousarray(h).astype(np.uint32) << 16).view(np.float32)
+
+
+def compact_rollout(N: int, T: int, seed: int, p_term: float, p_trunc: float = 0.0):
+    """A rollout in compact formats: rewards, values, next_values as bf16 bit
+    patterns (held as int16, which every torch version can move to a GPU),
+    masks as uint8; bootstrap_value float32. Returns (compact, float32 view)
+    where the float32 view holds exactly the values the compact arrays
+    encode, for the oracle."""
+    src = rollout(N, T, seed, p_term, p_trunc)
+    comp = {"bootstrap_value": src["bootstrap_value"]}
+    f32 = {"bootstrap_value": src["bootstrap_value"]}
+    for k in ("rewards", "values", "next_values"):
+        if k in src:
+            bits = to_bf16_bits(src[k])
+            comp[k] = bits.view(np.int16)
+            f32[k] = bf16_bits_to_f32(bits)
+    for k in ("terminateds", "truncateds"):
+        if k in src:
+            comp[k] = (src[k] != 0).astype(np.uint8)
+            f32[k] = comp[k].astype(np.float32)
+    return comp, f32

@@ -152,3 +152,18 @@ def test_shape_override_validation(lib):
 
 def test_workspace_init_rejects_null(lib):
     assert lib.rlcs_workspace_init(None, 64, None) == INVALID
+
+
+def test_compact_overlap_uses_element_sizes(lib):
+    # A uint8 mask plane of N*T bytes ends before an output placed right after
+    # it, although N*T float32 elements would reach into it. The rows are long
+    # and no workspace is given, so a call that passes the overlap check stops
+    # at the workspace check: nothing is ever launched on these fake pointers.
+    N, T = 4, 16384                                 # four 4096-step tiles per row
+    r, v, d = fake(0), fake(1), fake(2)
+    out = ctypes.c_void_p(d.value + N * T)          # right after the uint8 masks
+    assert lib.rlcs_gae_compact(r, v, d, None, None, None, out, N, T, 0.99, 0.95, None, 0,
+                                None) == WORKSPACE
+    inside = ctypes.c_void_p(d.value + N * T - 16)  # overlapping the masks
+    assert lib.rlcs_gae_compact(r, v, d, None, None, None, inside, N, T, 0.99, 0.95, None, 0,
+                                None) == INVALID

@@ -96,3 +96,41 @@ def test_affine_scan_shapes(rl, shape, chunk, T, reverse):
         _affine(rl, 3, T, 8100 + T, reverse, True, True, offset=1)   # unaligned rows
     finally:
         rl.rlcs_set_shape_override(rl.RLCS_SHAPE_AUTO, 0)
+
+
+# --------------------------------------------------------------------------
+# Compact input formats: bf16 rewards/values/next_values, uint8 masks
+# --------------------------------------------------------------------------
+
+def _compact(rl, N, T, seed, trunc, offset=0):
+    from synthetic_rollouts import compact_rollout
+    comp, f32 = compact_rollout(N, T, seed, p_term=0.01, p_trunc=0.005 if trunc else 0.0)
+    g = to_dev(comp, torch.device("cuda:0"), offset=offset)
+    kw = dict(truncateds=g["truncateds"], next_values=g["next_values"]) if trunc else {}
+    got = rl.rlcs_gae_compact(g["rewards"], g["values"], g["terminateds"], 0.99, 0.95,
+                              g["bootstrap_value"], **kw)
+    kwn = dict(truncateds=f32["truncateds"], next_values=f32["next_values"]) if trunc else {}
+    # the oracle sees exactly the values the compact arrays encode
+    want = oracle.gae(f32["rewards"], f32["values"], f32["terminateds"], 0.99, 0.95,
+                      f32["bootstrap_value"], **kwn)
+    compare("gae", {"out": got}, {"out": want}, TOL)
+    rl.check_all_workspaces()
+
+
+@pytest.mark.parametrize("N,T", [(4096, 128), (64, 512), (256, 4096), (256, 16384)])
+@pytest.mark.parametrize("trunc", [False, True])
+def test_gae_compact_sizes(rl, N, T, trunc):
+    _compact(rl, N, T, 9000 + T, trunc)
+
+
+@pytest.mark.parametrize("shape,chunk", SHAPES)
+@pytest.mark.parametrize("T", [1, 3, 130, 511, 2049, 7000])
+def test_gae_compact_shapes(rl, shape, chunk, T):
+    if shape == 1 and T > 512:
+        pytest.skip("warp-row shape is for T <= 512")
+    rl.rlcs_set_shape_override(shape, chunk)
+    try:
+        _compact(rl, 5, T, 9100 + T, True)
+        _compact(rl, 3, T, 9200 + T, True, offset=1)   # unaligned rows: scalar loads
+    finally:
+        rl.rlcs_set_shape_override(rl.RLCS_SHAPE_AUTO, 0)
