@@ -148,6 +148,35 @@ __device__ __forceinline__ float4 load_slot4(const Params &p, int k, int64_t row
   return load4(p.in[k] + row, t, T, vec);
 }
 
+// Vector path for register-loaded spans: the lane's four steps of strip j,
+// at element offset lane_off + 128*j of slot k; `left` = steps from the
+// lane's first step to the row end (the strip is past the end when
+// 128*j >= left). The slot pointer plus lane_off is formed once per slot and
+// every strip adds an immediate, so a load costs one instruction and the
+// bounds test one compare per strip.
+template <class E>
+__device__ __forceinline__ float4 load_lane4(const Params &p, int k, int64_t lane_off, int j,
+                                             int left) {
+  if (j * kStrip >= left) return f4zero();
+  if (E::kBF16Slots & bit(k)) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(
+        reinterpret_cast<const uint16_t *>(p.in[k]) + lane_off + j * kStrip));
+    return make_float4(bf16_bits_to_float(u.x & 0xffffu), bf16_bits_to_float(u.x >> 16),
+                       bf16_bits_to_float(u.y & 0xffffu), bf16_bits_to_float(u.y >> 16));
+  }
+  if (E::kU8Slots & bit(k)) {
+    const uint32_t u = __ldg(reinterpret_cast<const unsigned int *>(
+        reinterpret_cast<const uint8_t *>(p.in[k]) + lane_off + j * kStrip));
+    return make_float4(mask_byte(u), mask_byte(u >> 8), mask_byte(u >> 16), mask_byte(u >> 24));
+  }
+  return __ldg(reinterpret_cast<const float4 *>(p.in[k] + lane_off + j * kStrip));
+}
+
+__device__ __forceinline__ void store_lane4(float *out, int64_t lane_off, int j, int left,
+                                            float4 v) {
+  if (j * kStrip < left) *reinterpret_cast<float4 *>(out + lane_off + j * kStrip) = v;
+}
+
 // One step of slot k at element offset `off` from the slot's start.
 template <class E>
 __device__ __forceinline__ float load_slot1(const Params &p, int k, int64_t off) {
@@ -259,7 +288,13 @@ struct Strips {
   P excl[S], tot[S];
 
   // t_span: the span's first step within the row; T: the row length.
-  template <class Src>
+  // ZERO_PAD: steps past the row end arrive as zeros (register-loaded spans).
+  // Their coefficients are then finite, and they never reach a real output:
+  // a backward row's last step has beta = 0 (it is a cut), and a forward
+  // row's padding comes after every real step. So they need no per-step
+  // identity mask. Spans staged in shared memory (uninitialised past the end)
+  // keep the mask.
+  template <bool ZERO_PAD = false, class Src>
   __device__ __forceinline__ void build(const Params &p, const Src &src, float boot,
                                         int64_t t_span, int64_t T, int lane) {
     // Per-element bounds in 32-bit offsets from the span start: steps left in
@@ -272,13 +307,13 @@ struct Strips {
       // A strip wholly inside the row, and not holding the row's last step,
       // needs no per-step bound checks (uniform across the warp).
       if ((j + 1) * kStrip < rem && !(at_origin && j == 0))
-        build_strip<true>(p, src, boot, j, rem, false, lane);
+        build_strip<true, ZERO_PAD>(p, src, boot, j, rem, false, lane);
       else
-        build_strip<false>(p, src, boot, j, rem, at_origin, lane);
+        build_strip<false, ZERO_PAD>(p, src, boot, j, rem, at_origin, lane);
     }
   }
 
-  template <bool FULL, class Src>
+  template <bool FULL, bool ZERO_PAD, class Src>
   __device__ __forceinline__ void build_strip(const Params &p, const Src &src, float boot, int j,
                                               int rem, bool at_origin, int lane) {
     float4 raw[kNumSlots], nx[kNumSlots];
@@ -311,7 +346,7 @@ struct Strips {
       float a0 = 0.f, a1 = 0.f;
       P e;
       E::template coeff<TRUNC>(p, s, boot, e, a0, a1);
-      if (!FULL && o >= rem) e = identity(P{});  // ragged tail: padding is the identity
+      if (!FULL && !ZERO_PAD && o >= rem) e = identity(P{});  // padding is the identity
       el[j][i] = e;
       aux0[j][i] = a0;
       aux1[j][i] = a1;
@@ -421,14 +456,20 @@ __global__ void __launch_bounds__(kRowWarps * 32) warp_row_kernel(Params p) {
   pdl_wait();
   if (row >= p.N) return;  // whole warp leaves together
 
+  const int64_t lane_off = base + 4 * lane;
+  const int left = (int)(T - 4 * lane);  // T <= 512 in this tier
   float4 raw[kNumSlots][S];
 #pragma unroll
   for (int k = 0; k < kNumSlots; ++k) {
 #pragma unroll
-    for (int j = 0; j < S; ++j)
-      raw[k][j] = (St::kUse & bit(k)) ? load_slot4<E>(p, k, base, (int64_t)j * kStrip + 4 * lane,
-                                                      T, vec)
-                                      : f4zero();
+    for (int j = 0; j < S; ++j) {
+      if (!(St::kUse & bit(k)))
+        raw[k][j] = f4zero();
+      else if (vec)
+        raw[k][j] = load_lane4<E>(p, k, lane_off, j, left);
+      else
+        raw[k][j] = load_slot4<E>(p, k, base, (int64_t)j * kStrip + 4 * lane, T, false);
+    }
   }
   const float boot = (E::kUsesRowValue && p.boot) ? __ldg(p.boot + row) : 0.f;
   pdl_launch_dependents();
@@ -438,16 +479,23 @@ __global__ void __launch_bounds__(kRowWarps * 32) warp_row_kernel(Params p) {
   for (int k = 0; k < kNumSlots; ++k) halo[k] = 0.f;  // past the row end: never used
   const RegSource<S> src{raw, halo, 0.f, lane};
   St st;
-  st.build(p, src, boot, 0, T, lane);
+  st.template build<true>(p, src, boot, 0, T, lane);
   st.scan(lane);
   float4 o0[S], o1[S];
   st.finish(V(0), o0, o1);
 #pragma unroll
   for (int j = 0; j < S; ++j) {
-    const int64_t t = (int64_t)j * kStrip + 4 * lane;
-    store4(static_cast<float *>(p.out0) + base, t, T, vec, o0[j]);
-    if constexpr (E::kOuts > 1) {
-      if (p.out1) store4(p.out1 + base, t, T, vec, o1[j]);
+    if (vec) {
+      store_lane4(static_cast<float *>(p.out0), lane_off, j, left, o0[j]);
+      if constexpr (E::kOuts > 1) {
+        if (p.out1) store_lane4(p.out1, lane_off, j, left, o1[j]);
+      }
+    } else {
+      const int64_t t = (int64_t)j * kStrip + 4 * lane;
+      store4(static_cast<float *>(p.out0) + base, t, T, false, o0[j]);
+      if constexpr (E::kOuts > 1) {
+        if (p.out1) store4(p.out1 + base, t, T, false, o1[j]);
+      }
     }
   }
 }
@@ -787,14 +835,21 @@ __global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
   pdl_wait();
 
   const int64_t t_span = t0 + span_off;
+  const int64_t lane_off = base + t_span + 4 * lane;
+  const int64_t left64 = T - t_span - 4 * lane;
+  const int left = left64 > (int64_t)(1 << 30) ? (1 << 30) : (int)left64;
   float4 raw[kNumSlots][S];
 #pragma unroll
   for (int k = 0; k < kNumSlots; ++k) {
 #pragma unroll
-    for (int j = 0; j < S; ++j)
-      raw[k][j] = (kUse & bit(k)) ? load_slot4<E>(p, k, base,
-                                                  t_span + (int64_t)j * kStrip + 4 * lane, T, vec)
-                                  : f4zero();
+    for (int j = 0; j < S; ++j) {
+      if (!(kUse & bit(k)))
+        raw[k][j] = f4zero();
+      else if (vec)
+        raw[k][j] = load_lane4<E>(p, k, lane_off, j, left);
+      else
+        raw[k][j] = load_slot4<E>(p, k, base, t_span + (int64_t)j * kStrip + 4 * lane, T, false);
+    }
   }
   float halo[kNumSlots];
 #pragma unroll
@@ -809,7 +864,7 @@ __global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
 
   const RegSource<S> src{raw, halo, halo_d, lane};
   St st;
-  st.build(p, src, boot, t_span, T, lane);
+  st.template build<true>(p, src, boot, t_span, T, lane);
   const P wagg = st.scan(lane);
   if (lane == 0) s_warp[warp] = wagg;
   __syncthreads();
@@ -841,10 +896,17 @@ __global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
   st.finish(s_carry[warp], o0, o1);
 #pragma unroll
   for (int j = 0; j < S; ++j) {
-    const int64_t t = t_span + (int64_t)j * kStrip + 4 * lane;
-    store4(static_cast<float *>(p.out0) + base, t, T, vec, o0[j]);
-    if constexpr (E::kOuts > 1) {
-      if (p.out1) store4(p.out1 + base, t, T, vec, o1[j]);
+    if (vec) {
+      store_lane4(static_cast<float *>(p.out0), lane_off, j, left, o0[j]);
+      if constexpr (E::kOuts > 1) {
+        if (p.out1) store_lane4(p.out1, lane_off, j, left, o1[j]);
+      }
+    } else {
+      const int64_t t = t_span + (int64_t)j * kStrip + 4 * lane;
+      store4(static_cast<float *>(p.out0) + base, t, T, false, o0[j]);
+      if constexpr (E::kOuts > 1) {
+        if (p.out1) store4(p.out1 + base, t, T, false, o1[j]);
+      }
     }
   }
   if (Q > 1 && tid == 0) finish_launch(ts.ws, ts.total_tiles, s_epoch);
