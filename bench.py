@@ -76,6 +76,8 @@ def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "linear_recurrence_scan_affine_gb300", "csrc")
     for f in sorted(glob.glob(os.path.join(csrc, "*.cu*"))):
+        if os.path.basename(f) == "diag.cu":  # the diagnostic, not an estimator kernel
+            continue
         h.update(os.path.basename(f).encode())
         with open(f, "rb") as fh:
             h.update(fh.read())
@@ -475,6 +477,18 @@ def run_ours(args):
                 "us_per_launch": per_est[dom]["us_per_launch"],
                 "timing": "kernel alone: CUDA graph of back-to-back launches, each on its own "
                           "buffer set (rotation >= 3x L2), CUDA events on the launching stream"}
+    # what any launch of this size and shape costs: the diagnostic copy of the
+    # same bytes, and the same grid doing nothing
+    n_arrays = len(SPECS[dom][0]) + len(SPECS[dom][1])
+    copy_us = time_diag(torch, rl, n_arrays, dev, stream, l2, N, T, False)
+    empty_us = time_diag(torch, rl, n_arrays, dev, stream, l2, N, T, True)
+    roofline["reference"] = {
+        "stream_copy_us": copy_us, "empty_launch_us": empty_us,
+        "stream_copy_frac": bytes_per_launch(dom, N, T) / (copy_us * 1e-6) / 1e9 / peak,
+        "kernel_over_copy": per_est[dom]["us_per_launch"] / copy_us,
+        "what": "rlcs_diag_stream_copy: the warp-row launch shape moving the same bytes with no "
+                "scan (same prefetch and programmatic dependent launch); empty = the same grid "
+                "that only waits and exits"}
 
     # the long-row recipes, every estimator alone (same method as above)
     long_t = {}
@@ -577,6 +591,31 @@ def time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T, seconds=0.15):
             "gbs": bytes_per_launch(est, N, T) / sec / 1e9,
             "bytes_per_env_step": bytes_per_env_step(est), "rotating_sets": nsets,
             "footprint_over_l2": nsets * set_bytes / l2}
+
+
+def time_diag(torch, rl, n_arrays, dev, stream, l2, N, T, empty, seconds=0.1):
+    """The library's diagnostic stream copy in the warp-row launch shape:
+    n_arrays - 1 inputs summed into one output (the same bytes per launch as
+    an estimator with n_arrays arrays), back to back on rotating buffers; with
+    `empty` the same grid only waits and exits. Returns us per launch."""
+    n_in = max(1, n_arrays - 1)
+    set_bytes = n_arrays * N * T * 4
+    nsets = int(min(256, max(8, -(-3 * l2 // set_bytes))))
+    sets = [([torch.zeros(N, T, device=dev) for _ in range(n_in)], torch.empty(N, T, device=dev))
+            for _ in range(nsets)]
+    with torch.cuda.stream(stream):
+        for ins, out in sets:
+            rl.rlcs_diag_stream_copy(ins, out, empty)
+    torch.cuda.synchronize()
+    g = capture(torch, stream, lambda: [rl.rlcs_diag_stream_copy(i, o, empty) for i, o in sets])
+    with torch.cuda.stream(stream):
+        g.replay()
+    once = time_graph(torch, stream, g, 1)
+    reps = max(3, int(seconds / max(1e-6, once)))
+    sec = time_graph(torch, stream, g, reps) / (reps * nsets)
+    del g, sets
+    torch.cuda.synchronize()
+    return sec * 1e6
 
 
 def run_e2e(torch, rl, src, dev, stream, prm, order, steps, N, T, depth=2, block=16):

@@ -267,6 +267,16 @@ rlcs_status rlcs_gae_noalloc(const float *rewards, const float *values,
                              float *advantages, int64_t N, int64_t T, float gamma,
                              float lambda, rlcs_stream_t stream);
 
+/* Diagnostic, not an estimator: the warp-row shape's launch and data
+ * movement with no scan, for measuring what a launch of a given size costs
+ * before any estimator work. Reads n_inputs [N,T] float32 arrays (1..7,
+ * 16-byte aligned, T % 4 == 0) and writes their elementwise sum to `out`,
+ * with the same L2 prefetch and programmatic dependent launch as the
+ * estimators; with `empty` nonzero the same grid only waits and exits.
+ * Asynchronous on `stream`; RLCS_ERR_INVALID_ARG for bad arguments. */
+rlcs_status rlcs_diag_stream_copy(const float *const *inputs, int n_inputs, float *out,
+                                  int64_t N, int64_t T, int empty, rlcs_stream_t stream);
+
 /* Launch-shape selection, exposed for testing and tuning. The library picks
  * a shape from (N, T) and the SM count:
  *   RLCS_SHAPE_WARP_ROW    one warp per row, inputs in registers (T <= 512);

@@ -12,5 +12,5 @@ from .binding import (  # noqa: F401
     check_all_workspaces, lib, rlcs_check_status, rlcs_discounted_returns,
     rlcs_eligibility_traces, rlcs_episodic_prefix_sum, rlcs_gae, rlcs_lambda_returns,
     rlcs_retrace, rlcs_set_shape_override, rlcs_vtrace, rlcs_workspace_bytes,
-    rlcs_affine_scan, rlcs_gae_and_returns, rlcs_gae_compact,
+    rlcs_affine_scan, rlcs_gae_and_returns, rlcs_gae_compact, rlcs_diag_stream_copy,
     workspace_for)

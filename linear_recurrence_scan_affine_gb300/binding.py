@@ -49,6 +49,7 @@ def _load():
         "rlcs_gae_and_returns": ([P] * 8 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
         "rlcs_affine_scan": ([P] * 5 + [I64, I64, ctypes.c_int, P, SZ, P], ctypes.c_int),
         "rlcs_gae_compact": ([P] * 7 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_diag_stream_copy": ([P, ctypes.c_int, P, I64, I64, ctypes.c_int, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -62,7 +63,8 @@ EXPORTED = ("rlcs_workspace_bytes", "rlcs_workspace_init", "rlcs_check_status",
             "rlcs_status_string", "rlcs_set_shape_override", "rlcs_gae",
             "rlcs_lambda_returns", "rlcs_discounted_returns", "rlcs_vtrace",
             "rlcs_retrace", "rlcs_eligibility_traces", "rlcs_episodic_prefix_sum",
-            "rlcs_gae_and_returns", "rlcs_affine_scan", "rlcs_gae_compact")
+            "rlcs_gae_and_returns", "rlcs_affine_scan", "rlcs_gae_compact",
+            "rlcs_diag_stream_copy")
 
 
 def lib():
@@ -316,6 +318,16 @@ def rlcs_gae_compact(rewards, values, terminateds, gamma=0.99, lambda_=0.95,
                                  N, T, gamma, lambda_, _ptr(ws), wsb, _stream(stream)),
            "rlcs_gae_compact")
     return o.reshape(rewards.shape)
+
+
+def rlcs_diag_stream_copy(inputs, out, empty=False, stream=None):
+    """Diagnostic: the warp-row launch shape moving the same bytes as an
+    estimator without the scan (sum of the inputs into `out`)."""
+    ptrs = (ctypes.c_void_p * len(inputs))(*[t.data_ptr() for t in inputs])
+    N, T = out.shape
+    _check(_lib.rlcs_diag_stream_copy(ctypes.cast(ptrs, ctypes.c_void_p), len(inputs), _ptr(out),
+                                      N, T, 1 if empty else 0, _stream(stream)),
+           "rlcs_diag_stream_copy")
 
 
 def rlcs_check_status(workspace=None, stream=None):

@@ -134,3 +134,16 @@ def test_gae_compact_shapes(rl, shape, chunk, T):
         _compact(rl, 3, T, 9200 + T, True, offset=1)   # unaligned rows: scalar loads
     finally:
         rl.rlcs_set_shape_override(rl.RLCS_SHAPE_AUTO, 0)
+
+
+def test_diag_stream_copy_sums_inputs(rl):
+    dev = torch.device("cuda:0")
+    ins = [torch.randn(64, 256, device=dev) for _ in range(3)]
+    out = torch.empty(64, 256, device=dev)
+    rl.rlcs_diag_stream_copy(ins, out)
+    torch.cuda.synchronize()
+    assert torch.allclose(out, ins[0] + ins[1] + ins[2], rtol=0, atol=1e-6)
+    out.fill_(7.0)
+    rl.rlcs_diag_stream_copy(ins, out, empty=True)   # only waits: leaves out alone
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
