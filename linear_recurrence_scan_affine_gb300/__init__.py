@@ -13,4 +13,7 @@ from .binding import (  # noqa: F401
     rlcs_eligibility_traces, rlcs_episodic_prefix_sum, rlcs_gae, rlcs_lambda_returns,
     rlcs_retrace, rlcs_set_shape_override, rlcs_vtrace, rlcs_workspace_bytes,
     rlcs_affine_scan, rlcs_gae_and_returns, rlcs_gae_compact, rlcs_diag_stream_copy,
+    rlcs_gae_tm, rlcs_lambda_returns_tm, rlcs_discounted_returns_tm, rlcs_vtrace_tm,
+    rlcs_retrace_tm, rlcs_eligibility_traces_tm, rlcs_episodic_prefix_sum_tm,
+    rlcs_gae_and_returns_tm, rlcs_affine_scan_tm,
     workspace_for)

@@ -50,6 +50,15 @@ def _load():
         "rlcs_affine_scan": ([P] * 5 + [I64, I64, ctypes.c_int, P, SZ, P], ctypes.c_int),
         "rlcs_gae_compact": ([P] * 7 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
         "rlcs_diag_stream_copy": ([P, ctypes.c_int, P, I64, I64, ctypes.c_int, P], ctypes.c_int),
+        "rlcs_gae_tm": ([P] * 7 + [I64, I64, F, F, P], ctypes.c_int),
+        "rlcs_lambda_returns_tm": ([P] * 7 + [I64, I64, F, F, P], ctypes.c_int),
+        "rlcs_discounted_returns_tm": ([P] * 6 + [I64, I64, F, P], ctypes.c_int),
+        "rlcs_vtrace_tm": ([P] * 9 + [I64, I64, F, F, F, F, P], ctypes.c_int),
+        "rlcs_retrace_tm": ([P] * 9 + [I64, I64, F, F, F, P], ctypes.c_int),
+        "rlcs_eligibility_traces_tm": ([P] * 3 + [I64, I64, F, F, P], ctypes.c_int),
+        "rlcs_episodic_prefix_sum_tm": ([P] * 3 + [I64, I64, P], ctypes.c_int),
+        "rlcs_gae_and_returns_tm": ([P] * 8 + [I64, I64, F, F, P], ctypes.c_int),
+        "rlcs_affine_scan_tm": ([P] * 5 + [I64, I64, ctypes.c_int, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -64,7 +73,10 @@ EXPORTED = ("rlcs_workspace_bytes", "rlcs_workspace_init", "rlcs_check_status",
             "rlcs_lambda_returns", "rlcs_discounted_returns", "rlcs_vtrace",
             "rlcs_retrace", "rlcs_eligibility_traces", "rlcs_episodic_prefix_sum",
             "rlcs_gae_and_returns", "rlcs_affine_scan", "rlcs_gae_compact",
-            "rlcs_diag_stream_copy")
+            "rlcs_diag_stream_copy", "rlcs_gae_tm", "rlcs_lambda_returns_tm",
+            "rlcs_discounted_returns_tm", "rlcs_vtrace_tm", "rlcs_retrace_tm",
+            "rlcs_eligibility_traces_tm", "rlcs_episodic_prefix_sum_tm",
+            "rlcs_gae_and_returns_tm", "rlcs_affine_scan_tm")
 
 
 def lib():
@@ -328,6 +340,132 @@ def rlcs_diag_stream_copy(inputs, out, empty=False, stream=None):
     _check(_lib.rlcs_diag_stream_copy(ctypes.cast(ptrs, ctypes.c_void_p), len(inputs), _ptr(out),
                                       N, T, 1 if empty else 0, _stream(stream)),
            "rlcs_diag_stream_copy")
+
+
+# ---------------------------------------------------------------------------
+# Time-major [T, N] variants: same arguments as above with every per-step
+# tensor shaped [T, N]; bootstrap_value / x_init stay [N]. No workspace.
+# ---------------------------------------------------------------------------
+def _tm(*tensors, names, dtypes=None):
+    T, N = tensors[0].shape
+    out = []
+    for i, (t, name) in enumerate(zip(tensors, names)):
+        if t is None:
+            out.append(None)
+            continue
+        dt = dtypes[i] if dtypes else torch.float32
+        x = _rows(t, name, dtype=dt)
+        if x.shape != (T, N):
+            raise ValueError("%s must have shape (T=%d, N=%d)" % (name, T, N))
+        out.append(x)
+    return T, N, out
+
+
+def rlcs_gae_tm(rewards, values, terminateds, gamma=0.99, lambda_=0.95, bootstrap_value=None,
+                truncateds=None, next_values=None, out=None, stream=None):
+    T, N, (r, v, d, tr, nv) = _tm(rewards, values, terminateds, truncateds, next_values,
+                                  names=("rewards", "values", "terminateds", "truncateds",
+                                         "next_values"))
+    b = _boot(bootstrap_value, N)
+    o = torch.empty_like(r) if out is None else out
+    _check(_lib.rlcs_gae_tm(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b), _ptr(o), N, T,
+                            gamma, lambda_, _stream(stream)), "rlcs_gae_tm")
+    return o
+
+
+def rlcs_lambda_returns_tm(rewards, values, terminateds, gamma=0.99, lambda_=0.95,
+                           bootstrap_value=None, truncateds=None, next_values=None, out=None,
+                           stream=None):
+    T, N, (r, v, d, tr, nv) = _tm(rewards, values, terminateds, truncateds, next_values,
+                                  names=("rewards", "values", "terminateds", "truncateds",
+                                         "next_values"))
+    b = _boot(bootstrap_value, N)
+    o = torch.empty_like(r) if out is None else out
+    _check(_lib.rlcs_lambda_returns_tm(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
+                                       _ptr(o), N, T, gamma, lambda_, _stream(stream)),
+           "rlcs_lambda_returns_tm")
+    return o
+
+
+def rlcs_discounted_returns_tm(rewards, terminateds, gamma=0.99, bootstrap_value=None,
+                               truncateds=None, next_values=None, out=None, stream=None):
+    T, N, (r, d, tr, nv) = _tm(rewards, terminateds, truncateds, next_values,
+                               names=("rewards", "terminateds", "truncateds", "next_values"))
+    b = _boot(bootstrap_value, N)
+    o = torch.empty_like(r) if out is None else out
+    _check(_lib.rlcs_discounted_returns_tm(_ptr(r), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b), _ptr(o),
+                                           N, T, gamma, _stream(stream)),
+           "rlcs_discounted_returns_tm")
+    return o
+
+
+def rlcs_vtrace_tm(rewards, values, log_rhos, terminateds, gamma=0.99, lambda_=1.0, rho_bar=1.0,
+                   c_bar=1.0, bootstrap_value=None, truncateds=None, next_values=None,
+                   with_pg=True, stream=None):
+    T, N, (r, v, lr, d, tr, nv) = _tm(rewards, values, log_rhos, terminateds, truncateds,
+                                      next_values,
+                                      names=("rewards", "values", "log_rhos", "terminateds",
+                                             "truncateds", "next_values"))
+    b = _boot(bootstrap_value, N)
+    vs = torch.empty_like(r)
+    pg = torch.empty_like(r) if with_pg else None
+    _check(_lib.rlcs_vtrace_tm(_ptr(r), _ptr(v), _ptr(lr), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
+                               _ptr(vs), _ptr(pg), N, T, gamma, lambda_, rho_bar, c_bar,
+                               _stream(stream)), "rlcs_vtrace_tm")
+    return vs, pg
+
+
+def rlcs_retrace_tm(rewards, values, q_values, log_rhos, terminateds, gamma=0.99, lambda_=1.0,
+                    c_bar=1.0, bootstrap_value=None, truncateds=None, next_values=None,
+                    stream=None):
+    T, N, (r, v, q, lr, d, tr, nv) = _tm(rewards, values, q_values, log_rhos, terminateds,
+                                         truncateds, next_values,
+                                         names=("rewards", "values", "q_values", "log_rhos",
+                                                "terminateds", "truncateds", "next_values"))
+    b = _boot(bootstrap_value, N)
+    o = torch.empty_like(r)
+    _check(_lib.rlcs_retrace_tm(_ptr(r), _ptr(v), _ptr(q), _ptr(lr), _ptr(d), _ptr(tr), _ptr(nv),
+                                _ptr(b), _ptr(o), N, T, gamma, lambda_, c_bar, _stream(stream)),
+           "rlcs_retrace_tm")
+    return o
+
+
+def rlcs_eligibility_traces_tm(x, dones, gamma=0.99, lambda_=0.95, stream=None):
+    T, N, (xx, d) = _tm(x, dones, names=("x", "dones"))
+    o = torch.empty_like(xx)
+    _check(_lib.rlcs_eligibility_traces_tm(_ptr(xx), _ptr(d), _ptr(o), N, T, gamma, lambda_,
+                                           _stream(stream)), "rlcs_eligibility_traces_tm")
+    return o
+
+
+def rlcs_episodic_prefix_sum_tm(x, dones, stream=None):
+    T, N, (xx, d) = _tm(x, dones, names=("x", "dones"), dtypes=(torch.int32, torch.float32))
+    o = torch.empty_like(xx)
+    _check(_lib.rlcs_episodic_prefix_sum_tm(_ptr(xx), _ptr(d), _ptr(o), N, T, _stream(stream)),
+           "rlcs_episodic_prefix_sum_tm")
+    return o
+
+
+def rlcs_gae_and_returns_tm(rewards, values, terminateds, gamma=0.99, lambda_=0.95,
+                            bootstrap_value=None, truncateds=None, next_values=None, stream=None):
+    T, N, (r, v, d, tr, nv) = _tm(rewards, values, terminateds, truncateds, next_values,
+                                  names=("rewards", "values", "terminateds", "truncateds",
+                                         "next_values"))
+    b = _boot(bootstrap_value, N)
+    adv, ret = torch.empty_like(r), torch.empty_like(r)
+    _check(_lib.rlcs_gae_and_returns_tm(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
+                                        _ptr(adv), _ptr(ret), N, T, gamma, lambda_,
+                                        _stream(stream)), "rlcs_gae_and_returns_tm")
+    return adv, ret
+
+
+def rlcs_affine_scan_tm(a, b, reset=None, x_init=None, reverse=False, stream=None):
+    T, N, (aa, bb, rr) = _tm(a, b, reset, names=("a", "b", "reset"))
+    x0 = None if x_init is None else _boot(x_init, N)
+    o = torch.empty_like(aa)
+    _check(_lib.rlcs_affine_scan_tm(_ptr(aa), _ptr(bb), _ptr(rr), _ptr(x0), _ptr(o), N, T,
+                                    1 if reverse else 0, _stream(stream)), "rlcs_affine_scan_tm")
+    return o
 
 
 def rlcs_check_status(workspace=None, stream=None):

@@ -274,6 +274,19 @@ struct SmemSource {
   }
 };
 
+// One environment's column of a time-major tile in shared memory (one strip).
+struct ColumnSource {
+  const float *col[kNumSlots];  // per slot: this warp's column, 128 steps
+  float halo_next[kNumSlots];   // first step after the tile (scan order)
+  float halo_prev_d;            // done mask before the tile
+  int lane;
+  __device__ __forceinline__ float4 get(int k, int) const {
+    return *reinterpret_cast<const float4 *>(col[k] + 4 * lane);
+  }
+  __device__ __forceinline__ float following(int k, int) const { return halo_next[k]; }
+  __device__ __forceinline__ float preceding_d(int) const { return halo_prev_d; }
+};
+
 // ---------------------------------------------------------------------------
 // Strip engine for one warp's span of S strips.
 // ---------------------------------------------------------------------------
@@ -910,6 +923,146 @@ __global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
     }
   }
   if (Q > 1 && tid == 0) finish_launch(ts.ws, ts.total_tiles, s_epoch);
+}
+
+// ---------------------------------------------------------------------------
+// Time-major tier: inputs and outputs [T, N] (element (t, n) at t*N + n).
+// A block owns kTmEnvs environments (kTmEnvsPerWarp per warp) and walks T in tiles of
+// kStrip steps, in scan order, carrying each environment's value from tile
+// to tile: no look-back. Per tile, rows are loaded with coalesced accesses
+// (kTmEnvs consecutive environments per row) into an env-major shared tile
+// padded to kTmPitch floats, so the row writes and each warp's float4 reads
+// of its environment's column are both bank-conflict-free; the warp then runs
+// the strip engine on its column (lane l owns steps 4l..4l+3, exactly as in
+// the warp-row tier), writes its outputs into an output tile of the same
+// layout, and the block stores those rows coalesced.
+// ---------------------------------------------------------------------------
+#ifndef RLCS_TM_ENVS_PER_WARP
+#define RLCS_TM_ENVS_PER_WARP 1
+#endif
+constexpr int kTmWarps = 8;
+constexpr int kTmEnvsPerWarp = RLCS_TM_ENVS_PER_WARP;  // columns each warp scans, in turn
+constexpr int kTmEnvs = kTmWarps * kTmEnvsPerWarp;     // environments per block
+constexpr int kTmThreads = kTmWarps * 32;
+constexpr int kTmPitch = kStrip + 4;                   // floats per environment column
+constexpr int kTmRowsPerLoad = 32 / kTmEnvs;           // rows one warp instruction covers
+constexpr int kTmRowsPerPass = kTmWarps * kTmRowsPerLoad;
+constexpr int kTmPasses = kStrip / kTmRowsPerPass;
+static_assert(kTmEnvs <= 32 && 32 % kTmEnvs == 0, "a warp covers whole row segments");
+
+template <class E, bool TRUNC>
+constexpr int tm_tiles() {  // shared tiles: used input slots + outputs
+  return __builtin_popcount(Strips<E, TRUNC, 1>::kUse) + E::kOuts;
+}
+
+template <class E, bool TRUNC>
+__global__ void __launch_bounds__(kTmThreads) time_major_kernel(Params p) {
+  using St = Strips<E, TRUNC, 1>;
+  using V = typename St::V;
+  constexpr uint32_t kUse = St::kUse;
+  constexpr int kNumUsed = __builtin_popcount(kUse);
+  extern __shared__ __align__(16) float tm_smem[];  // [kNumUsed + kOuts][kTmEnvs][kTmPitch]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t N = p.N, T = p.T;
+  const int64_t env0 = (int64_t)blockIdx.x * kTmEnvs;
+  // loader mapping: one warp instruction = kTmRowsPerLoad rows x kTmEnvs environments
+  const int ld_env = lane % kTmEnvs, ld_row = lane / kTmEnvs;
+  const bool ld_ok = env0 + ld_env < N;
+  const int64_t tiles = (T + kStrip - 1) / kStrip;
+
+  auto tile_of = [&](int idx) { return tm_smem + (size_t)idx * kTmEnvs * kTmPitch; };
+
+  pdl_wait();
+  V carry[kTmEnvsPerWarp];
+  float boot[kTmEnvsPerWarp];
+  float halo_next[kTmEnvsPerWarp][kNumSlots];
+  float halo_prev_d[kTmEnvsPerWarp];
+#pragma unroll
+  for (int q = 0; q < kTmEnvsPerWarp; ++q) {
+    const int64_t env = env0 + warp * kTmEnvsPerWarp + q;
+    boot[q] = (E::kUsesRowValue && p.boot && env < N) ? __ldg(p.boot + env) : 0.f;
+    carry[q] = V(0);
+    halo_prev_d[q] = 0.f;
+#pragma unroll
+    for (int k = 0; k < kNumSlots; ++k) halo_next[q][k] = 0.f;
+  }
+
+  for (int64_t i = 0; i < tiles; ++i) {
+    const int64_t tt = E::kBackward ? (tiles - 1 - i) : i;
+    const int64_t t0 = tt * kStrip;
+    __syncthreads();  // the previous tile's shared reads are done
+    // coalesced row loads into the env-major tiles
+    {
+      int idx = 0;
+#pragma unroll
+      for (int k = 0; k < kNumSlots; ++k) {
+        if (!(kUse & bit(k))) continue;
+        float *tile = tile_of(idx);
+        float v[kTmPasses];
+#pragma unroll
+        for (int q = 0; q < kTmPasses; ++q) {
+          const int r = q * kTmRowsPerPass + warp * kTmRowsPerLoad + ld_row;
+          const int64_t t = t0 + r;
+          v[q] = (t < T && ld_ok) ? load_slot1<E>(p, k, t * N + env0 + ld_env) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < kTmPasses; ++q) {
+          const int r = q * kTmRowsPerPass + warp * kTmRowsPerLoad + ld_row;
+          tile[ld_env * kTmPitch + r] = v[q];
+        }
+        ++idx;
+      }
+    }
+    if (i == 0) pdl_launch_dependents();
+    __syncthreads();
+
+#pragma unroll 1
+    for (int q = 0; q < kTmEnvsPerWarp; ++q) {
+      const int e = warp * kTmEnvsPerWarp + q;  // this warp's column
+      ColumnSource src;
+      {
+        int idx = 0;
+#pragma unroll
+        for (int k = 0; k < kNumSlots; ++k) {
+          src.col[k] = tile_of(idx) + e * kTmPitch;  // unused slots alias a used one
+          if (kUse & bit(k)) ++idx;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < kNumSlots; ++k) src.halo_next[k] = halo_next[q][k];
+      src.halo_prev_d = halo_prev_d[q];
+      src.lane = lane;
+      St st;
+      st.template build<true>(p, src, boot[q], t0, T, lane);
+      const auto agg = st.scan(lane);
+      float4 o0[1], o1[1];
+      st.finish(carry[q], o0, o1);
+      carry[q] = apply(agg, carry[q]);
+      // values just outside the next tile in scan order
+#pragma unroll
+      for (int k = 0; k < kNumSlots; ++k)
+        if (E::kBackward && (E::kNext & bit(k))) halo_next[q][k] = src.col[k][0];
+      if (E::kPrevD) halo_prev_d[q] = src.col[kD][kStrip - 1];
+      *reinterpret_cast<float4 *>(tile_of(kNumUsed) + e * kTmPitch + 4 * lane) = o0[0];
+      if constexpr (E::kOuts > 1)
+        *reinterpret_cast<float4 *>(tile_of(kNumUsed + 1) + e * kTmPitch + 4 * lane) = o1[0];
+    }
+    __syncthreads();
+
+    // coalesced row stores
+#pragma unroll
+    for (int o = 0; o < E::kOuts; ++o) {
+      float *dst = (o == 0) ? static_cast<float *>(p.out0) : p.out1;
+      if (dst == nullptr) continue;
+      const float *tile = tile_of(kNumUsed + o);
+#pragma unroll
+      for (int q = 0; q < kTmPasses; ++q) {
+        const int r = q * kTmRowsPerPass + warp * kTmRowsPerLoad + ld_row;
+        const int64_t t = t0 + r;
+        if (t < T && ld_ok) dst[t * N + env0 + ld_env] = tile[ld_env * kTmPitch + r];
+      }
+    }
+  }
 }
 
 }  // namespace rlcs

@@ -8,6 +8,9 @@
 
 namespace rlcs {
 
+// Internal launch shape for time-major [T, N] inputs (not an rlcs_shape).
+constexpr int kShapeTimeMajor = 100;
+
 struct Plan {
   int shape;       // RLCS_SHAPE_WARP_ROW, RLCS_SHAPE_BLOCK_CHUNK or RLCS_SHAPE_BLOCK_TILE
   int S;           // strips per warp: 1, 2 or 4
@@ -35,6 +38,20 @@ inline cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaS
 
 template <class E, bool TRUNC, int S>
 inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws, cudaStream_t s) {
+  if (plan.shape == kShapeTimeMajor) {
+    constexpr size_t smem = (size_t)tm_tiles<E, TRUNC>() * kTmEnvs * kTmPitch * 4;
+    if constexpr (smem > 48 * 1024) {
+      static std::once_flag once;
+      static cudaError_t attr_err = cudaSuccess;
+      std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(time_major_kernel<E, TRUNC>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      });
+      if (attr_err != cudaSuccess) return attr_err;
+    }
+    const dim3 grid((unsigned)((p.N + kTmEnvs - 1) / kTmEnvs));
+    return launch_ex(time_major_kernel<E, TRUNC>, grid, dim3(kTmThreads), smem, s, plan.pdl, p);
+  }
   if (plan.shape == RLCS_SHAPE_WARP_ROW) {
     const dim3 grid((unsigned)((p.N + kRowWarps - 1) / kRowWarps));
     return launch_ex(warp_row_kernel<E, TRUNC, S>, grid, dim3(kRowWarps * 32), 0, s, plan.pdl, p);

@@ -18,6 +18,15 @@ std::atomic<int> g_override_shape{RLCS_SHAPE_AUTO};
 std::atomic<int64_t> g_override_chunk{0};
 std::atomic<int> g_sm_count[kMaxDevices];
 
+// Set while a time-major (_tm) entry point runs its row-major counterpart's
+// validation and launch; run() reads it. Thread-local, so concurrent callers
+// on other threads are unaffected.
+thread_local bool t_time_major = false;
+struct TimeMajorScope {
+  TimeMajorScope() { t_time_major = true; }
+  ~TimeMajorScope() { t_time_major = false; }
+};
+
 int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
@@ -44,10 +53,16 @@ int64_t pick_chunk(int64_t N, int64_t T) {
 }
 
 // Choose the launch shape for an [N, T] call.
-rlcs_status plan_call(int64_t N, int64_t T, bool trunc, Plan &plan) {
+rlcs_status plan_call(int64_t N, int64_t T, bool trunc, Plan &plan, bool time_major = false) {
   plan = Plan{};
   plan.trunc = trunc;
   plan.pdl = true;
+  if (time_major) {  // one shape: blocks of environments walk T in tiles
+    plan.shape = kShapeTimeMajor;
+    plan.S = 1;
+    plan.Q = 1;
+    return RLCS_OK;
+  }
   const int ov = g_override_shape.load(std::memory_order_relaxed);
   if (ov == RLCS_SHAPE_WARP_ROW || (ov == RLCS_SHAPE_AUTO && T <= kRowMaxT)) {
     if (T > kRowMaxT) return RLCS_ERR_INVALID_ARG;
@@ -84,10 +99,11 @@ bool overlaps(const Buf &a, const Buf &b) {
 // `opt`: the estimator's optional inputs are present (the truncation pair,
 // or the affine scan's reset mask already placed in p.in).
 // `esize`: bytes per element of each input slot (NULL: all float32).
+// `time_major`: arrays are [T, N] (element (t, n) at t*N + n).
 template <class Launch>
 rlcs_status run(Params &p, const float *trunc, const float *next_values, void *const *outs,
                 int n_outs, void *ws, size_t ws_bytes, cudaStream_t stream, Launch launch,
-                bool opt, const int *esize = nullptr) {
+                bool opt, const int *esize = nullptr, bool time_major = false) {
   const int64_t N = p.N, T = p.T;
   if (N <= 0 || T <= 0) return RLCS_ERR_INVALID_ARG;
   if (N > (int64_t)(INT64_MAX / 4) / T) return RLCS_ERR_INVALID_ARG;
@@ -113,7 +129,7 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
   p.vec = vec ? 1 : 0;
 
   Plan plan;
-  const rlcs_status st = plan_call(N, T, opt, plan);
+  const rlcs_status st = plan_call(N, T, opt, plan, time_major || t_time_major);
   if (st != RLCS_OK) return st;
   WsHeader *wsh = nullptr;
   if (plan.shape != RLCS_SHAPE_WARP_ROW) {
@@ -398,6 +414,94 @@ extern "C" rlcs_status rlcs_affine_scan(const float *a, const float *b, const fl
              reinterpret_cast<cudaStream_t>(stream),
              reverse ? launch_affine_backward : launch_affine_forward, reset != nullptr);
 }
+
+// ---------------------------------------------------------------------------
+// Time-major [T, N] entry points: the row-major validation and functors,
+// launched in the time-major shape (which needs no workspace).
+// ---------------------------------------------------------------------------
+extern "C" {
+
+rlcs_status rlcs_gae_tm(const float *rewards, const float *values, const float *terminateds,
+                        const float *truncateds, const float *next_values,
+                        const float *bootstrap_value, float *advantages, int64_t N, int64_t T,
+                        float gamma, float lambda, rlcs_stream_t stream) {
+  TimeMajorScope tm;
+  return rlcs_gae(rewards, values, terminateds, truncateds, next_values, bootstrap_value,
+                  advantages, N, T, gamma, lambda, nullptr, 0, stream);
+}
+
+rlcs_status rlcs_lambda_returns_tm(const float *rewards, const float *values,
+                                   const float *terminateds, const float *truncateds,
+                                   const float *next_values, const float *bootstrap_value,
+                                   float *returns, int64_t N, int64_t T, float gamma,
+                                   float lambda, rlcs_stream_t stream) {
+  TimeMajorScope tm;
+  return rlcs_lambda_returns(rewards, values, terminateds, truncateds, next_values,
+                             bootstrap_value, returns, N, T, gamma, lambda, nullptr, 0, stream);
+}
+
+rlcs_status rlcs_discounted_returns_tm(const float *rewards, const float *terminateds,
+                                       const float *truncateds, const float *next_values,
+                                       const float *bootstrap_value, float *returns, int64_t N,
+                                       int64_t T, float gamma, rlcs_stream_t stream) {
+  TimeMajorScope tm;
+  return rlcs_discounted_returns(rewards, terminateds, truncateds, next_values, bootstrap_value,
+                                 returns, N, T, gamma, nullptr, 0, stream);
+}
+
+rlcs_status rlcs_vtrace_tm(const float *rewards, const float *values, const float *log_rhos,
+                           const float *terminateds, const float *truncateds,
+                           const float *next_values, const float *bootstrap_value, float *vs,
+                           float *pg_advantages, int64_t N, int64_t T, float gamma,
+                           float lambda, float rho_bar, float c_bar, rlcs_stream_t stream) {
+  TimeMajorScope tm;
+  return rlcs_vtrace(rewards, values, log_rhos, terminateds, truncateds, next_values,
+                     bootstrap_value, vs, pg_advantages, N, T, gamma, lambda, rho_bar, c_bar,
+                     nullptr, 0, stream);
+}
+
+rlcs_status rlcs_retrace_tm(const float *rewards, const float *values, const float *q_values,
+                            const float *log_rhos, const float *terminateds,
+                            const float *truncateds, const float *next_values,
+                            const float *bootstrap_value, float *q_ret, int64_t N, int64_t T,
+                            float gamma, float lambda, float c_bar, rlcs_stream_t stream) {
+  TimeMajorScope tm;
+  return rlcs_retrace(rewards, values, q_values, log_rhos, terminateds, truncateds, next_values,
+                      bootstrap_value, q_ret, N, T, gamma, lambda, c_bar, nullptr, 0, stream);
+}
+
+rlcs_status rlcs_eligibility_traces_tm(const float *x, const float *dones, float *traces,
+                                       int64_t N, int64_t T, float gamma, float lambda,
+                                       rlcs_stream_t stream) {
+  TimeMajorScope tm;
+  return rlcs_eligibility_traces(x, dones, traces, N, T, gamma, lambda, nullptr, 0, stream);
+}
+
+rlcs_status rlcs_episodic_prefix_sum_tm(const int32_t *x, const float *dones, int32_t *out,
+                                        int64_t N, int64_t T, rlcs_stream_t stream) {
+  TimeMajorScope tm;
+  return rlcs_episodic_prefix_sum(x, dones, out, N, T, nullptr, 0, stream);
+}
+
+rlcs_status rlcs_gae_and_returns_tm(const float *rewards, const float *values,
+                                    const float *terminateds, const float *truncateds,
+                                    const float *next_values, const float *bootstrap_value,
+                                    float *advantages, float *returns, int64_t N, int64_t T,
+                                    float gamma, float lambda, rlcs_stream_t stream) {
+  TimeMajorScope tm;
+  return rlcs_gae_and_returns(rewards, values, terminateds, truncateds, next_values,
+                              bootstrap_value, advantages, returns, N, T, gamma, lambda, nullptr,
+                              0, stream);
+}
+
+rlcs_status rlcs_affine_scan_tm(const float *a, const float *b, const float *reset,
+                                const float *x_init, float *x, int64_t N, int64_t T, int reverse,
+                                rlcs_stream_t stream) {
+  TimeMajorScope tm;
+  return rlcs_affine_scan(a, b, reset, x_init, x, N, T, reverse, nullptr, 0, stream);
+}
+
+}  // extern "C"
 
 // ---------------------------------------------------------------------------
 // GAE for callers that cannot allocate device memory.

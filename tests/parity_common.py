@@ -81,7 +81,8 @@ def run_oracle(est, src, prm, trunc):
 
 def compare(est, got, want, tol, tag=""):
     for key, ref in want.items():
-        g = got[key].cpu().numpy()
+        g = got[key]
+        g = g.cpu().numpy() if hasattr(g, "cpu") else np.asarray(g)
         if est == "episodic_prefix_sum":
             bad = np.argwhere(g != ref)
             assert bad.size == 0, "%s%s: %d int32 mismatches, first at %s: %d vs %d" % (

@@ -1,0 +1,93 @@
+"""GPU parity for the time-major [T, N] entry points (the _tm functions).
+
+Inputs are drawn [N, T] as everywhere else, transposed to [T, N] for the
+GPU, and the outputs transposed back and compared element by element with
+the float64 oracle at the usual bar (1e-4 relative; the prefix sum
+bit-exact). Sizes cover ragged environment blocks (N not a multiple of 8),
+ragged and multi-tile T (tiles of 128 steps), truncations and the degenerate
+T = 1.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic_rollouts import affine_inputs, rollout
+from tests.parity_common import TOL, compare
+
+pytestmark = pytest.mark.gpu
+
+SIZES = [(4096, 128), (1000, 300), (7, 1), (33, 129), (256, 1030), (9, 4097)]
+PRM = dict(gamma=0.99, lambda_=0.95, rho_bar=1.0, c_bar=1.0)
+
+
+@pytest.fixture(scope="module")
+def rl():
+    assert torch.cuda.is_available(), "the -m gpu tests need a CUDA device"
+    import linear_recurrence_scan_affine_gb300 as rl
+    return rl
+
+
+def tm(a, dev=torch.device("cuda:0")):
+    return torch.from_numpy(np.ascontiguousarray(np.asarray(a).T)).to(dev)
+
+
+def back(t):
+    return t.cpu().numpy().T
+
+
+@pytest.mark.parametrize("N,T", SIZES)
+@pytest.mark.parametrize("trunc", [False, True])
+def test_backward_estimators_time_major(rl, N, T, trunc):
+    src = rollout(N, T, 11000 + N + T, p_term=0.01, p_trunc=0.005 if trunc else 0.0)
+    g = {k: (tm(v) if v.ndim == 2 else torch.from_numpy(v).cuda()) for k, v in src.items()}
+    kw = dict(truncateds=g["truncateds"], next_values=g["next_values"]) if trunc else {}
+    kwn = dict(truncateds=src["truncateds"], next_values=src["next_values"]) if trunc else {}
+    B, Bn = g["bootstrap_value"], src["bootstrap_value"]
+    r, v, d = g["rewards"], g["values"], g["terminateds"]
+    rn, vn, dn = src["rewards"], src["values"], src["terminateds"]
+    gm, lm = PRM["gamma"], PRM["lambda_"]
+    compare("gae", {"out": back(rl.rlcs_gae_tm(r, v, d, gm, lm, B, **kw))},
+            {"out": oracle.gae(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
+    compare("lambda_returns", {"out": back(rl.rlcs_lambda_returns_tm(r, v, d, gm, lm, B, **kw))},
+            {"out": oracle.lambda_returns(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
+    compare("discounted_returns",
+            {"out": back(rl.rlcs_discounted_returns_tm(r, d, gm, B, **kw))},
+            {"out": oracle.discounted_returns(rn, dn, gm, Bn, **kwn)}, TOL)
+    vs, pg = rl.rlcs_vtrace_tm(r, v, g["log_rhos"], d, gm, lm, 1.0, 1.0, B, **kw)
+    ovs, opg = oracle.vtrace(rn, vn, src["log_rhos"], dn, gm, lm, 1.0, 1.0, Bn, **kwn)
+    compare("vtrace", {"vs": back(vs), "pg": back(pg)}, {"vs": ovs, "pg": opg}, TOL)
+    compare("retrace",
+            {"out": back(rl.rlcs_retrace_tm(r, v, g["q_values"], g["log_rhos"], d, gm, lm, 1.0,
+                                            B, **kw))},
+            {"out": oracle.retrace(rn, vn, src["q_values"], src["log_rhos"], dn, gm, lm, 1.0,
+                                   Bn, **kwn)}, TOL)
+    adv, ret = rl.rlcs_gae_and_returns_tm(r, v, d, gm, lm, B, **kw)
+    compare("gae", {"out": back(adv)}, {"out": oracle.gae(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
+    compare("lambda_returns", {"out": back(ret)},
+            {"out": oracle.lambda_returns(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
+
+
+def _as_np(t):
+    return t if isinstance(t, np.ndarray) else t.cpu().numpy()
+
+
+@pytest.mark.parametrize("N,T", SIZES)
+def test_forward_estimators_time_major(rl, N, T):
+    src = rollout(N, T, 12000 + N + T, p_term=0.02)
+    d = tm(src["terminateds"])
+    got = back(rl.rlcs_eligibility_traces_tm(tm(src["x"]), d, 0.9, 0.8))
+    compare("eligibility_traces", {"out": got},
+            {"out": oracle.eligibility_traces(src["x"], src["terminateds"], 0.9, 0.8)}, TOL)
+    got = back(rl.rlcs_episodic_prefix_sum_tm(tm(src["x_int"]), d))
+    assert np.array_equal(got, oracle.episodic_prefix_sum(src["x_int"], src["terminateds"]))
+
+
+@pytest.mark.parametrize("N,T", SIZES)
+@pytest.mark.parametrize("reverse", [False, True])
+def test_affine_scan_time_major(rl, N, T, reverse):
+    src = affine_inputs(N, T, 13000 + N + T)
+    got = back(rl.rlcs_affine_scan_tm(tm(src["a"]), tm(src["b"]), tm(src["reset"]),
+                                      torch.from_numpy(src["x_init"]).cuda(), reverse=reverse))
+    want = oracle.affine_scan(src["a"], src["b"], src["reset"], src["x_init"], reverse=reverse)
+    compare("affine_scan", {"out": got}, {"out": want}, TOL)
