@@ -240,50 +240,67 @@ rlcs_status rlcs_affine_scan(const float *a, const float *b, const float *reset,
                              int reverse, void *workspace, size_t workspace_bytes,
                              rlcs_stream_t stream);
 
-/* Time-major layout. Each function below is its row-major namesake for
- * arrays stored [T, N] (element (t, n) at offset t*N + n; bootstrap_value and
- * x_init stay [N]): the same estimator, arguments, results and errors, minus
- * the workspace, which this layout never needs. Many RL rollout buffers are
- * stored this way; no transpose is needed. A block owns 8 environments and
- * walks T in 128-step tiles in scan order, carrying each environment's value,
- * so the layout suits many environments (N in the thousands) better than a
- * few very long rows. */
+/* Time-major layout. The technical summary's Problem Statement fixes the
+ * estimators' operands as [num_envs, seq_len] tensors; many RL rollout
+ * buffers store the same data time-major instead. Each function below is its
+ * row-major namesake for arrays stored [T, N] (element (t, n) at offset
+ * t*N + n; bootstrap_value and x_init stay [N]): the same estimator,
+ * arguments, results and errors, without a transpose. Lane l of a warp owns
+ * environment 32*g + l, so every access moves whole 128-byte row segments; a
+ * block owns 32 environments and one chunk of steps, and chunks of the same
+ * environments are linked by a decoupled look-back.
+ *
+ * Workspace: rlcs_workspace_bytes_tm(N, T) bytes, prepared as for the
+ * row-major entries (zeroed once, one per stream, never shared by calls that
+ * may overlap). It is required only when T spans more than one chunk (the
+ * size function still answers nonzero for shorter rows); when it is missing
+ * or short the call returns RLCS_ERR_WORKSPACE and launches nothing. */
+size_t rlcs_workspace_bytes_tm(int64_t N, int64_t T);
+
 rlcs_status rlcs_gae_tm(const float *rewards, const float *values, const float *terminateds,
                         const float *truncateds, const float *next_values,
                         const float *bootstrap_value, float *advantages, int64_t N, int64_t T,
-                        float gamma, float lambda, rlcs_stream_t stream);
+                        float gamma, float lambda, void *workspace, size_t workspace_bytes,
+                        rlcs_stream_t stream);
 rlcs_status rlcs_lambda_returns_tm(const float *rewards, const float *values,
                                    const float *terminateds, const float *truncateds,
                                    const float *next_values, const float *bootstrap_value,
                                    float *returns, int64_t N, int64_t T, float gamma,
-                                   float lambda, rlcs_stream_t stream);
+                                   float lambda, void *workspace, size_t workspace_bytes,
+                                   rlcs_stream_t stream);
 rlcs_status rlcs_discounted_returns_tm(const float *rewards, const float *terminateds,
                                        const float *truncateds, const float *next_values,
                                        const float *bootstrap_value, float *returns, int64_t N,
-                                       int64_t T, float gamma, rlcs_stream_t stream);
+                                       int64_t T, float gamma, void *workspace,
+                                       size_t workspace_bytes, rlcs_stream_t stream);
 rlcs_status rlcs_vtrace_tm(const float *rewards, const float *values, const float *log_rhos,
                            const float *terminateds, const float *truncateds,
                            const float *next_values, const float *bootstrap_value, float *vs,
                            float *pg_advantages, int64_t N, int64_t T, float gamma,
-                           float lambda, float rho_bar, float c_bar, rlcs_stream_t stream);
+                           float lambda, float rho_bar, float c_bar, void *workspace,
+                           size_t workspace_bytes, rlcs_stream_t stream);
 rlcs_status rlcs_retrace_tm(const float *rewards, const float *values, const float *q_values,
                             const float *log_rhos, const float *terminateds,
                             const float *truncateds, const float *next_values,
                             const float *bootstrap_value, float *q_ret, int64_t N, int64_t T,
-                            float gamma, float lambda, float c_bar, rlcs_stream_t stream);
+                            float gamma, float lambda, float c_bar, void *workspace,
+                            size_t workspace_bytes, rlcs_stream_t stream);
 rlcs_status rlcs_eligibility_traces_tm(const float *x, const float *dones, float *traces,
                                        int64_t N, int64_t T, float gamma, float lambda,
+                                       void *workspace, size_t workspace_bytes,
                                        rlcs_stream_t stream);
 rlcs_status rlcs_episodic_prefix_sum_tm(const int32_t *x, const float *dones, int32_t *out,
-                                        int64_t N, int64_t T, rlcs_stream_t stream);
+                                        int64_t N, int64_t T, void *workspace,
+                                        size_t workspace_bytes, rlcs_stream_t stream);
 rlcs_status rlcs_gae_and_returns_tm(const float *rewards, const float *values,
                                     const float *terminateds, const float *truncateds,
                                     const float *next_values, const float *bootstrap_value,
                                     float *advantages, float *returns, int64_t N, int64_t T,
-                                    float gamma, float lambda, rlcs_stream_t stream);
+                                    float gamma, float lambda, void *workspace,
+                                    size_t workspace_bytes, rlcs_stream_t stream);
 rlcs_status rlcs_affine_scan_tm(const float *a, const float *b, const float *reset,
                                 const float *x_init, float *x, int64_t N, int64_t T, int reverse,
-                                rlcs_stream_t stream);
+                                void *workspace, size_t workspace_bytes, rlcs_stream_t stream);
 
 /* GAE for callers that cannot allocate device memory.
  * The paper has no counterpart: this is a library convenience. Some callers

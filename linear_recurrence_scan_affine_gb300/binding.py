@@ -35,6 +35,7 @@ def _load():
     P, I64, F, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
     sig = {
         "rlcs_workspace_bytes": ([I64, I64], SZ),
+        "rlcs_workspace_bytes_tm": ([I64, I64], SZ),
         "rlcs_workspace_init": ([P, SZ, P], ctypes.c_int),
         "rlcs_check_status": ([P, P], ctypes.c_int),
         "rlcs_status_string": ([ctypes.c_int], ctypes.c_char_p),
@@ -50,15 +51,15 @@ def _load():
         "rlcs_affine_scan": ([P] * 5 + [I64, I64, ctypes.c_int, P, SZ, P], ctypes.c_int),
         "rlcs_gae_compact": ([P] * 7 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
         "rlcs_diag_stream_copy": ([P, ctypes.c_int, P, I64, I64, ctypes.c_int, P], ctypes.c_int),
-        "rlcs_gae_tm": ([P] * 7 + [I64, I64, F, F, P], ctypes.c_int),
-        "rlcs_lambda_returns_tm": ([P] * 7 + [I64, I64, F, F, P], ctypes.c_int),
-        "rlcs_discounted_returns_tm": ([P] * 6 + [I64, I64, F, P], ctypes.c_int),
-        "rlcs_vtrace_tm": ([P] * 9 + [I64, I64, F, F, F, F, P], ctypes.c_int),
-        "rlcs_retrace_tm": ([P] * 9 + [I64, I64, F, F, F, P], ctypes.c_int),
-        "rlcs_eligibility_traces_tm": ([P] * 3 + [I64, I64, F, F, P], ctypes.c_int),
-        "rlcs_episodic_prefix_sum_tm": ([P] * 3 + [I64, I64, P], ctypes.c_int),
-        "rlcs_gae_and_returns_tm": ([P] * 8 + [I64, I64, F, F, P], ctypes.c_int),
-        "rlcs_affine_scan_tm": ([P] * 5 + [I64, I64, ctypes.c_int, P], ctypes.c_int),
+        "rlcs_gae_tm": ([P] * 7 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_lambda_returns_tm": ([P] * 7 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_discounted_returns_tm": ([P] * 6 + [I64, I64, F, P, SZ, P], ctypes.c_int),
+        "rlcs_vtrace_tm": ([P] * 9 + [I64, I64, F, F, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_retrace_tm": ([P] * 9 + [I64, I64, F, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_eligibility_traces_tm": ([P] * 3 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_episodic_prefix_sum_tm": ([P] * 3 + [I64, I64, P, SZ, P], ctypes.c_int),
+        "rlcs_gae_and_returns_tm": ([P] * 8 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_affine_scan_tm": ([P] * 5 + [I64, I64, ctypes.c_int, P, SZ, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -73,7 +74,8 @@ EXPORTED = ("rlcs_workspace_bytes", "rlcs_workspace_init", "rlcs_check_status",
             "rlcs_lambda_returns", "rlcs_discounted_returns", "rlcs_vtrace",
             "rlcs_retrace", "rlcs_eligibility_traces", "rlcs_episodic_prefix_sum",
             "rlcs_gae_and_returns", "rlcs_affine_scan", "rlcs_gae_compact",
-            "rlcs_diag_stream_copy", "rlcs_gae_tm", "rlcs_lambda_returns_tm",
+            "rlcs_diag_stream_copy", "rlcs_workspace_bytes_tm", "rlcs_gae_tm",
+            "rlcs_lambda_returns_tm",
             "rlcs_discounted_returns_tm", "rlcs_vtrace_tm", "rlcs_retrace_tm",
             "rlcs_eligibility_traces_tm", "rlcs_episodic_prefix_sum_tm",
             "rlcs_gae_and_returns_tm", "rlcs_affine_scan_tm")
@@ -104,8 +106,11 @@ _ws_lock = threading.Lock()
 _ws_cache = {}
 
 
-def workspace_for(N, T, device, stream=None):
-    need = _lib.rlcs_workspace_bytes(N, T)
+def workspace_for(N, T, device, stream=None, need=None):
+    """The cached workspace of (device, stream), grown to `need` bytes (default:
+    what a row-major [N, T] call needs)."""
+    if need is None:
+        need = _lib.rlcs_workspace_bytes(N, T)
     if need == 0:
         return None, 0
     s = torch.cuda.current_stream(device) if stream is None else stream
@@ -344,8 +349,12 @@ def rlcs_diag_stream_copy(inputs, out, empty=False, stream=None):
 
 # ---------------------------------------------------------------------------
 # Time-major [T, N] variants: same arguments as above with every per-step
-# tensor shaped [T, N]; bootstrap_value / x_init stay [N]. No workspace.
+# tensor shaped [T, N]; bootstrap_value / x_init stay [N].
 # ---------------------------------------------------------------------------
+def _tm_ws(N, T, device, stream):
+    return workspace_for(N, T, device, stream, need=_lib.rlcs_workspace_bytes_tm(N, T))
+
+
 def _tm(*tensors, names, dtypes=None):
     T, N = tensors[0].shape
     out = []
@@ -368,8 +377,9 @@ def rlcs_gae_tm(rewards, values, terminateds, gamma=0.99, lambda_=0.95, bootstra
                                          "next_values"))
     b = _boot(bootstrap_value, N)
     o = torch.empty_like(r) if out is None else out
+    ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_gae_tm(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b), _ptr(o), N, T,
-                            gamma, lambda_, _stream(stream)), "rlcs_gae_tm")
+                            gamma, lambda_, _ptr(ws), wsb, _stream(stream)), "rlcs_gae_tm")
     return o
 
 
@@ -381,8 +391,10 @@ def rlcs_lambda_returns_tm(rewards, values, terminateds, gamma=0.99, lambda_=0.9
                                          "next_values"))
     b = _boot(bootstrap_value, N)
     o = torch.empty_like(r) if out is None else out
+    ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_lambda_returns_tm(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
-                                       _ptr(o), N, T, gamma, lambda_, _stream(stream)),
+                                       _ptr(o), N, T, gamma, lambda_, _ptr(ws), wsb,
+                                       _stream(stream)),
            "rlcs_lambda_returns_tm")
     return o
 
@@ -393,8 +405,9 @@ def rlcs_discounted_returns_tm(rewards, terminateds, gamma=0.99, bootstrap_value
                                names=("rewards", "terminateds", "truncateds", "next_values"))
     b = _boot(bootstrap_value, N)
     o = torch.empty_like(r) if out is None else out
+    ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_discounted_returns_tm(_ptr(r), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b), _ptr(o),
-                                           N, T, gamma, _stream(stream)),
+                                           N, T, gamma, _ptr(ws), wsb, _stream(stream)),
            "rlcs_discounted_returns_tm")
     return o
 
@@ -409,9 +422,10 @@ def rlcs_vtrace_tm(rewards, values, log_rhos, terminateds, gamma=0.99, lambda_=1
     b = _boot(bootstrap_value, N)
     vs = torch.empty_like(r)
     pg = torch.empty_like(r) if with_pg else None
+    ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_vtrace_tm(_ptr(r), _ptr(v), _ptr(lr), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
                                _ptr(vs), _ptr(pg), N, T, gamma, lambda_, rho_bar, c_bar,
-                               _stream(stream)), "rlcs_vtrace_tm")
+                               _ptr(ws), wsb, _stream(stream)), "rlcs_vtrace_tm")
     return vs, pg
 
 
@@ -424,8 +438,10 @@ def rlcs_retrace_tm(rewards, values, q_values, log_rhos, terminateds, gamma=0.99
                                                 "terminateds", "truncateds", "next_values"))
     b = _boot(bootstrap_value, N)
     o = torch.empty_like(r)
+    ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_retrace_tm(_ptr(r), _ptr(v), _ptr(q), _ptr(lr), _ptr(d), _ptr(tr), _ptr(nv),
-                                _ptr(b), _ptr(o), N, T, gamma, lambda_, c_bar, _stream(stream)),
+                                _ptr(b), _ptr(o), N, T, gamma, lambda_, c_bar, _ptr(ws), wsb,
+                                _stream(stream)),
            "rlcs_retrace_tm")
     return o
 
@@ -433,15 +449,19 @@ def rlcs_retrace_tm(rewards, values, q_values, log_rhos, terminateds, gamma=0.99
 def rlcs_eligibility_traces_tm(x, dones, gamma=0.99, lambda_=0.95, stream=None):
     T, N, (xx, d) = _tm(x, dones, names=("x", "dones"))
     o = torch.empty_like(xx)
+    ws, wsb = _tm_ws(N, T, xx.device, stream)
     _check(_lib.rlcs_eligibility_traces_tm(_ptr(xx), _ptr(d), _ptr(o), N, T, gamma, lambda_,
-                                           _stream(stream)), "rlcs_eligibility_traces_tm")
+                                           _ptr(ws), wsb, _stream(stream)),
+           "rlcs_eligibility_traces_tm")
     return o
 
 
 def rlcs_episodic_prefix_sum_tm(x, dones, stream=None):
     T, N, (xx, d) = _tm(x, dones, names=("x", "dones"), dtypes=(torch.int32, torch.float32))
     o = torch.empty_like(xx)
-    _check(_lib.rlcs_episodic_prefix_sum_tm(_ptr(xx), _ptr(d), _ptr(o), N, T, _stream(stream)),
+    ws, wsb = _tm_ws(N, T, xx.device, stream)
+    _check(_lib.rlcs_episodic_prefix_sum_tm(_ptr(xx), _ptr(d), _ptr(o), N, T, _ptr(ws), wsb,
+                                            _stream(stream)),
            "rlcs_episodic_prefix_sum_tm")
     return o
 
@@ -453,9 +473,10 @@ def rlcs_gae_and_returns_tm(rewards, values, terminateds, gamma=0.99, lambda_=0.
                                          "next_values"))
     b = _boot(bootstrap_value, N)
     adv, ret = torch.empty_like(r), torch.empty_like(r)
+    ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_gae_and_returns_tm(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
                                         _ptr(adv), _ptr(ret), N, T, gamma, lambda_,
-                                        _stream(stream)), "rlcs_gae_and_returns_tm")
+                                        _ptr(ws), wsb, _stream(stream)), "rlcs_gae_and_returns_tm")
     return adv, ret
 
 
@@ -463,8 +484,10 @@ def rlcs_affine_scan_tm(a, b, reset=None, x_init=None, reverse=False, stream=Non
     T, N, (aa, bb, rr) = _tm(a, b, reset, names=("a", "b", "reset"))
     x0 = None if x_init is None else _boot(x_init, N)
     o = torch.empty_like(aa)
+    ws, wsb = _tm_ws(N, T, aa.device, stream)
     _check(_lib.rlcs_affine_scan_tm(_ptr(aa), _ptr(bb), _ptr(rr), _ptr(x0), _ptr(o), N, T,
-                                    1 if reverse else 0, _stream(stream)), "rlcs_affine_scan_tm")
+                                    1 if reverse else 0, _ptr(ws), wsb, _stream(stream)),
+           "rlcs_affine_scan_tm")
     return o
 
 

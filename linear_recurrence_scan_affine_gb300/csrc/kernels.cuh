@@ -19,6 +19,8 @@
 //                       waits).
 #pragma once
 
+#include <type_traits>
+
 #include "estimators.cuh"
 
 namespace rlcs {
@@ -927,142 +929,299 @@ __global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
 
 // ---------------------------------------------------------------------------
 // Time-major tier: inputs and outputs [T, N] (element (t, n) at t*N + n).
-// A block owns kTmEnvs environments (kTmEnvsPerWarp per warp) and walks T in tiles of
-// kStrip steps, in scan order, carrying each environment's value from tile
-// to tile: no look-back. Per tile, rows are loaded with coalesced accesses
-// (kTmEnvs consecutive environments per row) into an env-major shared tile
-// padded to kTmPitch floats, so the row writes and each warp's float4 reads
-// of its environment's column are both bank-conflict-free; the warp then runs
-// the strip engine on its column (lane l owns steps 4l..4l+3, exactly as in
-// the warp-row tier), writes its outputs into an output tile of the same
-// layout, and the block stores those rows coalesced.
+// Lane l of every warp owns environment n = 32*g + l of the block's group g,
+// so each load or store instruction of a warp moves one 128-byte row segment
+// (32 consecutive environments at one step) and no data passes through
+// shared memory. A block owns one chunk of kTmChunk steps of its 32
+// environments; warp w holds steps [kTmSteps*w, kTmSteps*(w+1)) of the chunk
+// in registers and composes them serially, per lane, into one affine pair.
+// The warps' pairs meet in shared memory, and warp 0 links the chunk to the
+// chunks before it in scan order with a per-environment decoupled look-back
+// (one workspace record per environment and chunk). Each warp then walks its
+// steps again from its carry-in and stores the outputs.
 // ---------------------------------------------------------------------------
-#ifndef RLCS_TM_ENVS_PER_WARP
-#define RLCS_TM_ENVS_PER_WARP 1
+#ifndef RLCS_TM_WARPS
+#define RLCS_TM_WARPS 16
 #endif
-constexpr int kTmWarps = 8;
-constexpr int kTmEnvsPerWarp = RLCS_TM_ENVS_PER_WARP;  // columns each warp scans, in turn
-constexpr int kTmEnvs = kTmWarps * kTmEnvsPerWarp;     // environments per block
+#ifndef RLCS_TM_STEPS
+#define RLCS_TM_STEPS 8
+#endif
+constexpr int kTmWarps = RLCS_TM_WARPS;        // warps per block
 constexpr int kTmThreads = kTmWarps * 32;
-constexpr int kTmPitch = kStrip + 4;                   // floats per environment column
-constexpr int kTmRowsPerLoad = 32 / kTmEnvs;           // rows one warp instruction covers
-constexpr int kTmRowsPerPass = kTmWarps * kTmRowsPerLoad;
-constexpr int kTmPasses = kStrip / kTmRowsPerPass;
-static_assert(kTmEnvs <= 32 && 32 % kTmEnvs == 0, "a warp covers whole row segments");
+constexpr int kTmSteps = RLCS_TM_STEPS;        // steps per warp (registers per lane)
+constexpr int kTmChunk = kTmWarps * kTmSteps;  // steps per block
+constexpr int kTmEnvs = 32;                    // environments per block (one per lane)
 
-template <class E, bool TRUNC>
-constexpr int tm_tiles() {  // shared tiles: used input slots + outputs
-  return __builtin_popcount(Strips<E, TRUNC, 1>::kUse) + E::kOuts;
+struct TmShape {
+  WsHeader *ws;    // workspace header; NULL when one chunk covers T
+  int64_t groups;  // G = ceil(N / 32)
+  int64_t chunks;  // chunks per environment = ceil(T / kTmChunk)
+};
+
+// Decoupled look-back with one chain per lane (warp-wide call): lane l's
+// record for this chunk is self + l, its predecessors in scan order are
+// self + l - j*stride for j = 1..npred. Inactive lanes (environments past N)
+// neither publish nor wait. Returns the value just outside the chunk on its
+// scan-origin side. Every wait is bounded; on timeout the status word records
+// RLCS_ERR_TIMEOUT and missing aggregates count as the identity.
+template <class P, class V>
+__device__ V lookback_lanes(WsHeader *ws, int64_t self, int64_t stride, int64_t npred, P agg,
+                            uint32_t tag, int lane, bool active) {
+  WsRecord *rec = reinterpret_cast<WsRecord *>(ws + 1) + self + lane;
+  const uint32_t tagA = (tag << 2) | kStateAgg, tagP = (tag << 2) | kStateInc;
+  if (npred == 0) {  // the scan origin: nothing before it
+    if (active) st_relaxed_gpu_u64(&rec->inc, tagged(tagP, vbits(apply(agg, V(0)))));
+    return V(0);
+  }
+  if (active) {
+    st_relaxed_gpu_u64(&rec->m, tagged(tagA, vbits(agg.m)));
+    st_relaxed_gpu_u64(&rec->c, tagged(tagA, vbits(agg.c)));
+  }
+  P acc = identity(P{});
+  V X = V(0);
+  bool done = !active, timed_out = false;
+  int64_t j = 1;  // distance of the predecessor this lane reads next
+  uint64_t start = 0;
+  unsigned backoff = 64;
+  while (!__all_sync(kFull, done)) {
+    bool moved = false;
+    if (!done) {
+      const WsRecord *r = rec - j * stride;
+      const uint64_t wi = ld_relaxed_gpu_u64(&r->inc);
+      if ((uint32_t)(wi >> 32) == tagP) {
+        V incv;
+        vfrom((uint32_t)wi, incv);
+        X = apply(acc, incv);
+        done = moved = true;
+      } else {
+        const uint64_t wm = ld_relaxed_gpu_u64(&r->m), wc = ld_relaxed_gpu_u64(&r->c);
+        if ((uint32_t)(wm >> 32) == tagA && (uint32_t)(wc >> 32) == tagA) {
+          P a;
+          vfrom((uint32_t)wm, a.m);
+          vfrom((uint32_t)wc, a.c);
+          acc = compose(acc, a);
+          moved = true;
+          if (++j > npred) {  // the origin publishes an inclusive value: not reached
+            X = apply(acc, V(0));
+            done = true;
+          }
+        }
+      }
+    }
+    if (__any_sync(kFull, moved)) {
+      start = 0;
+      backoff = 64;
+      continue;
+    }
+    const uint64_t now = globaltimer_ns();
+    if (start == 0) start = now;
+    if (__any_sync(kFull, now - start > kWaitLimitNs)) {
+      if (!done) {
+        X = apply(acc, V(0));
+        done = true;
+      }
+      timed_out = true;
+      break;
+    }
+    __nanosleep(backoff);  // leave issue slots to the warps doing work
+    if (backoff < 1024) backoff <<= 1;
+  }
+  if (timed_out && lane == 0) set_status(ws, kStatusTimeout);
+  if (active) st_relaxed_gpu_u64(&rec->inc, tagged(tagP, vbits(apply(agg, X))));
+  return X;
+}
+
+__device__ __forceinline__ float ldg_at(const void *base, int64_t byte_off) {
+  return __ldg(reinterpret_cast<const float *>(static_cast<const char *>(base) + byte_off));
+}
+
+// One warp's span of kTmSteps steps for its 32 environments. boff[j]: byte
+// offset of step ts+j of this lane's environment; rowb: bytes per row (4N).
+// FULL: the span holds neither step 0 nor step T-1 and every lane's
+// environment exists, so no step needs a bounds check or an edge flag.
+template <int L>
+struct TmRaw {
+  float v[kNumSlots][L];   // inputs at ts .. ts+L-1
+  float next[kNumSlots];   // at ts+L (backward estimators' successor values)
+  float prev_d;            // done mask at ts-1 (forward estimators)
+};
+
+// Issue every load of the span (nothing here waits for one).
+template <class E, bool TRUNC, bool FULL>
+__device__ __forceinline__ void tm_load(const Params &p, const int64_t (&boff)[kTmSteps],
+                                        int64_t rowb, int64_t ts, int64_t T, bool env_ok,
+                                        TmRaw<kTmSteps> &raw) {
+  constexpr uint32_t kUse = E::kSlots | (TRUNC ? E::kOptSlots : 0u);
+  constexpr int L = kTmSteps;
+#pragma unroll
+  for (int k = 0; k < kNumSlots; ++k) {
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+      const bool ok = FULL || (env_ok && ts + j < T);
+      raw.v[k][j] = ((kUse & bit(k)) && ok) ? ldg_at(p.in[k], boff[j]) : 0.f;
+    }
+  }
+  // a span wholly past T (last chunk) reads neither neighbour
+  const bool next_ok = FULL || (env_ok && ts + L < T);
+#pragma unroll
+  for (int k = 0; k < kNumSlots; ++k)
+    raw.next[k] = (E::kBackward && (E::kNext & bit(k)) && next_ok)
+                      ? ldg_at(p.in[k], boff[L - 1] + rowb)
+                      : 0.f;
+  const bool prev_ok = FULL || (env_ok && ts > 0 && ts <= T);
+  raw.prev_d = (E::kPrevD && prev_ok) ? ldg_at(p.in[kD], boff[0] - rowb) : 0.f;
+}
+
+// Build every step's pair; steps past T become the identity (never stored).
+template <class E, bool TRUNC, bool FULL>
+__device__ __forceinline__ void tm_build(const Params &p, const TmRaw<kTmSteps> &raw,
+                                         int64_t ts, int64_t T, float boot,
+                                         typename E::Pair (&e)[kTmSteps],
+                                         float (&aux0)[kTmSteps], float (&aux1)[kTmSteps]) {
+  using P = typename E::Pair;
+  constexpr int L = kTmSteps;
+#pragma unroll
+  for (int j = 0; j < L; ++j) {
+    StepIn st;
+    st.r = raw.v[kR][j];
+    st.v = raw.v[kV][j];
+    st.q = raw.v[kQ][j];
+    st.lr = raw.v[kLR][j];
+    st.d = raw.v[kD][j];
+    st.tau = raw.v[kTau][j];
+    st.nv = raw.v[kNV][j];
+    st.vn = (j + 1 < L) ? raw.v[kV][j + 1] : raw.next[kV];
+    st.qn = (j + 1 < L) ? raw.v[kQ][j + 1] : raw.next[kQ];
+    st.lrn = (j + 1 < L) ? raw.v[kLR][j + 1] : raw.next[kLR];
+    st.dp = (j > 0) ? raw.v[kD][j - 1] : raw.prev_d;
+    st.last = FULL ? false : (ts + j == T - 1);
+    st.first = FULL ? false : (ts + j == 0);
+    aux0[j] = aux1[j] = 0.f;
+    E::template coeff<TRUNC>(p, st, boot, e[j], aux0[j], aux1[j]);
+    if (!FULL && ts + j >= T) e[j] = identity(P{});
+  }
+}
+
+// Walk the span from the value adjacent to it on the scan-origin side and
+// store every step's output(s).
+template <class E, bool FULL>
+__device__ __forceinline__ void tm_emit(const Params &p, const int64_t (&boff)[kTmSteps],
+                                        int64_t ts, int64_t T, bool env_ok,
+                                        typename ValueOf<typename E::Pair>::type nb,
+                                        const typename E::Pair (&e)[kTmSteps],
+                                        const float (&aux0)[kTmSteps],
+                                        const float (&aux1)[kTmSteps]) {
+  using V = typename ValueOf<typename E::Pair>::type;
+  constexpr int L = kTmSteps;
+  char *out0 = static_cast<char *>(p.out0);
+  char *out1 = reinterpret_cast<char *>(p.out1);
+#pragma unroll
+  for (int jj = 0; jj < L; ++jj) {
+    const int j = E::kBackward ? L - 1 - jj : jj;
+    const V A = apply(e[j], nb);
+    if (FULL || (env_ok && ts + j < T)) {
+      if constexpr (std::is_same<V, uint32_t>::value) {
+        *reinterpret_cast<uint32_t *>(out0 + boff[j]) = A;
+      } else {
+        *reinterpret_cast<float *>(out0 + boff[j]) = E::out0(A, nb, e[j], aux0[j], aux1[j]);
+        if constexpr (E::kOuts > 1) {
+          if (out1)
+            *reinterpret_cast<float *>(out1 + boff[j]) = E::out1(A, nb, e[j], aux0[j], aux1[j]);
+        }
+      }
+    }
+    nb = A;
+  }
 }
 
 template <class E, bool TRUNC>
-__global__ void __launch_bounds__(kTmThreads) time_major_kernel(Params p) {
-  using St = Strips<E, TRUNC, 1>;
-  using V = typename St::V;
-  constexpr uint32_t kUse = St::kUse;
-  constexpr int kNumUsed = __builtin_popcount(kUse);
-  extern __shared__ __align__(16) float tm_smem[];  // [kNumUsed + kOuts][kTmEnvs][kTmPitch]
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__global__ void __launch_bounds__(kTmThreads) time_major_kernel(Params p, TmShape sh) {
+  static_assert((E::kBF16Slots | E::kU8Slots) == 0u, "time-major slots are 4-byte words");
+  using P = typename E::Pair;
+  using V = typename ValueOf<P>::type;
+  constexpr int L = kTmSteps;
+  __shared__ P s_agg[kTmWarps][kTmEnvs];
+  __shared__ V s_in[kTmWarps][kTmEnvs];
+  __shared__ uint32_t s_epoch;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t N = p.N, T = p.T;
-  const int64_t env0 = (int64_t)blockIdx.x * kTmEnvs;
-  // loader mapping: one warp instruction = kTmRowsPerLoad rows x kTmEnvs environments
-  const int ld_env = lane % kTmEnvs, ld_row = lane / kTmEnvs;
-  const bool ld_ok = env0 + ld_env < N;
-  const int64_t tiles = (T + kStrip - 1) / kStrip;
-
-  auto tile_of = [&](int idx) { return tm_smem + (size_t)idx * kTmEnvs * kTmPitch; };
+  const int64_t g = blockIdx.x % sh.groups;
+  const int64_t q = blockIdx.x / sh.groups;  // chunk position in scan order
+  const int64_t chunk = E::kBackward ? sh.chunks - 1 - q : q;
+  const int64_t n = g * kTmEnvs + lane;
+  const bool env_ok = n < N;
+  const int64_t ts = chunk * kTmChunk + (int64_t)warp * L;  // this warp's first step
+  const bool chained = sh.chunks > 1;
+  // uniform across the warp: an interior span of a full group of environments
+  const bool full = ts > 0 && ts + L < T && (g + 1) * kTmEnvs <= N;
+  const int64_t rowb = N * 4;
+  int64_t boff[L];
+  boff[0] = (ts * N + n) * 4;
+#pragma unroll
+  for (int j = 1; j < L; ++j) boff[j] = boff[j - 1] + rowb;
 
   pdl_wait();
-  V carry[kTmEnvsPerWarp];
-  float boot[kTmEnvsPerWarp];
-  float halo_next[kTmEnvsPerWarp][kNumSlots];
-  float halo_prev_d[kTmEnvsPerWarp];
+  TmRaw<L> raw;
+  if (full)
+    tm_load<E, TRUNC, true>(p, boff, rowb, ts, T, env_ok, raw);
+  else
+    tm_load<E, TRUNC, false>(p, boff, rowb, ts, T, env_ok, raw);
+  const float boot = (E::kUsesRowValue && p.boot && env_ok) ? __ldg(p.boot + n) : 0.f;
+  if (chained && threadIdx.x == 0) s_epoch = ld_relaxed_gpu(&sh.ws->epoch);
+  // Besides letting the next grid launch, this instruction keeps the
+  // compiler from sinking the loads above into the arithmetic below: every
+  // load of the span is in flight before the first one is waited on.
+  pdl_launch_dependents();
+  P e[L];
+  float aux0[L], aux1[L];
+  if (full)
+    tm_build<E, TRUNC, true>(p, raw, ts, T, boot, e, aux0, aux1);
+  else
+    tm_build<E, TRUNC, false>(p, raw, ts, T, boot, e, aux0, aux1);
+
+  P agg = identity(P{});
+  if (E::kBackward) {
 #pragma unroll
-  for (int q = 0; q < kTmEnvsPerWarp; ++q) {
-    const int64_t env = env0 + warp * kTmEnvsPerWarp + q;
-    boot[q] = (E::kUsesRowValue && p.boot && env < N) ? __ldg(p.boot + env) : 0.f;
-    carry[q] = V(0);
-    halo_prev_d[q] = 0.f;
+    for (int j = L - 1; j >= 0; --j) agg = compose(e[j], agg);
+  } else {
 #pragma unroll
-    for (int k = 0; k < kNumSlots; ++k) halo_next[q][k] = 0.f;
+    for (int j = 0; j < L; ++j) agg = compose(e[j], agg);
   }
+  s_agg[warp][lane] = agg;
+  __syncthreads();
 
-  for (int64_t i = 0; i < tiles; ++i) {
-    const int64_t tt = E::kBackward ? (tiles - 1 - i) : i;
-    const int64_t t0 = tt * kStrip;
-    __syncthreads();  // the previous tile's shared reads are done
-    // coalesced row loads into the env-major tiles
-    {
-      int idx = 0;
-#pragma unroll
-      for (int k = 0; k < kNumSlots; ++k) {
-        if (!(kUse & bit(k))) continue;
-        float *tile = tile_of(idx);
-        float v[kTmPasses];
-#pragma unroll
-        for (int q = 0; q < kTmPasses; ++q) {
-          const int r = q * kTmRowsPerPass + warp * kTmRowsPerLoad + ld_row;
-          const int64_t t = t0 + r;
-          v[q] = (t < T && ld_ok) ? load_slot1<E>(p, k, t * N + env0 + ld_env) : 0.f;
-        }
-#pragma unroll
-        for (int q = 0; q < kTmPasses; ++q) {
-          const int r = q * kTmRowsPerPass + warp * kTmRowsPerLoad + ld_row;
-          tile[ld_env * kTmPitch + r] = v[q];
-        }
-        ++idx;
-      }
+  if (warp == 0) {
+    // the chunk's pair: warps in order outer-first from the scan origin side
+    P cagg = identity(P{});
+    if (E::kBackward) {
+      for (int w = kTmWarps - 1; w >= 0; --w) cagg = compose(s_agg[w][lane], cagg);
+    } else {
+      for (int w = 0; w < kTmWarps; ++w) cagg = compose(s_agg[w][lane], cagg);
     }
-    if (i == 0) pdl_launch_dependents();
-    __syncthreads();
-
-#pragma unroll 1
-    for (int q = 0; q < kTmEnvsPerWarp; ++q) {
-      const int e = warp * kTmEnvsPerWarp + q;  // this warp's column
-      ColumnSource src;
-      {
-        int idx = 0;
-#pragma unroll
-        for (int k = 0; k < kNumSlots; ++k) {
-          src.col[k] = tile_of(idx) + e * kTmPitch;  // unused slots alias a used one
-          if (kUse & bit(k)) ++idx;
-        }
+    V X = V(0);
+    if (chained)
+      X = lookback_lanes<P, V>(sh.ws, (q * sh.groups + g) * kTmEnvs, sh.groups * kTmEnvs, q,
+                               cagg, s_epoch & kTagMask, lane, env_ok);
+    if (E::kBackward) {
+      for (int w = kTmWarps - 1; w >= 0; --w) {
+        s_in[w][lane] = X;
+        X = apply(s_agg[w][lane], X);
       }
-#pragma unroll
-      for (int k = 0; k < kNumSlots; ++k) src.halo_next[k] = halo_next[q][k];
-      src.halo_prev_d = halo_prev_d[q];
-      src.lane = lane;
-      St st;
-      st.template build<true>(p, src, boot[q], t0, T, lane);
-      const auto agg = st.scan(lane);
-      float4 o0[1], o1[1];
-      st.finish(carry[q], o0, o1);
-      carry[q] = apply(agg, carry[q]);
-      // values just outside the next tile in scan order
-#pragma unroll
-      for (int k = 0; k < kNumSlots; ++k)
-        if (E::kBackward && (E::kNext & bit(k))) halo_next[q][k] = src.col[k][0];
-      if (E::kPrevD) halo_prev_d[q] = src.col[kD][kStrip - 1];
-      *reinterpret_cast<float4 *>(tile_of(kNumUsed) + e * kTmPitch + 4 * lane) = o0[0];
-      if constexpr (E::kOuts > 1)
-        *reinterpret_cast<float4 *>(tile_of(kNumUsed + 1) + e * kTmPitch + 4 * lane) = o1[0];
-    }
-    __syncthreads();
-
-    // coalesced row stores
-#pragma unroll
-    for (int o = 0; o < E::kOuts; ++o) {
-      float *dst = (o == 0) ? static_cast<float *>(p.out0) : p.out1;
-      if (dst == nullptr) continue;
-      const float *tile = tile_of(kNumUsed + o);
-#pragma unroll
-      for (int q = 0; q < kTmPasses; ++q) {
-        const int r = q * kTmRowsPerPass + warp * kTmRowsPerLoad + ld_row;
-        const int64_t t = t0 + r;
-        if (t < T && ld_ok) dst[t * N + env0 + ld_env] = tile[ld_env * kTmPitch + r];
+    } else {
+      for (int w = 0; w < kTmWarps; ++w) {
+        s_in[w][lane] = X;
+        X = apply(s_agg[w][lane], X);
       }
     }
   }
+  __syncthreads();
+
+  const V nb = s_in[warp][lane];  // value adjacent to this warp's span, scan-origin side
+  if (full)
+    tm_emit<E, true>(p, boff, ts, T, env_ok, nb, e, aux0, aux1);
+  else
+    tm_emit<E, false>(p, boff, ts, T, env_ok, nb, e, aux0, aux1);
+  if (chained && threadIdx.x == 0) finish_launch(sh.ws, sh.groups * sh.chunks, s_epoch);
 }
 
 }  // namespace rlcs

@@ -20,6 +20,24 @@ struct Plan {
   bool pdl;        // launch with programmatic stream serialization
 };
 
+// Raise Kernel's dynamic shared-memory limit to `bytes` on the current
+// device, once per device (the attribute is per device and per function).
+template <auto Kernel>
+inline cudaError_t allow_dynamic_smem(size_t bytes) {
+  if (bytes <= 48 * 1024) return cudaSuccess;
+  static std::mutex mu;
+  static uint64_t done = 0;  // bit d: set on device d (devices 0..63; others every call)
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t b = dev < 64 ? (uint64_t{1} << dev) : 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (b & done) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done |= b;
+  return e;
+}
+
 template <class K, class... Args>
 inline cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                              bool pdl, Args... args) {
@@ -39,18 +57,14 @@ inline cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaS
 template <class E, bool TRUNC, int S>
 inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws, cudaStream_t s) {
   if (plan.shape == kShapeTimeMajor) {
-    constexpr size_t smem = (size_t)tm_tiles<E, TRUNC>() * kTmEnvs * kTmPitch * 4;
-    if constexpr (smem > 48 * 1024) {
-      static std::once_flag once;
-      static cudaError_t attr_err = cudaSuccess;
-      std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(time_major_kernel<E, TRUNC>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      });
-      if (attr_err != cudaSuccess) return attr_err;
+    if constexpr ((E::kBF16Slots | E::kU8Slots) != 0u) {
+      return cudaErrorInvalidValue;  // no time-major entry takes compact inputs
+    } else {
+      const int64_t groups = (p.N + kTmEnvs - 1) / kTmEnvs;
+      const TmShape sh{plan.Q > 1 ? ws : nullptr, groups, plan.Q};
+      return launch_ex(time_major_kernel<E, TRUNC>, dim3((unsigned)(groups * plan.Q)),
+                       dim3(kTmThreads), 0, s, plan.pdl, p, sh);
     }
-    const dim3 grid((unsigned)((p.N + kTmEnvs - 1) / kTmEnvs));
-    return launch_ex(time_major_kernel<E, TRUNC>, grid, dim3(kTmThreads), smem, s, plan.pdl, p);
   }
   if (plan.shape == RLCS_SHAPE_WARP_ROW) {
     const dim3 grid((unsigned)((p.N + kRowWarps - 1) / kRowWarps));
@@ -70,13 +84,7 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
     }
     constexpr uint32_t kUse = Strips<E, TRUNC, S>::kUse;
     constexpr size_t smem = (size_t)__builtin_popcount(kUse) * kChunkWarps * kStrip * S * 4;
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-      attr_err = cudaFuncSetAttribute(block_chunk_kernel<E, TRUNC, S>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    });
-    if (attr_err != cudaSuccess) return attr_err;
+    if (const cudaError_t e = allow_dynamic_smem<block_chunk_kernel<E, TRUNC, S>>(smem)) return e;
     ChunkShape cs{ws, plan.Q, p.N * plan.Q};
     return launch_ex(block_chunk_kernel<E, TRUNC, S>, dim3((unsigned)(p.N * plan.Q)),
                      dim3(kChunkThreads), smem, s, plan.pdl, p, cs);

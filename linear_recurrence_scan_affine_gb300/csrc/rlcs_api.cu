@@ -57,10 +57,10 @@ rlcs_status plan_call(int64_t N, int64_t T, bool trunc, Plan &plan, bool time_ma
   plan = Plan{};
   plan.trunc = trunc;
   plan.pdl = true;
-  if (time_major) {  // one shape: blocks of environments walk T in tiles
+  if (time_major) {  // one shape: a block per 32 environments and kTmChunk steps
     plan.shape = kShapeTimeMajor;
     plan.S = 1;
-    plan.Q = 1;
+    plan.Q = ceil_div(T, kTmChunk);
     return RLCS_OK;
   }
   const int ov = g_override_shape.load(std::memory_order_relaxed);
@@ -81,6 +81,12 @@ rlcs_status plan_call(int64_t N, int64_t T, bool trunc, Plan &plan, bool time_ma
 
 size_t ws_bytes_for(int64_t N, int64_t Q) {
   return sizeof(WsHeader) + sizeof(WsRecord) * (size_t)N * (size_t)Q;
+}
+
+// Time-major records: one per environment (N rounded up to whole 32-lane
+// groups) and chunk of kTmChunk steps.
+size_t ws_bytes_tm(int64_t N, int64_t T) {
+  return ws_bytes_for(ceil_div(N, kTmEnvs) * kTmEnvs, ceil_div(T, kTmChunk));
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -135,7 +141,9 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
   if (plan.shape != RLCS_SHAPE_WARP_ROW) {
     if (N * plan.Q >= (int64_t)UINT32_MAX) return RLCS_ERR_INVALID_ARG;
     if (plan.Q > 1) {
-      if (!ws || ws_bytes < ws_bytes_for(N, plan.Q) || !aligned16(ws)) return RLCS_ERR_WORKSPACE;
+      const size_t need =
+          plan.shape == kShapeTimeMajor ? ws_bytes_tm(N, T) : ws_bytes_for(N, plan.Q);
+      if (!ws || ws_bytes < need || !aligned16(ws)) return RLCS_ERR_WORKSPACE;
     }
     if (ws && ws_bytes >= sizeof(WsHeader) && aligned16(ws)) wsh = static_cast<WsHeader *>(ws);
     for (int k = 0; k < kNumSlots; ++k) {
@@ -170,6 +178,11 @@ extern "C" {
 size_t rlcs_workspace_bytes(int64_t N, int64_t T) {
   if (N <= 0 || T <= 0) return 0;
   return ws_bytes_for(N, ceil_div(T, kMinChunk));
+}
+
+size_t rlcs_workspace_bytes_tm(int64_t N, int64_t T) {
+  if (N <= 0 || T <= 0) return 0;
+  return ws_bytes_tm(N, T);
 }
 
 rlcs_status rlcs_workspace_init(void *workspace, size_t bytes, rlcs_stream_t stream) {
@@ -417,88 +430,100 @@ extern "C" rlcs_status rlcs_affine_scan(const float *a, const float *b, const fl
 
 // ---------------------------------------------------------------------------
 // Time-major [T, N] entry points: the row-major validation and functors,
-// launched in the time-major shape (which needs no workspace).
+// launched in the time-major shape.
 // ---------------------------------------------------------------------------
 extern "C" {
 
 rlcs_status rlcs_gae_tm(const float *rewards, const float *values, const float *terminateds,
                         const float *truncateds, const float *next_values,
                         const float *bootstrap_value, float *advantages, int64_t N, int64_t T,
-                        float gamma, float lambda, rlcs_stream_t stream) {
+                        float gamma, float lambda, void *workspace, size_t workspace_bytes,
+                        rlcs_stream_t stream) {
   TimeMajorScope tm;
   return rlcs_gae(rewards, values, terminateds, truncateds, next_values, bootstrap_value,
-                  advantages, N, T, gamma, lambda, nullptr, 0, stream);
+                  advantages, N, T, gamma, lambda, workspace, workspace_bytes, stream);
 }
 
 rlcs_status rlcs_lambda_returns_tm(const float *rewards, const float *values,
                                    const float *terminateds, const float *truncateds,
                                    const float *next_values, const float *bootstrap_value,
                                    float *returns, int64_t N, int64_t T, float gamma,
-                                   float lambda, rlcs_stream_t stream) {
+                                   float lambda, void *workspace, size_t workspace_bytes,
+                                   rlcs_stream_t stream) {
   TimeMajorScope tm;
   return rlcs_lambda_returns(rewards, values, terminateds, truncateds, next_values,
-                             bootstrap_value, returns, N, T, gamma, lambda, nullptr, 0, stream);
+                             bootstrap_value, returns, N, T, gamma, lambda, workspace,
+                             workspace_bytes, stream);
 }
 
 rlcs_status rlcs_discounted_returns_tm(const float *rewards, const float *terminateds,
                                        const float *truncateds, const float *next_values,
                                        const float *bootstrap_value, float *returns, int64_t N,
-                                       int64_t T, float gamma, rlcs_stream_t stream) {
+                                       int64_t T, float gamma, void *workspace,
+                                       size_t workspace_bytes, rlcs_stream_t stream) {
   TimeMajorScope tm;
   return rlcs_discounted_returns(rewards, terminateds, truncateds, next_values, bootstrap_value,
-                                 returns, N, T, gamma, nullptr, 0, stream);
+                                 returns, N, T, gamma, workspace, workspace_bytes, stream);
 }
 
 rlcs_status rlcs_vtrace_tm(const float *rewards, const float *values, const float *log_rhos,
                            const float *terminateds, const float *truncateds,
                            const float *next_values, const float *bootstrap_value, float *vs,
                            float *pg_advantages, int64_t N, int64_t T, float gamma,
-                           float lambda, float rho_bar, float c_bar, rlcs_stream_t stream) {
+                           float lambda, float rho_bar, float c_bar, void *workspace,
+                           size_t workspace_bytes, rlcs_stream_t stream) {
   TimeMajorScope tm;
   return rlcs_vtrace(rewards, values, log_rhos, terminateds, truncateds, next_values,
                      bootstrap_value, vs, pg_advantages, N, T, gamma, lambda, rho_bar, c_bar,
-                     nullptr, 0, stream);
+                     workspace, workspace_bytes, stream);
 }
 
 rlcs_status rlcs_retrace_tm(const float *rewards, const float *values, const float *q_values,
                             const float *log_rhos, const float *terminateds,
                             const float *truncateds, const float *next_values,
                             const float *bootstrap_value, float *q_ret, int64_t N, int64_t T,
-                            float gamma, float lambda, float c_bar, rlcs_stream_t stream) {
+                            float gamma, float lambda, float c_bar, void *workspace,
+                            size_t workspace_bytes, rlcs_stream_t stream) {
   TimeMajorScope tm;
   return rlcs_retrace(rewards, values, q_values, log_rhos, terminateds, truncateds, next_values,
-                      bootstrap_value, q_ret, N, T, gamma, lambda, c_bar, nullptr, 0, stream);
+                      bootstrap_value, q_ret, N, T, gamma, lambda, c_bar, workspace,
+                      workspace_bytes, stream);
 }
 
 rlcs_status rlcs_eligibility_traces_tm(const float *x, const float *dones, float *traces,
                                        int64_t N, int64_t T, float gamma, float lambda,
+                                       void *workspace, size_t workspace_bytes,
                                        rlcs_stream_t stream) {
   TimeMajorScope tm;
-  return rlcs_eligibility_traces(x, dones, traces, N, T, gamma, lambda, nullptr, 0, stream);
+  return rlcs_eligibility_traces(x, dones, traces, N, T, gamma, lambda, workspace,
+                                 workspace_bytes, stream);
 }
 
 rlcs_status rlcs_episodic_prefix_sum_tm(const int32_t *x, const float *dones, int32_t *out,
-                                        int64_t N, int64_t T, rlcs_stream_t stream) {
+                                        int64_t N, int64_t T, void *workspace,
+                                        size_t workspace_bytes, rlcs_stream_t stream) {
   TimeMajorScope tm;
-  return rlcs_episodic_prefix_sum(x, dones, out, N, T, nullptr, 0, stream);
+  return rlcs_episodic_prefix_sum(x, dones, out, N, T, workspace, workspace_bytes, stream);
 }
 
 rlcs_status rlcs_gae_and_returns_tm(const float *rewards, const float *values,
                                     const float *terminateds, const float *truncateds,
                                     const float *next_values, const float *bootstrap_value,
                                     float *advantages, float *returns, int64_t N, int64_t T,
-                                    float gamma, float lambda, rlcs_stream_t stream) {
+                                    float gamma, float lambda, void *workspace,
+                                    size_t workspace_bytes, rlcs_stream_t stream) {
   TimeMajorScope tm;
   return rlcs_gae_and_returns(rewards, values, terminateds, truncateds, next_values,
-                              bootstrap_value, advantages, returns, N, T, gamma, lambda, nullptr,
-                              0, stream);
+                              bootstrap_value, advantages, returns, N, T, gamma, lambda,
+                              workspace, workspace_bytes, stream);
 }
 
 rlcs_status rlcs_affine_scan_tm(const float *a, const float *b, const float *reset,
                                 const float *x_init, float *x, int64_t N, int64_t T, int reverse,
-                                rlcs_stream_t stream) {
+                                void *workspace, size_t workspace_bytes, rlcs_stream_t stream) {
   TimeMajorScope tm;
-  return rlcs_affine_scan(a, b, reset, x_init, x, N, T, reverse, nullptr, 0, stream);
+  return rlcs_affine_scan(a, b, reset, x_init, x, N, T, reverse, workspace, workspace_bytes,
+                          stream);
 }
 
 }  // extern "C"

@@ -136,6 +136,30 @@ def test_long_rows_need_a_workspace(lib):
                small) == WORKSPACE
 
 
+def test_time_major_workspace(lib):
+    # one 32-byte record per environment (rounded up to groups of 32) and
+    # chunk, after the 64-byte header; nonzero even when one chunk covers T
+    assert lib.rlcs_workspace_bytes_tm(0, 10) == 0
+    assert lib.rlcs_workspace_bytes_tm(10, 0) == 0
+    one = lib.rlcs_workspace_bytes_tm(32, 1)
+    assert one == 64 + 32 * 32
+    assert lib.rlcs_workspace_bytes_tm(1, 1) == one
+    per_chunk = 32 * 32
+    chunk = next(t for t in range(1, 4097) if lib.rlcs_workspace_bytes_tm(32, t + 1) > one)
+    assert chunk in (32, 64, 128, 256)
+    assert lib.rlcs_workspace_bytes_tm(33, 3 * chunk) == 64 + 2 * 3 * per_chunk
+    # rows longer than one chunk need it; a missing or short one launches nothing
+    a = [fake(i) for i in range(4)]
+    N, T = 4, 1000
+    assert lib.rlcs_gae_tm(a[0], a[1], a[2], None, None, None, a[3], N, T, 0.99, 0.95, None, 0,
+                           None) == WORKSPACE
+    short = lib.rlcs_workspace_bytes_tm(N, T) - 32
+    assert lib.rlcs_gae_tm(a[0], a[1], a[2], None, None, None, a[3], N, T, 0.99, 0.95, fake(9),
+                           short, None) == WORKSPACE
+    assert lib.rlcs_affine_scan_tm(a[0], a[1], None, None, a[3], N, T, 1, None, 0,
+                                   None) == WORKSPACE
+
+
 def test_shape_override_validation(lib):
     assert lib.rlcs_set_shape_override(7, 0) == INVALID
     assert lib.rlcs_set_shape_override(3, 512) == INVALID

@@ -3,9 +3,11 @@
 Inputs are drawn [N, T] as everywhere else, transposed to [T, N] for the
 GPU, and the outputs transposed back and compared element by element with
 the float64 oracle at the usual bar (1e-4 relative; the prefix sum
-bit-exact). Sizes cover ragged environment blocks (N not a multiple of 8),
-ragged and multi-tile T (tiles of 128 steps), truncations and the degenerate
-T = 1.
+bit-exact). A block owns 32 environments and one chunk of T (128 steps);
+chunks of the same environments are linked by a look-back through the
+workspace. Sizes cover ragged environment groups (N not a multiple of 32),
+exact group and chunk edges, ragged and many-chunk T (chains of up to 1024
+chunks), truncations and the degenerate T = 1.
 """
 import numpy as np
 import pytest
@@ -13,11 +15,12 @@ import torch
 
 import oracle
 from synthetic_rollouts import affine_inputs, rollout
-from tests.parity_common import TOL, compare
+from tests.parity_common import TOL, TOL_VLONG, compare
 
 pytestmark = pytest.mark.gpu
 
-SIZES = [(4096, 128), (1000, 300), (7, 1), (33, 129), (256, 1030), (9, 4097)]
+SIZES = [(4096, 128), (1000, 300), (7, 1), (33, 129), (256, 1030), (9, 4097), (32, 128),
+         (31, 129), (64, 16384)]
 PRM = dict(gamma=0.99, lambda_=0.95, rho_bar=1.0, c_bar=1.0)
 
 
@@ -68,10 +71,6 @@ def test_backward_estimators_time_major(rl, N, T, trunc):
             {"out": oracle.lambda_returns(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
 
 
-def _as_np(t):
-    return t if isinstance(t, np.ndarray) else t.cpu().numpy()
-
-
 @pytest.mark.parametrize("N,T", SIZES)
 def test_forward_estimators_time_major(rl, N, T):
     src = rollout(N, T, 12000 + N + T, p_term=0.02)
@@ -91,3 +90,42 @@ def test_affine_scan_time_major(rl, N, T, reverse):
                                       torch.from_numpy(src["x_init"]).cuda(), reverse=reverse))
     want = oracle.affine_scan(src["a"], src["b"], src["reset"], src["x_init"], reverse=reverse)
     compare("affine_scan", {"out": got}, {"out": want}, TOL)
+
+
+def test_very_long_time_major_rows(rl):
+    # 1024 chunks per environment: the longest look-back chains
+    N, T = 8, 131072
+    src = rollout(N, T, 14000, p_term=1e-4)
+    g = {k: (tm(v) if v.ndim == 2 else torch.from_numpy(v).cuda()) for k, v in src.items()}
+    got = back(rl.rlcs_gae_tm(g["rewards"], g["values"], g["terminateds"], 0.999, 1.0,
+                              g["bootstrap_value"]))
+    want = oracle.gae(src["rewards"], src["values"], src["terminateds"], 0.999, 1.0,
+                      src["bootstrap_value"])
+    compare("gae", {"out": got}, {"out": want}, TOL_VLONG)
+    vs, pg = rl.rlcs_vtrace_tm(g["rewards"], g["values"], g["log_rhos"], g["terminateds"],
+                               0.999, 1.0, 1.0, 1.0, g["bootstrap_value"])
+    ovs, opg = oracle.vtrace(src["rewards"], src["values"], src["log_rhos"], src["terminateds"],
+                             0.999, 1.0, 1.0, 1.0, src["bootstrap_value"])
+    compare("vtrace", {"vs": back(vs), "pg": back(pg)}, {"vs": ovs, "pg": opg}, TOL_VLONG)
+
+
+def test_time_major_repeat_calls(rl):
+    # The workspace moves to a new epoch after every chained launch. Every
+    # repeat must meet the oracle; the last bits of float results may differ
+    # with the point where a look-back found an inclusive value, so only the
+    # integer path is required to repeat bit for bit.
+    N, T = 1000, 3000
+    src = rollout(N, T, 15000, p_term=0.01, p_trunc=0.005)
+    g = {k: (tm(v) if v.ndim == 2 else torch.from_numpy(v).cuda()) for k, v in src.items()}
+    kw = dict(truncateds=g["truncateds"], next_values=g["next_values"])
+    want = oracle.retrace(src["rewards"], src["values"], src["q_values"], src["log_rhos"],
+                          src["terminateds"], 0.99, 0.95, 1.0, src["bootstrap_value"],
+                          truncateds=src["truncateds"], next_values=src["next_values"])
+    for _ in range(3):
+        got = rl.rlcs_retrace_tm(g["rewards"], g["values"], g["q_values"], g["log_rhos"],
+                                 g["terminateds"], 0.99, 0.95, 1.0, g["bootstrap_value"], **kw)
+        compare("retrace", {"out": back(got)}, {"out": want}, TOL)
+    first = rl.rlcs_episodic_prefix_sum_tm(g["x_int"], g["terminateds"]).clone()
+    for _ in range(3):
+        assert torch.equal(rl.rlcs_episodic_prefix_sum_tm(g["x_int"], g["terminateds"]), first)
+    rl.check_all_workspaces()
