@@ -63,9 +63,12 @@ EXTRA = {
     "affine_scan": (("a", "b", "reset"), ("out",)),
     "gae_compact": (("rewards_bf16", "values_bf16", "terminateds_u8"), ("out",)),
 }
+# The seven on time-major [T, N] arrays (the _tm entry points), same bytes.
+EXTRA.update({est + "_tm": spec for est, spec in ESTIMATORS.items()})
 ELEM_BYTES = {"rewards_bf16": 2, "values_bf16": 2, "terminateds_u8": 1}   # others: 4
 SPECS = dict(ESTIMATORS, **EXTRA)
-ROW_VALUE = BACKWARD + ("gae_and_returns", "affine_scan", "gae_compact")  # one value per row
+ROW_VALUE = BACKWARD + tuple(e + "_tm" for e in BACKWARD) + (
+    "gae_and_returns", "affine_scan", "gae_compact")  # one value per row
 
 
 def kernel_source_hash():
@@ -299,34 +302,35 @@ def make_sets(torch, rl, src, dev, nsets):
 
 def launch(rl, est, e, prm):
     g, lm = prm["gamma"], prm["lambda_"]
-    if est == "gae":
-        rl.rlcs_gae(e["rewards"], e["values"], e["terminateds"], g, lm, e["bootstrap_value"],
-                    out=e["out"])
-    elif est == "lambda_returns":
-        rl.rlcs_lambda_returns(e["rewards"], e["values"], e["terminateds"], g, lm,
-                               e["bootstrap_value"], out=e["out"])
-    elif est == "discounted_returns":
-        rl.rlcs_discounted_returns(e["rewards"], e["terminateds"], g, e["bootstrap_value"],
-                                   out=e["out"])
-    elif est == "vtrace":
-        rl.rlcs_vtrace(e["rewards"], e["values"], e["log_rhos"], e["terminateds"], g, lm,
-                       prm["rho_bar"], prm["c_bar"], e["bootstrap_value"], out=e["vs"],
-                       out_pg=e["pg"])
-    elif est == "retrace":
-        rl.rlcs_retrace(e["rewards"], e["values"], e["q_values"], e["log_rhos"],
-                        e["terminateds"], g, lm, prm["c_bar"], e["bootstrap_value"], out=e["out"])
-    elif est == "eligibility_traces":
-        rl.rlcs_eligibility_traces(e["x"], e["terminateds"], g, lm, out=e["out"])
-    elif est == "episodic_prefix_sum":
-        rl.rlcs_episodic_prefix_sum(e["x_int"], e["terminateds"], out=e["out"])
-    elif est == "gae_and_returns":
-        rl.rlcs_gae_and_returns(e["rewards"], e["values"], e["terminateds"], g, lm,
-                                e["bootstrap_value"], out=e["out"], out_returns=e["out2"])
-    elif est == "affine_scan":
-        rl.rlcs_affine_scan(e["a"], e["b"], e["reset"], e["x_init"], reverse=True, out=e["out"])
-    elif est == "gae_compact":
-        rl.rlcs_gae_compact(e["rewards_bf16"], e["values_bf16"], e["terminateds_u8"], g, lm,
-                            e["bootstrap_value"], out=e["out"])
+    tm = est.endswith("_tm")  # the time-major entry point of the same estimator
+    base = est[:-3] if tm else est
+    f = getattr(rl, "rlcs_" + est)
+    if base == "gae":
+        f(e["rewards"], e["values"], e["terminateds"], g, lm, e["bootstrap_value"], out=e["out"])
+    elif base == "lambda_returns":
+        f(e["rewards"], e["values"], e["terminateds"], g, lm, e["bootstrap_value"], out=e["out"])
+    elif base == "discounted_returns":
+        f(e["rewards"], e["terminateds"], g, e["bootstrap_value"], out=e["out"])
+    elif base == "vtrace":
+        f(e["rewards"], e["values"], e["log_rhos"], e["terminateds"], g, lm, prm["rho_bar"],
+          prm["c_bar"], e["bootstrap_value"], out=e["vs"], out_pg=e["pg"])
+    elif base == "retrace":
+        f(e["rewards"], e["values"], e["q_values"], e["log_rhos"], e["terminateds"], g, lm,
+          prm["c_bar"], e["bootstrap_value"], out=e["out"])
+    elif base == "eligibility_traces":
+        f(e["x"], e["terminateds"], g, lm, out=e["out"])
+    elif base == "episodic_prefix_sum":
+        f(e["x_int"], e["terminateds"], out=e["out"])
+    elif base == "gae_and_returns":
+        f(e["rewards"], e["values"], e["terminateds"], g, lm, e["bootstrap_value"], out=e["out"],
+          out_returns=e["out2"])
+    elif base == "affine_scan":
+        f(e["a"], e["b"], e["reset"], e["x_init"], reverse=True, out=e["out"])
+    elif base == "gae_compact":
+        f(e["rewards_bf16"], e["values_bf16"], e["terminateds_u8"], g, lm, e["bootstrap_value"],
+          out=e["out"])
+    else:
+        raise ValueError(est)
 
 
 def capture(torch, stream, fn):
@@ -516,13 +520,17 @@ def run_ours(args):
             comp, _ = compact_rollout(nN, nT, seed + 9, w.p_term)
             srcn.update(rewards_bf16=comp["rewards"], values_bf16=comp["values"],
                         terminateds_u8=comp["terminateds"])
+            # the same arrays stored time-major for the _tm entry points
+            srcn_tm = {k: (np.ascontiguousarray(v.T) if v.ndim == 2 else v)
+                       for k, v in srcn.items()}
             res = {}
             for est in EXTRA:
-                r_ = time_alone(torch, rl, est, srcn, dev, stream, prm, l2, nN, nT, seconds=0.08)
+                r_ = time_alone(torch, rl, est, srcn_tm if est.endswith("_tm") else srcn, dev,
+                                stream, prm, l2, nN, nT, seconds=0.08)
                 r_["frac_of_measured_hbm"] = r_["gbs"] / peak
                 res[est] = r_
             next_rows["%dx%d" % (nN, nT)] = res
-            del srcn
+            del srcn, srcn_tm
         rl.check_all_workspaces()
 
     e2e = run_e2e(torch, rl, src, dev, stream, prm, order, max(32, min(K, 512)), N, T)
@@ -571,7 +579,7 @@ def time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T, seconds=0.15):
     sets = []
     for _ in range(nsets):
         e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + (row_key,)}
-        odt = torch.int32 if est == "episodic_prefix_sum" else torch.float32
+        odt = torch.int32 if est.startswith("episodic_prefix_sum") else torch.float32
         for o in outs:
             e[o] = torch.empty(e[ins[0]].shape, dtype=odt, device=dev)
         sets.append(e)

@@ -414,14 +414,14 @@ def rlcs_discounted_returns_tm(rewards, terminateds, gamma=0.99, bootstrap_value
 
 def rlcs_vtrace_tm(rewards, values, log_rhos, terminateds, gamma=0.99, lambda_=1.0, rho_bar=1.0,
                    c_bar=1.0, bootstrap_value=None, truncateds=None, next_values=None,
-                   with_pg=True, stream=None):
+                   with_pg=True, out=None, out_pg=None, stream=None):
     T, N, (r, v, lr, d, tr, nv) = _tm(rewards, values, log_rhos, terminateds, truncateds,
                                       next_values,
                                       names=("rewards", "values", "log_rhos", "terminateds",
                                              "truncateds", "next_values"))
     b = _boot(bootstrap_value, N)
-    vs = torch.empty_like(r)
-    pg = torch.empty_like(r) if with_pg else None
+    vs = torch.empty_like(r) if out is None else out
+    pg = (torch.empty_like(r) if out_pg is None else out_pg) if with_pg else None
     ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_vtrace_tm(_ptr(r), _ptr(v), _ptr(lr), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
                                _ptr(vs), _ptr(pg), N, T, gamma, lambda_, rho_bar, c_bar,
@@ -430,14 +430,14 @@ def rlcs_vtrace_tm(rewards, values, log_rhos, terminateds, gamma=0.99, lambda_=1
 
 
 def rlcs_retrace_tm(rewards, values, q_values, log_rhos, terminateds, gamma=0.99, lambda_=1.0,
-                    c_bar=1.0, bootstrap_value=None, truncateds=None, next_values=None,
+                    c_bar=1.0, bootstrap_value=None, truncateds=None, next_values=None, out=None,
                     stream=None):
     T, N, (r, v, q, lr, d, tr, nv) = _tm(rewards, values, q_values, log_rhos, terminateds,
                                          truncateds, next_values,
                                          names=("rewards", "values", "q_values", "log_rhos",
                                                 "terminateds", "truncateds", "next_values"))
     b = _boot(bootstrap_value, N)
-    o = torch.empty_like(r)
+    o = torch.empty_like(r) if out is None else out
     ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_retrace_tm(_ptr(r), _ptr(v), _ptr(q), _ptr(lr), _ptr(d), _ptr(tr), _ptr(nv),
                                 _ptr(b), _ptr(o), N, T, gamma, lambda_, c_bar, _ptr(ws), wsb,
@@ -446,9 +446,9 @@ def rlcs_retrace_tm(rewards, values, q_values, log_rhos, terminateds, gamma=0.99
     return o
 
 
-def rlcs_eligibility_traces_tm(x, dones, gamma=0.99, lambda_=0.95, stream=None):
+def rlcs_eligibility_traces_tm(x, dones, gamma=0.99, lambda_=0.95, out=None, stream=None):
     T, N, (xx, d) = _tm(x, dones, names=("x", "dones"))
-    o = torch.empty_like(xx)
+    o = torch.empty_like(xx) if out is None else out
     ws, wsb = _tm_ws(N, T, xx.device, stream)
     _check(_lib.rlcs_eligibility_traces_tm(_ptr(xx), _ptr(d), _ptr(o), N, T, gamma, lambda_,
                                            _ptr(ws), wsb, _stream(stream)),
@@ -456,9 +456,9 @@ def rlcs_eligibility_traces_tm(x, dones, gamma=0.99, lambda_=0.95, stream=None):
     return o
 
 
-def rlcs_episodic_prefix_sum_tm(x, dones, stream=None):
+def rlcs_episodic_prefix_sum_tm(x, dones, out=None, stream=None):
     T, N, (xx, d) = _tm(x, dones, names=("x", "dones"), dtypes=(torch.int32, torch.float32))
-    o = torch.empty_like(xx)
+    o = torch.empty_like(xx) if out is None else out
     ws, wsb = _tm_ws(N, T, xx.device, stream)
     _check(_lib.rlcs_episodic_prefix_sum_tm(_ptr(xx), _ptr(d), _ptr(o), N, T, _ptr(ws), wsb,
                                             _stream(stream)),
@@ -467,12 +467,14 @@ def rlcs_episodic_prefix_sum_tm(x, dones, stream=None):
 
 
 def rlcs_gae_and_returns_tm(rewards, values, terminateds, gamma=0.99, lambda_=0.95,
-                            bootstrap_value=None, truncateds=None, next_values=None, stream=None):
+                            bootstrap_value=None, truncateds=None, next_values=None, out=None,
+                            out_returns=None, stream=None):
     T, N, (r, v, d, tr, nv) = _tm(rewards, values, terminateds, truncateds, next_values,
                                   names=("rewards", "values", "terminateds", "truncateds",
                                          "next_values"))
     b = _boot(bootstrap_value, N)
-    adv, ret = torch.empty_like(r), torch.empty_like(r)
+    adv = torch.empty_like(r) if out is None else out
+    ret = torch.empty_like(r) if out_returns is None else out_returns
     ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_gae_and_returns_tm(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
                                         _ptr(adv), _ptr(ret), N, T, gamma, lambda_,
@@ -480,10 +482,10 @@ def rlcs_gae_and_returns_tm(rewards, values, terminateds, gamma=0.99, lambda_=0.
     return adv, ret
 
 
-def rlcs_affine_scan_tm(a, b, reset=None, x_init=None, reverse=False, stream=None):
+def rlcs_affine_scan_tm(a, b, reset=None, x_init=None, reverse=False, out=None, stream=None):
     T, N, (aa, bb, rr) = _tm(a, b, reset, names=("a", "b", "reset"))
     x0 = None if x_init is None else _boot(x_init, N)
-    o = torch.empty_like(aa)
+    o = torch.empty_like(aa) if out is None else out
     ws, wsb = _tm_ws(N, T, aa.device, stream)
     _check(_lib.rlcs_affine_scan_tm(_ptr(aa), _ptr(bb), _ptr(rr), _ptr(x0), _ptr(o), N, T,
                                     1 if reverse else 0, _ptr(ws), wsb, _stream(stream)),

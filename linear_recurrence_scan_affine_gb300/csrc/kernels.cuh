@@ -933,24 +933,20 @@ __global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
 // so each load or store instruction of a warp moves one 128-byte row segment
 // (32 consecutive environments at one step) and no data passes through
 // shared memory. A block owns one chunk of kTmChunk steps of its 32
-// environments; warp w holds steps [kTmSteps*w, kTmSteps*(w+1)) of the chunk
-// in registers and composes them serially, per lane, into one affine pair.
+// environments; warp w holds steps [L*w, L*(w+1)) of the chunk in registers
+// (L = 8 or 16) and composes them serially, per lane, into one affine pair.
 // The warps' pairs meet in shared memory, and warp 0 links the chunk to the
 // chunks before it in scan order with a per-environment decoupled look-back
 // (one workspace record per environment and chunk). Each warp then walks its
 // steps again from its carry-in and stores the outputs.
 // ---------------------------------------------------------------------------
-#ifndef RLCS_TM_WARPS
-#define RLCS_TM_WARPS 16
-#endif
-#ifndef RLCS_TM_STEPS
-#define RLCS_TM_STEPS 8
-#endif
-constexpr int kTmWarps = RLCS_TM_WARPS;        // warps per block
-constexpr int kTmThreads = kTmWarps * 32;
-constexpr int kTmSteps = RLCS_TM_STEPS;        // steps per warp (registers per lane)
-constexpr int kTmChunk = kTmWarps * kTmSteps;  // steps per block
-constexpr int kTmEnvs = 32;                    // environments per block (one per lane)
+constexpr int kTmChunk = 128;  // steps per block (one chunk of 32 environments)
+constexpr int kTmEnvs = 32;    // environments per block (one per lane)
+// A block of kTmChunk/L warps, each holding L steps of the chunk in registers.
+template <int L>
+constexpr int tm_threads() {
+  return kTmChunk / L * 32;
+}
 
 struct TmShape {
   WsHeader *ws;    // workspace header; NULL when one chunk covers T
@@ -1035,7 +1031,7 @@ __device__ __forceinline__ float ldg_at(const void *base, int64_t byte_off) {
   return __ldg(reinterpret_cast<const float *>(static_cast<const char *>(base) + byte_off));
 }
 
-// One warp's span of kTmSteps steps for its 32 environments. boff[j]: byte
+// One warp's span of L steps for its 32 environments. boff[j]: byte
 // offset of step ts+j of this lane's environment; rowb: bytes per row (4N).
 // FULL: the span holds neither step 0 nor step T-1 and every lane's
 // environment exists, so no step needs a bounds check or an edge flag.
@@ -1047,12 +1043,10 @@ struct TmRaw {
 };
 
 // Issue every load of the span (nothing here waits for one).
-template <class E, bool TRUNC, bool FULL>
-__device__ __forceinline__ void tm_load(const Params &p, const int64_t (&boff)[kTmSteps],
-                                        int64_t rowb, int64_t ts, int64_t T, bool env_ok,
-                                        TmRaw<kTmSteps> &raw) {
+template <class E, bool TRUNC, bool FULL, int L>
+__device__ __forceinline__ void tm_load(const Params &p, const int64_t (&boff)[L], int64_t rowb,
+                                        int64_t ts, int64_t T, bool env_ok, TmRaw<L> &raw) {
   constexpr uint32_t kUse = E::kSlots | (TRUNC ? E::kOptSlots : 0u);
-  constexpr int L = kTmSteps;
 #pragma unroll
   for (int k = 0; k < kNumSlots; ++k) {
 #pragma unroll
@@ -1073,13 +1067,11 @@ __device__ __forceinline__ void tm_load(const Params &p, const int64_t (&boff)[k
 }
 
 // Build every step's pair; steps past T become the identity (never stored).
-template <class E, bool TRUNC, bool FULL>
-__device__ __forceinline__ void tm_build(const Params &p, const TmRaw<kTmSteps> &raw,
-                                         int64_t ts, int64_t T, float boot,
-                                         typename E::Pair (&e)[kTmSteps],
-                                         float (&aux0)[kTmSteps], float (&aux1)[kTmSteps]) {
+template <class E, bool TRUNC, bool FULL, int L>
+__device__ __forceinline__ void tm_build(const Params &p, const TmRaw<L> &raw, int64_t ts,
+                                         int64_t T, float boot, typename E::Pair (&e)[L],
+                                         float (&aux0)[L], float (&aux1)[L]) {
   using P = typename E::Pair;
-  constexpr int L = kTmSteps;
 #pragma unroll
   for (int j = 0; j < L; ++j) {
     StepIn st;
@@ -1104,15 +1096,13 @@ __device__ __forceinline__ void tm_build(const Params &p, const TmRaw<kTmSteps> 
 
 // Walk the span from the value adjacent to it on the scan-origin side and
 // store every step's output(s).
-template <class E, bool FULL>
-__device__ __forceinline__ void tm_emit(const Params &p, const int64_t (&boff)[kTmSteps],
-                                        int64_t ts, int64_t T, bool env_ok,
+template <class E, bool FULL, int L>
+__device__ __forceinline__ void tm_emit(const Params &p, const int64_t (&boff)[L], int64_t ts,
+                                        int64_t T, bool env_ok,
                                         typename ValueOf<typename E::Pair>::type nb,
-                                        const typename E::Pair (&e)[kTmSteps],
-                                        const float (&aux0)[kTmSteps],
-                                        const float (&aux1)[kTmSteps]) {
+                                        const typename E::Pair (&e)[L], const float (&aux0)[L],
+                                        const float (&aux1)[L]) {
   using V = typename ValueOf<typename E::Pair>::type;
-  constexpr int L = kTmSteps;
   char *out0 = static_cast<char *>(p.out0);
   char *out1 = reinterpret_cast<char *>(p.out1);
 #pragma unroll
@@ -1134,14 +1124,15 @@ __device__ __forceinline__ void tm_emit(const Params &p, const int64_t (&boff)[k
   }
 }
 
-template <class E, bool TRUNC>
-__global__ void __launch_bounds__(kTmThreads) time_major_kernel(Params p, TmShape sh) {
+template <class E, bool TRUNC, int L>
+__global__ void __launch_bounds__(tm_threads<L>()) time_major_kernel(Params p, TmShape sh) {
   static_assert((E::kBF16Slots | E::kU8Slots) == 0u, "time-major slots are 4-byte words");
+  static_assert(kTmChunk % L == 0 && kTmChunk / L <= 32, "whole warps per chunk");
   using P = typename E::Pair;
   using V = typename ValueOf<P>::type;
-  constexpr int L = kTmSteps;
-  __shared__ P s_agg[kTmWarps][kTmEnvs];
-  __shared__ V s_in[kTmWarps][kTmEnvs];
+  constexpr int kWarps = kTmChunk / L;
+  __shared__ P s_agg[kWarps][kTmEnvs];
+  __shared__ V s_in[kWarps][kTmEnvs];
   __shared__ uint32_t s_epoch;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t N = p.N, T = p.T;
@@ -1163,9 +1154,9 @@ __global__ void __launch_bounds__(kTmThreads) time_major_kernel(Params p, TmShap
   pdl_wait();
   TmRaw<L> raw;
   if (full)
-    tm_load<E, TRUNC, true>(p, boff, rowb, ts, T, env_ok, raw);
+    tm_load<E, TRUNC, true, L>(p, boff, rowb, ts, T, env_ok, raw);
   else
-    tm_load<E, TRUNC, false>(p, boff, rowb, ts, T, env_ok, raw);
+    tm_load<E, TRUNC, false, L>(p, boff, rowb, ts, T, env_ok, raw);
   const float boot = (E::kUsesRowValue && p.boot && env_ok) ? __ldg(p.boot + n) : 0.f;
   if (chained && threadIdx.x == 0) s_epoch = ld_relaxed_gpu(&sh.ws->epoch);
   // Besides letting the next grid launch, this instruction keeps the
@@ -1175,9 +1166,9 @@ __global__ void __launch_bounds__(kTmThreads) time_major_kernel(Params p, TmShap
   P e[L];
   float aux0[L], aux1[L];
   if (full)
-    tm_build<E, TRUNC, true>(p, raw, ts, T, boot, e, aux0, aux1);
+    tm_build<E, TRUNC, true, L>(p, raw, ts, T, boot, e, aux0, aux1);
   else
-    tm_build<E, TRUNC, false>(p, raw, ts, T, boot, e, aux0, aux1);
+    tm_build<E, TRUNC, false, L>(p, raw, ts, T, boot, e, aux0, aux1);
 
   P agg = identity(P{});
   if (E::kBackward) {
@@ -1194,21 +1185,21 @@ __global__ void __launch_bounds__(kTmThreads) time_major_kernel(Params p, TmShap
     // the chunk's pair: warps in order outer-first from the scan origin side
     P cagg = identity(P{});
     if (E::kBackward) {
-      for (int w = kTmWarps - 1; w >= 0; --w) cagg = compose(s_agg[w][lane], cagg);
+      for (int w = kWarps - 1; w >= 0; --w) cagg = compose(s_agg[w][lane], cagg);
     } else {
-      for (int w = 0; w < kTmWarps; ++w) cagg = compose(s_agg[w][lane], cagg);
+      for (int w = 0; w < kWarps; ++w) cagg = compose(s_agg[w][lane], cagg);
     }
     V X = V(0);
     if (chained)
       X = lookback_lanes<P, V>(sh.ws, (q * sh.groups + g) * kTmEnvs, sh.groups * kTmEnvs, q,
                                cagg, s_epoch & kTagMask, lane, env_ok);
     if (E::kBackward) {
-      for (int w = kTmWarps - 1; w >= 0; --w) {
+      for (int w = kWarps - 1; w >= 0; --w) {
         s_in[w][lane] = X;
         X = apply(s_agg[w][lane], X);
       }
     } else {
-      for (int w = 0; w < kTmWarps; ++w) {
+      for (int w = 0; w < kWarps; ++w) {
         s_in[w][lane] = X;
         X = apply(s_agg[w][lane], X);
       }
@@ -1218,9 +1209,9 @@ __global__ void __launch_bounds__(kTmThreads) time_major_kernel(Params p, TmShap
 
   const V nb = s_in[warp][lane];  // value adjacent to this warp's span, scan-origin side
   if (full)
-    tm_emit<E, true>(p, boff, ts, T, env_ok, nb, e, aux0, aux1);
+    tm_emit<E, true, L>(p, boff, ts, T, env_ok, nb, e, aux0, aux1);
   else
-    tm_emit<E, false>(p, boff, ts, T, env_ok, nb, e, aux0, aux1);
+    tm_emit<E, false, L>(p, boff, ts, T, env_ok, nb, e, aux0, aux1);
   if (chained && threadIdx.x == 0) finish_launch(sh.ws, sh.groups * sh.chunks, s_epoch);
 }
 

@@ -62,8 +62,15 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
     } else {
       const int64_t groups = (p.N + kTmEnvs - 1) / kTmEnvs;
       const TmShape sh{plan.Q > 1 ? ws : nullptr, groups, plan.Q};
-      return launch_ex(time_major_kernel<E, TRUNC>, dim3((unsigned)(groups * plan.Q)),
-                       dim3(kTmThreads), 0, s, plan.pdl, p, sh);
+      const dim3 grid((unsigned)(groups * plan.Q));
+      // Measured on GB300: 16 warps of 8 steps for short rows, where more
+      // warps per chunk finish it sooner; 8 warps of 16 steps from T = 1024,
+      // where more bytes in flight per lane pay.
+      if (p.T >= 1024)
+        return launch_ex(time_major_kernel<E, TRUNC, 16>, grid, dim3(tm_threads<16>()), 0, s,
+                         plan.pdl, p, sh);
+      return launch_ex(time_major_kernel<E, TRUNC, 8>, grid, dim3(tm_threads<8>()), 0, s,
+                       plan.pdl, p, sh);
     }
   }
   if (plan.shape == RLCS_SHAPE_WARP_ROW) {

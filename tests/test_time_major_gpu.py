@@ -7,7 +7,8 @@ bit-exact). A block owns 32 environments and one chunk of T (128 steps);
 chunks of the same environments are linked by a look-back through the
 workspace. Sizes cover ragged environment groups (N not a multiple of 32),
 exact group and chunk edges, ragged and many-chunk T (chains of up to 1024
-chunks), truncations and the degenerate T = 1.
+chunks), both warp shapes (8-step spans below T = 1024, 16-step spans from
+there), truncations and the degenerate T = 1.
 """
 import numpy as np
 import pytest
@@ -20,7 +21,7 @@ from tests.parity_common import TOL, TOL_VLONG, compare
 pytestmark = pytest.mark.gpu
 
 SIZES = [(4096, 128), (1000, 300), (7, 1), (33, 129), (256, 1030), (9, 4097), (32, 128),
-         (31, 129), (64, 16384)]
+         (31, 129), (64, 16384), (48, 1023)]
 PRM = dict(gamma=0.99, lambda_=0.95, rho_bar=1.0, c_bar=1.0)
 
 
