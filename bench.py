@@ -741,10 +741,12 @@ def run_profile(args):
     prm = dict(gamma=w.gamma, lambda_=w.lambda_, rho_bar=w.rho_bar, c_bar=w.c_bar)
     src = rollout(N, w.T, w.seed, w.p_term)
     est = args.profile
+    if est.endswith("_tm"):  # the same arrays stored time-major
+        src = {k: (np.ascontiguousarray(v.T) if v.ndim == 2 else v) for k, v in src.items()}
     nsets = max(2, min(ROTATING_SETS, args.sets))
     sets = []
     for _ in range(nsets):
-        ins, outs = ESTIMATORS[est]
+        ins, outs = SPECS[est]
         e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + ("bootstrap_value",)}
         for o in outs:
             e[o] = torch.empty_like(e[ins[0]])
@@ -768,7 +770,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-long-t", action="store_true", help="skip the long-row sweep")
-    ap.add_argument("--profile", choices=tuple(ESTIMATORS), default=None,
+    ap.add_argument("--profile", choices=tuple(SPECS), default=None,
                     help="eager launches of one estimator only (for ncu)")
     ap.add_argument("--workload", default=WORKLOAD, choices=tuple(WORKLOADS))
     ap.add_argument("--rows", type=int, default=0, help="profile mode: rows (0 = workload's N)")
