@@ -629,29 +629,33 @@ def time_diag(torch, rl, n_arrays, dev, stream, l2, N, T, empty, seconds=0.1):
 def run_e2e(torch, rl, src, dev, stream, prm, order, steps, N, T, depth=2, block=16):
     """Whole steps through the public API from pinned host memory.
 
-    Like a rollout buffer, one step's inputs for all seven estimators sit in
-    one contiguous pinned host buffer and its outputs come back into another;
-    each step copies its inputs in with one host-to-device copy, runs the
-    seven rlcs_* calls, and copies every output back with one device-to-host
-    copy. Steps are pipelined over `depth` device buffer slots on separate
-    copy-in, compute and copy-out streams, so step i+1's copy-in overlaps step
-    i's kernels and step i-1's copy-out."""
-    def layout(kind):
+    Like a rollout buffer, one step's rollout (every array any of the seven
+    estimators reads, each once: rewards, values, terminateds, log_rhos,
+    q_values, x, x_int and the bootstrap values) sits in one contiguous pinned
+    host buffer and the outputs come back into another. Each step copies the
+    rollout in with one host-to-device copy, runs the seven rlcs_* calls on
+    it, and copies every output back with one device-to-host copy. Steps are
+    pipelined over `depth` device buffer slots on separate copy-in, compute
+    and copy-out streams, so step i+1's copy-in overlaps step i's kernels and
+    step i-1's copy-out."""
+    in_names = []
+    for est in order:
+        for k in ESTIMATORS[est][0] + ("bootstrap_value",):
+            if k not in in_names:
+                in_names.append(k)
+
+    def place(items):
         off, fields = 0, []
-        for est in order:
-            ins, outs = ESTIMATORS[est]
-            names = ins + ("bootstrap_value",) if kind == "in" else outs
-            for k in names:
-                ref = src[k] if kind == "in" else src["rewards"]
-                nbytes = ref.size * ref.itemsize
-                fields.append((est, k, off, ref.shape, ref.dtype))
-                off += (nbytes + 255) // 256 * 256
+        for key, ref in items:
+            fields.append((key, off, ref.shape, ref.dtype))
+            off += (ref.size * ref.itemsize + 255) // 256 * 256
         return fields, off
 
-    in_fields, in_bytes = layout("in")
-    out_fields, out_bytes = layout("out")
+    in_fields, in_bytes = place([(k, src[k]) for k in in_names])
+    out_fields, out_bytes = place([((est, o), src["rewards"]) for est in order
+                                   for o in ESTIMATORS[est][1]])
     h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
-    for est, k, off, shp, dt in in_fields:
+    for k, off, shp, dt in in_fields:
         a = src[k]
         h_in[off:off + a.size * a.itemsize].copy_(torch.from_numpy(a.view(np.uint8).reshape(-1)))
     h_out = [torch.empty(out_bytes, dtype=torch.uint8).pin_memory() for _ in range(depth)]
@@ -660,11 +664,13 @@ def run_e2e(torch, rl, src, dev, stream, prm, order, steps, N, T, depth=2, block
     tdt = {np.dtype(np.float32): torch.float32, np.dtype(np.int32): torch.int32}
 
     def views(buf_in, buf_out):
-        sets = {est: {} for est in order}
-        for est, k, off, shp, dt in in_fields:
+        shared = {}
+        for k, off, shp, dt in in_fields:
             n = int(np.prod(shp))
-            sets[est][k] = buf_in[off:off + n * 4].view(tdt[dt]).view(*shp)
-        for est, k, off, shp, dt in out_fields:
+            shared[k] = buf_in[off:off + n * 4].view(tdt[dt]).view(*shp)
+        sets = {est: {k: shared[k] for k in ESTIMATORS[est][0] + ("bootstrap_value",)}
+                for est in order}
+        for (est, k), off, shp, dt in out_fields:
             n = int(np.prod(shp))
             ref_dt = tdt[src[ESTIMATORS[est][0][0]].dtype]
             sets[est][k] = buf_out[off:off + n * 4].view(ref_dt).view(*shp)
@@ -723,10 +729,12 @@ def run_e2e(torch, rl, src, dev, stream, prm, order, steps, N, T, depth=2, block
     sec = time_graph(torch, stream, g, reps) / (reps * block)
     return {"value": N * T / sec, "unit": UNIT, "h2d_bytes_per_step": in_bytes,
             "d2h_bytes_per_step": out_bytes, "ms_per_step": sec * 1e3,
-            "path": "one pinned host->device copy of all seven estimators' inputs, seven rlcs_* "
-                    "calls on seven streams, one device->pinned host copy of all outputs, per "
-                    "step; %d-slot pipeline over copy-in / compute / copy-out streams, CUDA "
-                    "graph of %d steps" % (depth, block)}
+            "h2d_gbs": in_bytes / sec / 1e9, "d2h_gbs": out_bytes / sec / 1e9,
+            "path": "one pinned host->device copy of the rollout (each array the seven "
+                    "estimators read, once), seven rlcs_* calls on seven streams, one "
+                    "device->pinned host copy of all outputs, per step; %d-slot pipeline over "
+                    "copy-in / compute / copy-out streams, CUDA graph of %d steps"
+                    % (depth, block)}
 
 
 def run_profile(args):
