@@ -22,9 +22,10 @@ struct Plan {
 
 // Raise Kernel's dynamic shared-memory limit to `bytes` on the current
 // device, once per device (the attribute is per device and per function).
+// Set even below 48 KiB: without it, static plus dynamic shared memory must
+// fit in 48 KiB together.
 template <auto Kernel>
 inline cudaError_t allow_dynamic_smem(size_t bytes) {
-  if (bytes <= 48 * 1024) return cudaSuccess;
   static std::mutex mu;
   static uint64_t done = 0;  // bit d: set on device d (devices 0..63; others every call)
   int dev = 0;
