@@ -333,6 +333,31 @@ def launch(rl, est, e, prm):
         raise ValueError(est)
 
 
+def group_kwargs(est, e, prm):
+    """Keyword arguments of rlcs_run_group for one estimator's buffer set."""
+    g, lm = prm["gamma"], prm["lambda_"]
+    if est in ("gae", "lambda_returns"):
+        return dict(rewards=e["rewards"], values=e["values"], terminateds=e["terminateds"],
+                    gamma=g, lambda_=lm, bootstrap_value=e["bootstrap_value"], out=e["out"])
+    if est == "discounted_returns":
+        return dict(rewards=e["rewards"], terminateds=e["terminateds"], gamma=g,
+                    bootstrap_value=e["bootstrap_value"], out=e["out"])
+    if est == "vtrace":
+        return dict(rewards=e["rewards"], values=e["values"], log_rhos=e["log_rhos"],
+                    terminateds=e["terminateds"], gamma=g, lambda_=lm, rho_bar=prm["rho_bar"],
+                    c_bar=prm["c_bar"], bootstrap_value=e["bootstrap_value"], out=e["vs"],
+                    out_pg=e["pg"])
+    if est == "retrace":
+        return dict(rewards=e["rewards"], values=e["values"], q_values=e["q_values"],
+                    log_rhos=e["log_rhos"], terminateds=e["terminateds"], gamma=g, lambda_=lm,
+                    c_bar=prm["c_bar"], bootstrap_value=e["bootstrap_value"], out=e["out"])
+    if est == "eligibility_traces":
+        return dict(x=e["x"], dones=e["terminateds"], gamma=g, lambda_=lm, out=e["out"])
+    if est == "episodic_prefix_sum":
+        return dict(x=e["x_int"], dones=e["terminateds"], out=e["out"])
+    raise ValueError(est)
+
+
 def capture(torch, stream, fn):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
@@ -408,8 +433,21 @@ def run_ours(args):
         for est in order:
             stream.wait_stream(side[est])
 
+    # the seven calls of a step as one grouped launch (rlcs_run_group)
+    group_calls = [[(est, group_kwargs(est, sets[i][est], prm)) for est in order]
+                   for i in range(ROTATING_SETS)]
+    with torch.cuda.stream(stream):
+        for i in range(ROTATING_SETS):
+            rl.rlcs_run_group(group_calls[i])
+    torch.cuda.synchronize()
+
+    def grouped_block():
+        for i in range(BLOCK):
+            rl.rlcs_run_group(group_calls[i % ROTATING_SETS])
+
     graphs = {"serial": capture(torch, stream, serial_block),
-              "concurrent": capture(torch, stream, concurrent_block)}
+              "concurrent": capture(torch, stream, concurrent_block),
+              "grouped": capture(torch, stream, grouped_block)}
     K = max(args.steps, 1)
     reps = (K + BLOCK - 1) // BLOCK
     K = reps * BLOCK
@@ -420,8 +458,11 @@ def run_ours(args):
                 g_.replay()
     torch.cuda.synchronize()
 
-    # the serial schedule, timed first (reported beside the headline)
-    serial_sec = time_graph(torch, stream, graphs["serial"], reps) / K
+    # every schedule timed once; the fastest is timed again as the headline,
+    # with the clocks sampled (the others are reported beside it)
+    sched_sec = {k: time_graph(torch, stream, g_, reps) / K for k, g_ in graphs.items()}
+    serial_sec = sched_sec["serial"]
+    headline = min(("concurrent", "grouped"), key=lambda k: sched_sec[k])
 
     sampler = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ
                            else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
@@ -435,7 +476,7 @@ def run_ours(args):
     with torch.cuda.stream(stream):
         t_start.record(stream)
         for _ in range(reps):
-            graphs["concurrent"].replay()
+            graphs[headline].replay()
         t_end.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
@@ -455,7 +496,12 @@ def run_ours(args):
     per_est = {}
     for est in order:
         per_est[est] = time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T)
-    dom = max(per_est, key=lambda e: per_est[e]["us_per_launch"])
+    # the dominant kernel: the grouped kernel when it is the headline (one
+    # launch per step), else the slowest estimator alone
+    grouped = headline == "grouped"
+    dom = "group" if grouped else max(per_est, key=lambda e: per_est[e]["us_per_launch"])
+    dom_bytes = step_bytes if grouped else bytes_per_launch(dom, N, T)
+    dom_us = 1e6 * elapsed / K if grouped else per_est[dom]["us_per_launch"]
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -474,25 +520,36 @@ def run_ours(args):
         # counters count only for the kernel sources they were taken on
         if tr.get("kernel_source_sha256_16") == kernel_source_hash():
             traffic = tr.get("%s_%dx%d" % (dom, N, T))
-    achieved = per_est[dom]["gbs"]
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+    achieved = dom_bytes / (dom_us * 1e-6) / 1e9
+    roofline = {"bound": "hbm",
+                "kernel": ("group_row_kernel: the seven estimators in one launch" if grouped
+                           else dom),
+                "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
-                "traffic": traffic, "bytes_per_launch": bytes_per_launch(dom, N, T),
-                "us_per_launch": per_est[dom]["us_per_launch"],
-                "timing": "kernel alone: CUDA graph of back-to-back launches, each on its own "
-                          "buffer set (rotation >= 3x L2), CUDA events on the launching stream"}
+                "traffic": traffic, "bytes_per_launch": dom_bytes, "us_per_launch": dom_us,
+                "timing": ("the headline's timed region: one grouped launch per step on its "
+                           "own buffer set (rotation >= 3x L2), CUDA events on the launching "
+                           "stream" if grouped else
+                           "kernel alone: CUDA graph of back-to-back launches, each on its own "
+                           "buffer set (rotation >= 3x L2), CUDA events on the launching "
+                           "stream")}
     # what any launch of this size and shape costs: the diagnostic copy of the
-    # same bytes, and the same grid doing nothing
-    n_arrays = len(SPECS[dom][0]) + len(SPECS[dom][1])
-    copy_us = time_diag(torch, rl, n_arrays, dev, stream, l2, N, T, False)
-    empty_us = time_diag(torch, rl, n_arrays, dev, stream, l2, N, T, True)
+    # same bytes (for the group: 16-byte elements over as many rows as make
+    # the step's bytes), and the same grid doing nothing
+    if grouped:
+        n_arrays, n_rows = 4, step_bytes // (16 * T)
+    else:
+        n_arrays, n_rows = len(SPECS[dom][0]) + len(SPECS[dom][1]), N
+    copy_us = time_diag(torch, rl, n_arrays, dev, stream, l2, n_rows, T, False)
+    empty_us = time_diag(torch, rl, n_arrays, dev, stream, l2, n_rows, T, True)
     roofline["reference"] = {
         "stream_copy_us": copy_us, "empty_launch_us": empty_us,
-        "stream_copy_frac": bytes_per_launch(dom, N, T) / (copy_us * 1e-6) / 1e9 / peak,
-        "kernel_over_copy": per_est[dom]["us_per_launch"] / copy_us,
-        "what": "rlcs_diag_stream_copy: the warp-row launch shape moving the same bytes with no "
-                "scan (same prefetch and programmatic dependent launch); empty = the same grid "
-                "that only waits and exits"}
+        "stream_copy_frac": dom_bytes / (copy_us * 1e-6) / 1e9 / peak,
+        "kernel_over_copy": dom_us / copy_us,
+        "what": "rlcs_diag_stream_copy: the warp-row launch shape moving the same bytes "
+                "(%d arrays x %d rows x %d steps) with no scan (same prefetch and programmatic "
+                "dependent launch); empty = the same grid that only waits and exits"
+                % (n_arrays, n_rows, T)}
 
     # the long-row recipes, every estimator alone (same method as above)
     long_t = {}
@@ -550,9 +607,19 @@ def run_ours(args):
                        "bytes_per_step_algorithmic": step_bytes,
                        "l2": "inputs larger than L2: %d rotating buffer sets, %.0f MB footprint "
                              "= %.1fx L2" % (ROTATING_SETS, footprint / 1e6, footprint / l2),
-                       "launch": "CUDA graph of %d steps; the seven estimators on seven "
-                                 "streams (fork/join), programmatic dependent launch "
-                                 "within each stream" % BLOCK,
+                       "launch": ("CUDA graph of %d steps; each step one rlcs_run_group "
+                                  "call: the seven estimators in one launch, programmatic "
+                                  "dependent launch between steps" % BLOCK if grouped else
+                                  "CUDA graph of %d steps; the seven estimators on seven "
+                                  "streams (fork/join), programmatic dependent launch "
+                                  "within each stream" % BLOCK),
+                       "schedules": {k: {"ms_per_step": v * 1e3,
+                                         "value": world * N * T / v,
+                                         "launches_per_step": 1 if k == "grouped" else 7}
+                                     for k, v in sched_sec.items()},
+                       "schedule_notes": {"serial": "seven rlcs_* calls on one stream",
+                                          "concurrent": "seven rlcs_* calls on seven streams",
+                                          "grouped": "one rlcs_run_group call"},
                        "serial_schedule": {"ms_per_step": serial_sec * 1e3,
                                            "value": world * N * T / serial_sec,
                                            "note": "same steps, all seven calls on one "
@@ -561,7 +628,7 @@ def run_ours(args):
             "hbm_gbs": step_gbs, "hbm_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
             "hbm_frac_of_measured": step_gbs / peak,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": 7 * K, "clocks": clocks, "per_estimator": per_est,
+            "gpu_launches": (1 if grouped else 7) * K, "clocks": clocks, "per_estimator": per_est,
             "long_t_sweep": long_t, "next_rows": next_rows,
         }
         print(json.dumps(line), flush=True)

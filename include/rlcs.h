@@ -302,6 +302,59 @@ rlcs_status rlcs_affine_scan_tm(const float *a, const float *b, const float *res
                                 const float *x_init, float *x, int64_t N, int64_t T, int reverse,
                                 void *workspace, size_t workspace_bytes, rlcs_stream_t stream);
 
+/* Grouped calls. Several estimator calls on short rows (T <= 512 each) run
+ * in one kernel launch instead of one launch each: every call computes
+ * exactly what its namesake entry point computes (same definitions, same
+ * validation), on its own arrays and sizes. A launch has a fixed cost of a
+ * few microseconds whatever its size, which dominates calls of a few MB
+ * (4096 x 128 rows); one launch for the group pays it once. The paper has no
+ * counterpart: it is a launch-level convenience for the seven estimators.
+ *
+ * rlcs_call: one call. `estimator` selects the namesake; the pointer fields
+ * are that entry point's arguments (rewards holds x for the two forward
+ * estimators, int32 for the prefix sum; terminateds holds their dones; out
+ * is the first output, out2 V-trace's pg_advantages (may be NULL) or the
+ * fused call's returns). Fields the estimator does not take are ignored;
+ * `reserved` must be 0. All pointers are device memory owned by the caller.
+ *
+ * Calls are grouped by strips per row (T <= 128, <= 256, <= 512) and by
+ * whether their truncation inputs are present; each class is one launch, in
+ * the order of first appearance, on `stream`. Errors: RLCS_ERR_INVALID_ARG
+ * for more than RLCS_MAX_GROUP calls, a call with T > 512, any argument its
+ * namesake would reject, or an output of one call overlapping any array of
+ * another call (the calls run concurrently); nothing is launched then.
+ * RLCS_ERR_CUDA if a launch fails. No workspace is used. */
+#define RLCS_MAX_GROUP 16
+typedef enum {
+  RLCS_EST_GAE = 0,
+  RLCS_EST_LAMBDA_RETURNS = 1,
+  RLCS_EST_DISCOUNTED_RETURNS = 2,
+  RLCS_EST_VTRACE = 3,
+  RLCS_EST_RETRACE = 4,
+  RLCS_EST_ELIGIBILITY_TRACES = 5,
+  RLCS_EST_EPISODIC_PREFIX_SUM = 6,
+  RLCS_EST_GAE_AND_RETURNS = 7
+} rlcs_estimator;
+
+typedef struct {
+  int32_t estimator; /* rlcs_estimator */
+  int32_t reserved;  /* must be 0 */
+  const void *rewards;
+  const float *values;
+  const float *q_values;
+  const float *log_rhos;
+  const float *terminateds;
+  const float *truncateds;
+  const float *next_values;
+  const float *bootstrap_value;
+  void *out;
+  float *out2;
+  int64_t N, T;
+  float gamma, lambda, rho_bar, c_bar;
+} rlcs_call;
+
+rlcs_status rlcs_run_group(const rlcs_call *calls, int n_calls, rlcs_stream_t stream);
+
 /* GAE for callers that cannot allocate device memory.
  * The paper has no counterpart: this is a library convenience. Some callers
  * cannot call cudaMalloc, such as a plugin inside a host program that owns

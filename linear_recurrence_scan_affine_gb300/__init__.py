@@ -15,5 +15,5 @@ from .binding import (  # noqa: F401
     rlcs_affine_scan, rlcs_gae_and_returns, rlcs_gae_compact, rlcs_diag_stream_copy,
     rlcs_gae_tm, rlcs_lambda_returns_tm, rlcs_discounted_returns_tm, rlcs_vtrace_tm,
     rlcs_retrace_tm, rlcs_eligibility_traces_tm, rlcs_episodic_prefix_sum_tm,
-    rlcs_gae_and_returns_tm, rlcs_affine_scan_tm,
+    rlcs_gae_and_returns_tm, rlcs_affine_scan_tm, rlcs_run_group, GROUP_ESTIMATORS, MAX_GROUP,
     workspace_for)

@@ -59,6 +59,7 @@ def _load():
         "rlcs_eligibility_traces_tm": ([P] * 3 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
         "rlcs_episodic_prefix_sum_tm": ([P] * 3 + [I64, I64, P, SZ, P], ctypes.c_int),
         "rlcs_gae_and_returns_tm": ([P] * 8 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
+        "rlcs_run_group": ([P, ctypes.c_int, P], ctypes.c_int),
         "rlcs_affine_scan_tm": ([P] * 5 + [I64, I64, ctypes.c_int, P, SZ, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -78,7 +79,7 @@ EXPORTED = ("rlcs_workspace_bytes", "rlcs_workspace_init", "rlcs_check_status",
             "rlcs_lambda_returns_tm",
             "rlcs_discounted_returns_tm", "rlcs_vtrace_tm", "rlcs_retrace_tm",
             "rlcs_eligibility_traces_tm", "rlcs_episodic_prefix_sum_tm",
-            "rlcs_gae_and_returns_tm", "rlcs_affine_scan_tm")
+            "rlcs_gae_and_returns_tm", "rlcs_affine_scan_tm", "rlcs_run_group")
 
 
 def lib():
@@ -491,6 +492,129 @@ def rlcs_affine_scan_tm(a, b, reset=None, x_init=None, reverse=False, out=None, 
                                     1 if reverse else 0, _ptr(ws), wsb, _stream(stream)),
            "rlcs_affine_scan_tm")
     return o
+
+
+# ---------------------------------------------------------------------------
+# Grouped calls on short rows (T <= 512): one launch per class of calls.
+# ---------------------------------------------------------------------------
+class RlcsCall(ctypes.Structure):
+    """Mirror of rlcs_call in include/rlcs.h."""
+    _fields_ = [("estimator", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("rewards", ctypes.c_void_p), ("values", ctypes.c_void_p),
+                ("q_values", ctypes.c_void_p), ("log_rhos", ctypes.c_void_p),
+                ("terminateds", ctypes.c_void_p), ("truncateds", ctypes.c_void_p),
+                ("next_values", ctypes.c_void_p), ("bootstrap_value", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("out2", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("T", ctypes.c_int64),
+                ("gamma", ctypes.c_float), ("lambda_", ctypes.c_float),
+                ("rho_bar", ctypes.c_float), ("c_bar", ctypes.c_float)]
+
+
+GROUP_ESTIMATORS = {"gae": 0, "lambda_returns": 1, "discounted_returns": 2, "vtrace": 3,
+                    "retrace": 4, "eligibility_traces": 5, "episodic_prefix_sum": 6,
+                    "gae_and_returns": 7}
+MAX_GROUP = 16
+
+
+def _group_call(est, kw):
+    """(RlcsCall, result, tensors to keep alive) for one grouped call; the
+    keywords and defaults are those of the namesake wrapper."""
+    kw = dict(kw)
+    c = RlcsCall()
+    c.estimator = GROUP_ESTIMATORS[est]
+    keep = []
+
+    def take(name, dtype=torch.float32, required=True):
+        t = kw.pop(name, None)
+        if t is None:
+            if required:
+                raise ValueError("%s: %s is required" % (est, name))
+            return None
+        x = _rows(t, name, dtype)
+        keep.append(x)
+        return x
+
+    if est in ("eligibility_traces", "episodic_prefix_sum"):
+        x = take("x", torch.int32 if est == "episodic_prefix_sum" else torch.float32)
+        d = take("dones")
+        N, T = x.shape
+        if d.shape != (N, T):
+            raise ValueError("dones must have shape (%d, %d)" % (N, T))
+        c.rewards, c.terminateds = x.data_ptr(), d.data_ptr()
+        lead = x
+    else:
+        r = take("rewards")
+        N, T = r.shape
+        named = {"values": est != "discounted_returns",
+                 "q_values": est == "retrace",
+                 "log_rhos": est in ("vtrace", "retrace"),
+                 "terminateds": True}
+        for name, used in named.items():
+            if used:
+                t = take(name)
+                if t.shape != (N, T):
+                    raise ValueError("%s must have shape (%d, %d)" % (name, N, T))
+                setattr(c, name, t.data_ptr())
+        for name in ("truncateds", "next_values"):
+            t = _opt(kw.pop(name, None), name, N, T)
+            if t is not None:
+                keep.append(t)
+                setattr(c, name, t.data_ptr())
+        b = _boot(kw.pop("bootstrap_value", None), N)
+        if b is not None:
+            keep.append(b)
+            c.bootstrap_value = b.data_ptr()
+        c.rewards = r.data_ptr()
+        lead = r
+    lam_default = 1.0 if est in ("vtrace", "retrace") else 0.95
+    c.gamma = kw.pop("gamma", 0.99)
+    c.lambda_ = kw.pop("lambda_", lam_default)
+    c.rho_bar = kw.pop("rho_bar", 1.0)
+    c.c_bar = kw.pop("c_bar", 1.0)
+    c.N, c.T = N, T
+    out = kw.pop("out", None)
+    out = torch.empty_like(lead) if out is None else out
+    keep.append(out)
+    c.out = out.data_ptr()
+    result = out
+    if est == "vtrace":
+        pg = kw.pop("out_pg", None)
+        if kw.pop("with_pg", True):
+            pg = torch.empty_like(lead) if pg is None else pg
+            keep.append(pg)
+            c.out2 = pg.data_ptr()
+        else:
+            pg = None
+        result = (out, pg)
+    elif est == "gae_and_returns":
+        ret = kw.pop("out_returns", None)
+        ret = torch.empty_like(lead) if ret is None else ret
+        keep.append(ret)
+        c.out2 = ret.data_ptr()
+        result = (out, ret)
+    if kw:
+        raise TypeError("%s: unexpected arguments %s" % (est, sorted(kw)))
+    return c, result, keep
+
+
+def rlcs_run_group(calls, stream=None):
+    """Run up to MAX_GROUP estimator calls on short rows (T <= 512) in one
+    launch per class (rows up to 128 / 256 / 512 steps, truncation inputs
+    present or not). `calls` is a list of (estimator, kwargs) pairs: the
+    estimator is a key of GROUP_ESTIMATORS and kwargs are what its namesake
+    wrapper takes (x and dones for the two forward estimators). Returns the
+    namesakes' results, in order. No output may overlap another call's
+    arrays: the calls run concurrently."""
+    arr = (RlcsCall * max(1, len(calls)))()
+    keep, results = [], []
+    for i, (est, kw) in enumerate(calls):
+        c, res, k = _group_call(est, kw)
+        arr[i] = c
+        keep += k
+        results.append(res)
+    _check(_lib.rlcs_run_group(ctypes.cast(arr, ctypes.c_void_p), len(calls), _stream(stream)),
+           "rlcs_run_group")
+    return results
 
 
 def rlcs_check_status(workspace=None, stream=None):

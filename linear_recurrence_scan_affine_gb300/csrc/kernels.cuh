@@ -451,12 +451,13 @@ struct Strips {
 // ---------------------------------------------------------------------------
 // Warp-row tier: one warp per row, S strips (T <= 128*S).
 // ---------------------------------------------------------------------------
+// One block of the warp-row tier: rows kRowWarps*block .. +kRowWarps-1.
 template <class E, bool TRUNC, int S>
-__global__ void __launch_bounds__(kRowWarps * 32) warp_row_kernel(Params p) {
+__device__ __forceinline__ void warp_row_body(const Params &p, int64_t block) {
   using St = Strips<E, TRUNC, S>;
   using V = typename St::V;
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * kRowWarps + (threadIdx.x >> 5);
+  const int64_t row = block * kRowWarps + (threadIdx.x >> 5);
   const int64_t T = p.T;
   const int64_t base = row * T;
   const bool vec = p.vec != 0;
@@ -512,6 +513,56 @@ __global__ void __launch_bounds__(kRowWarps * 32) warp_row_kernel(Params p) {
         if (p.out1) store4(p.out1 + base, t, T, false, o1[j]);
       }
     }
+  }
+}
+
+template <class E, bool TRUNC, int S>
+__global__ void __launch_bounds__(kRowWarps * 32) warp_row_kernel(Params p) {
+  warp_row_body<E, TRUNC, S>(p, blockIdx.x);
+}
+
+// ---------------------------------------------------------------------------
+// Grouped warp-row launch: several independent calls on short rows (T <= 128*S)
+// in one grid. Call c owns blocks [first_block[c], first_block[c+1]) and runs
+// the warp-row body of its estimator on them, so the group pays one launch's
+// fixed cost. Calls in one group share S and whether their optional inputs are
+// present.
+// ---------------------------------------------------------------------------
+constexpr int kMaxGroup = 16;
+enum GroupKind : int {
+  kGroupGae = 0,
+  kGroupLambdaReturns,
+  kGroupDiscountedReturns,
+  kGroupVTrace,
+  kGroupRetrace,
+  kGroupEligibilityTraces,
+  kGroupEpisodicPrefixSum,
+  kGroupGaeAndReturns,
+  kGroupKinds
+};
+struct GroupParams {
+  int n;                                // calls in the group
+  int kind[kMaxGroup];                  // GroupKind of each call
+  int64_t first_block[kMaxGroup + 1];   // block ranges; first_block[n] = grid size
+  Params p[kMaxGroup];
+};
+
+template <bool TRUNC, int S>
+__global__ void __launch_bounds__(kRowWarps * 32) group_row_kernel(GroupParams gp) {
+  int c = 0;  // uniform per block
+  while (c + 1 < gp.n && (int64_t)blockIdx.x >= gp.first_block[c + 1]) ++c;
+  const int64_t b = (int64_t)blockIdx.x - gp.first_block[c];
+  const Params &p = gp.p[c];
+  switch (gp.kind[c]) {
+    case kGroupGae: warp_row_body<Gae, TRUNC, S>(p, b); break;
+    case kGroupLambdaReturns: warp_row_body<LambdaReturns, TRUNC, S>(p, b); break;
+    case kGroupDiscountedReturns: warp_row_body<DiscountedReturns, TRUNC, S>(p, b); break;
+    case kGroupVTrace: warp_row_body<VTrace, TRUNC, S>(p, b); break;
+    case kGroupRetrace: warp_row_body<Retrace, TRUNC, S>(p, b); break;
+    case kGroupEligibilityTraces: warp_row_body<EligibilityTraces, false, S>(p, b); break;
+    case kGroupEpisodicPrefixSum: warp_row_body<EpisodicPrefixSum, false, S>(p, b); break;
+    case kGroupGaeAndReturns: warp_row_body<GaeAndReturns, TRUNC, S>(p, b); break;
+    default: break;
   }
 }
 

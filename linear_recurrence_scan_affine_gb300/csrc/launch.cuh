@@ -130,5 +130,7 @@ cudaError_t launch_gae_and_returns(const Params &, const Plan &, WsHeader *, cud
 cudaError_t launch_gae_compact(const Params &, const Plan &, WsHeader *, cudaStream_t);
 cudaError_t launch_affine_forward(const Params &, const Plan &, WsHeader *, cudaStream_t);
 cudaError_t launch_affine_backward(const Params &, const Plan &, WsHeader *, cudaStream_t);
+// One launch of grouped warp-row calls sharing S and the optional-input flag.
+cudaError_t launch_group(const GroupParams &gp, int S, bool trunc, cudaStream_t s);
 
 }  // namespace rlcs

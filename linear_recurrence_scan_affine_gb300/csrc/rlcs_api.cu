@@ -27,6 +27,45 @@ struct TimeMajorScope {
   ~TimeMajorScope() { t_time_major = false; }
 };
 
+struct Buf {
+  const void *p;
+  size_t bytes;
+};
+bool overlaps(const Buf &a, const Buf &b) {
+  if (!a.p || !b.p) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// Set while rlcs_run_group passes its calls through their namesake entry
+// points: run() validates each call as usual, then records it here instead
+// of launching it.
+struct GroupEntry {
+  Params p;
+  int kind;
+  int S;
+  bool trunc;
+  Buf reads[kNumSlots + 1];  // input planes and the bootstrap array
+  Buf writes[2];
+};
+struct GroupCollect {
+  int n = 0;
+  GroupEntry e[kMaxGroup];
+};
+thread_local GroupCollect *t_group = nullptr;
+
+int group_kind(cudaError_t (*launch)(const Params &, const Plan &, WsHeader *, cudaStream_t)) {
+  if (launch == launch_gae) return kGroupGae;
+  if (launch == launch_lambda_returns) return kGroupLambdaReturns;
+  if (launch == launch_discounted_returns) return kGroupDiscountedReturns;
+  if (launch == launch_vtrace) return kGroupVTrace;
+  if (launch == launch_retrace) return kGroupRetrace;
+  if (launch == launch_eligibility_traces) return kGroupEligibilityTraces;
+  if (launch == launch_episodic_prefix_sum) return kGroupEpisodicPrefixSum;
+  if (launch == launch_gae_and_returns) return kGroupGaeAndReturns;
+  return -1;
+}
+
 int sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 152;
@@ -91,15 +130,6 @@ size_t ws_bytes_tm(int64_t N, int64_t T) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-struct Buf {
-  const void *p;
-  size_t bytes;
-};
-bool overlaps(const Buf &a, const Buf &b) {
-  if (!a.p || !b.p) return false;
-  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
-  return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
-}
 
 // Shared tail of every entry point.
 // `opt`: the estimator's optional inputs are present (the truncation pair,
@@ -133,6 +163,22 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
       if (overlaps(ob, Buf{outs[o2], plane})) return RLCS_ERR_INVALID_ARG;
   }
   p.vec = vec ? 1 : 0;
+
+  if (t_group != nullptr) {  // record a grouped call instead of launching it
+    const int kind = group_kind(launch);
+    if (kind < 0 || time_major || t_time_major || T > kRowMaxT || esize != nullptr)
+      return RLCS_ERR_INVALID_ARG;
+    if (t_group->n >= kMaxGroup) return RLCS_ERR_INVALID_ARG;
+    GroupEntry &g = t_group->e[t_group->n++];
+    g.p = p;
+    g.kind = kind;
+    g.S = T <= 128 ? 1 : (T <= 256 ? 2 : 4);
+    g.trunc = opt;
+    for (int k = 0; k < kNumSlots; ++k) g.reads[k] = Buf{p.in[k], plane};
+    g.reads[kNumSlots] = Buf{p.boot, (size_t)N * 4u};
+    for (int o = 0; o < 2; ++o) g.writes[o] = Buf{o < n_outs ? outs[o] : nullptr, plane};
+    return RLCS_OK;
+  }
 
   Plan plan;
   const rlcs_status st = plan_call(N, T, opt, plan, time_major || t_time_major);
@@ -527,6 +573,118 @@ rlcs_status rlcs_affine_scan_tm(const float *a, const float *b, const float *res
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Grouped calls on short rows: one launch per (strips, optional inputs) class.
+// ---------------------------------------------------------------------------
+namespace rlcs {
+namespace {
+
+// Pass one call through its namesake entry point (validation and recording).
+rlcs_status group_one(const rlcs_call &c, rlcs_stream_t stream) {
+  switch (c.estimator) {
+    case RLCS_EST_GAE:
+      return rlcs_gae(static_cast<const float *>(c.rewards), c.values, c.terminateds,
+                      c.truncateds, c.next_values, c.bootstrap_value,
+                      static_cast<float *>(c.out), c.N, c.T, c.gamma, c.lambda, nullptr, 0,
+                      stream);
+    case RLCS_EST_LAMBDA_RETURNS:
+      return rlcs_lambda_returns(static_cast<const float *>(c.rewards), c.values,
+                                 c.terminateds, c.truncateds, c.next_values, c.bootstrap_value,
+                                 static_cast<float *>(c.out), c.N, c.T, c.gamma, c.lambda,
+                                 nullptr, 0, stream);
+    case RLCS_EST_DISCOUNTED_RETURNS:
+      return rlcs_discounted_returns(static_cast<const float *>(c.rewards), c.terminateds,
+                                     c.truncateds, c.next_values, c.bootstrap_value,
+                                     static_cast<float *>(c.out), c.N, c.T, c.gamma, nullptr, 0,
+                                     stream);
+    case RLCS_EST_VTRACE:
+      return rlcs_vtrace(static_cast<const float *>(c.rewards), c.values, c.log_rhos,
+                         c.terminateds, c.truncateds, c.next_values, c.bootstrap_value,
+                         static_cast<float *>(c.out), c.out2, c.N, c.T, c.gamma, c.lambda,
+                         c.rho_bar, c.c_bar, nullptr, 0, stream);
+    case RLCS_EST_RETRACE:
+      return rlcs_retrace(static_cast<const float *>(c.rewards), c.values, c.q_values,
+                          c.log_rhos, c.terminateds, c.truncateds, c.next_values,
+                          c.bootstrap_value, static_cast<float *>(c.out), c.N, c.T, c.gamma,
+                          c.lambda, c.c_bar, nullptr, 0, stream);
+    case RLCS_EST_ELIGIBILITY_TRACES:
+      return rlcs_eligibility_traces(static_cast<const float *>(c.rewards), c.terminateds,
+                                     static_cast<float *>(c.out), c.N, c.T, c.gamma, c.lambda,
+                                     nullptr, 0, stream);
+    case RLCS_EST_EPISODIC_PREFIX_SUM:
+      return rlcs_episodic_prefix_sum(static_cast<const int32_t *>(c.rewards), c.terminateds,
+                                      static_cast<int32_t *>(c.out), c.N, c.T, nullptr, 0,
+                                      stream);
+    case RLCS_EST_GAE_AND_RETURNS:
+      return rlcs_gae_and_returns(static_cast<const float *>(c.rewards), c.values,
+                                  c.terminateds, c.truncateds, c.next_values, c.bootstrap_value,
+                                  static_cast<float *>(c.out), c.out2, c.N, c.T, c.gamma,
+                                  c.lambda, nullptr, 0, stream);
+  }
+  return RLCS_ERR_INVALID_ARG;
+}
+
+struct GroupScope {
+  explicit GroupScope(GroupCollect *g) { t_group = g; }
+  ~GroupScope() { t_group = nullptr; }
+};
+
+}  // namespace
+}  // namespace rlcs
+
+extern "C" rlcs_status rlcs_run_group(const rlcs_call *calls, int n_calls, rlcs_stream_t stream) {
+  if (n_calls < 0 || n_calls > RLCS_MAX_GROUP || (n_calls > 0 && calls == nullptr))
+    return RLCS_ERR_INVALID_ARG;
+  if (n_calls == 0) return RLCS_OK;
+  GroupCollect col;
+  {
+    GroupScope scope(&col);
+    for (int i = 0; i < n_calls; ++i) {
+      if (calls[i].reserved != 0) return RLCS_ERR_INVALID_ARG;
+      const rlcs_status st = group_one(calls[i], stream);
+      if (st != RLCS_OK) return st;
+    }
+  }
+  // calls run concurrently: no call may write what another reads or writes
+  for (int i = 0; i < col.n; ++i)
+    for (int w = 0; w < 2; ++w) {
+      const Buf &out = col.e[i].writes[w];
+      if (!out.p) continue;
+      for (int j = 0; j < col.n; ++j) {
+        if (j == i) continue;
+        for (const Buf &b : col.e[j].reads)
+          if (overlaps(out, b)) return RLCS_ERR_INVALID_ARG;
+        for (const Buf &b : col.e[j].writes)
+          if (overlaps(out, b)) return RLCS_ERR_INVALID_ARG;
+      }
+    }
+  // one launch per class, calls in their given order within it
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  bool done[kMaxGroup] = {};
+  for (int i = 0; i < col.n; ++i) {
+    if (done[i]) continue;
+    GroupParams gp;
+    std::memset(&gp, 0, sizeof(gp));
+    int64_t blocks = 0;
+    for (int j = i; j < col.n; ++j) {
+      if (done[j] || col.e[j].S != col.e[i].S || col.e[j].trunc != col.e[i].trunc) continue;
+      done[j] = true;
+      gp.kind[gp.n] = col.e[j].kind;
+      gp.p[gp.n] = col.e[j].p;
+      gp.first_block[gp.n] = blocks;
+      blocks += ceil_div(col.e[j].p.N, kRowWarps);
+      ++gp.n;
+    }
+    gp.first_block[gp.n] = blocks;
+    if (blocks >= (int64_t)INT32_MAX) return RLCS_ERR_INVALID_ARG;
+    if (launch_group(gp, col.e[i].S, col.e[i].trunc, s) != cudaSuccess) {
+      cudaGetLastError();
+      return RLCS_ERR_CUDA;
+    }
+  }
+  return RLCS_OK;
+}
 
 // ---------------------------------------------------------------------------
 // GAE for callers that cannot allocate device memory.

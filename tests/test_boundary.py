@@ -191,3 +191,72 @@ def test_compact_overlap_uses_element_sizes(lib):
     inside = ctypes.c_void_p(d.value + N * T - 16)  # overlapping the masks
     assert lib.rlcs_gae_compact(r, v, d, None, None, None, inside, N, T, 0.99, 0.95, None, 0,
                                 None) == INVALID
+
+
+def test_rlcs_call_layout_matches_the_header(tmp_path):
+    # the ctypes mirror of rlcs_call has the C struct's size and offsets
+    import ctypes as ct
+    import subprocess
+    from linear_recurrence_scan_affine_gb300.binding import RlcsCall
+    fields = [f for f, _ in RlcsCall._fields_]
+    cname = {"lambda_": "lambda"}
+    prog = tmp_path / "layout.c"
+    prog.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "rlcs.h"\nint main(void) {\n'
+                    '  printf("%zu\\n", sizeof(rlcs_call));\n'
+                    + "".join('  printf("%%zu\\n", offsetof(rlcs_call, %s));\n' % cname.get(f, f)
+                              for f in fields)
+                    + "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), "-I",
+                    "/usr/local/cuda/include", str(prog), "-o", str(exe)], check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                          check=True).stdout.split()]
+    assert got[0] == ct.sizeof(RlcsCall)
+    assert got[1:] == [getattr(RlcsCall, f).offset for f in fields]
+
+
+def _call(est, N=4, T=8, **ptrs):
+    from linear_recurrence_scan_affine_gb300.binding import RlcsCall, GROUP_ESTIMATORS
+    c = RlcsCall()
+    c.estimator = GROUP_ESTIMATORS[est] if isinstance(est, str) else est
+    for k, v in ptrs.items():
+        setattr(c, k, v.value if isinstance(v, ctypes.c_void_p) else v)
+    c.N, c.T, c.gamma, c.lambda_, c.rho_bar, c.c_bar = N, T, 0.99, 0.95, 1.0, 1.0
+    return c
+
+
+def _group(lib, calls):
+    from linear_recurrence_scan_affine_gb300.binding import RlcsCall
+    arr = (RlcsCall * max(1, len(calls)))(*calls)
+    return lib.rlcs_run_group(ctypes.cast(arr, ctypes.c_void_p), len(calls), None)
+
+
+def test_group_validation(lib):
+    # every case is rejected before anything is launched
+    a = [fake(i) for i in range(12)]
+    gae = dict(rewards=a[0], values=a[1], terminateds=a[2], out=a[3])
+    assert lib.rlcs_run_group(None, 0, None) == OK            # nothing to do
+    assert lib.rlcs_run_group(None, 2, None) == INVALID
+    assert lib.rlcs_run_group(None, -1, None) == INVALID
+    assert _group(lib, [_call("gae", **gae)] * 17) == INVALID  # more than RLCS_MAX_GROUP
+    assert _group(lib, [_call("gae", T=513, **gae)]) == INVALID  # long rows are not grouped
+    assert _group(lib, [_call(99, **gae)]) == INVALID           # unknown estimator
+    bad = _call("gae", **gae)
+    bad.reserved = 1
+    assert _group(lib, [bad]) == INVALID
+    # the namesake's own checks: a missing input, half a truncation pair, aliasing
+    assert _group(lib, [_call("gae", rewards=a[0], terminateds=a[2], out=a[3])]) == INVALID
+    assert _group(lib, [_call("gae", truncateds=a[4], **gae)]) == INVALID
+    assert _group(lib, [_call("gae", rewards=a[0], values=a[1], terminateds=a[2],
+                              out=a[1])]) == INVALID
+    assert _group(lib, [_call("gae_and_returns", **gae)]) == INVALID  # returns missing
+    # one call writing what another reads or writes (they run concurrently)
+    other = dict(rewards=a[5], values=a[6], terminateds=a[7], out=a[8])
+    assert _group(lib, [_call("gae", **gae),
+                        _call("lambda_returns", **dict(other, out=a[0]))]) == INVALID
+    assert _group(lib, [_call("gae", **gae),
+                        _call("lambda_returns", **dict(other, out=a[3]))]) == INVALID
+    inner = ctypes.c_void_p(a[2].value + 64)
+    assert _group(lib, [_call("gae", **gae),
+                        _call("discounted_returns", rewards=a[5], terminateds=a[7],
+                              out=inner)]) == INVALID
