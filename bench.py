@@ -564,7 +564,10 @@ def run_ours(args):
                                 seconds=0.08)
                 r_["frac_of_measured_hbm"] = r_["gbs"] / peak
                 res[est] = r_
-            long_t[name] = res
+            step_l = time_step(torch, rl, wl.estimators, src_l, dev, stream, prm_l, l2, wl.N,
+                               wl.T)
+            step_l["frac_of_measured_hbm"] = step_l["gbs"] / peak
+            long_t[name] = {"step": step_l, "alone": res}
             del src_l
         rl.check_all_workspaces()
 
@@ -666,6 +669,69 @@ def time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T, seconds=0.15):
             "gbs": bytes_per_launch(est, N, T) / sec / 1e9,
             "bytes_per_env_step": bytes_per_env_step(est), "rotating_sets": nsets,
             "footprint_over_l2": nsets * set_bytes / l2}
+
+
+def time_step(torch, rl, ests, src, dev, stream, prm, l2, N, T, seconds=0.15):
+    """The estimators of one step over rotating buffer sets that span >= 3x
+    the L2, in two schedules: each estimator on its own stream (as the
+    headline step) and all on one stream. Returns both and, as the step, the
+    faster: time per step and the step's algorithmic GB/s."""
+    step_bytes = sum(bytes_per_launch(e, N, T) for e in ests)
+    nsets = int(min(64, max(2, -(-3 * l2 // step_bytes))))
+    sets = []
+    for _ in range(nsets):
+        st = {}
+        for est in ests:
+            ins, outs = ESTIMATORS[est]
+            e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + ("bootstrap_value",)}
+            odt = torch.int32 if est == "episodic_prefix_sum" else torch.float32
+            for o in outs:
+                e[o] = torch.empty(e[ins[0]].shape, dtype=odt, device=dev)
+            st[est] = e
+        sets.append(st)
+    side = {est: torch.cuda.Stream(dev) for est in ests}
+    for est in ests:  # warm-up: every side stream's workspace exists before capture
+        side[est].wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side[est]):
+            for st in sets:
+                launch(rl, est, st[est], prm)
+    torch.cuda.synchronize()
+
+    def concurrent():
+        for est in ests:
+            side[est].wait_stream(stream)
+            with torch.cuda.stream(side[est]):
+                for st in sets:
+                    launch(rl, est, st[est], prm)
+        for est in ests:
+            stream.wait_stream(side[est])
+
+    def serial():
+        for st in sets:
+            for est in ests:
+                launch(rl, est, st[est], prm)
+
+    with torch.cuda.stream(stream):  # the one-stream schedule's workspace
+        serial()
+    torch.cuda.synchronize()
+    us = {}
+    for name, fn in (("streams", concurrent), ("one_stream", serial)):
+        g = capture(torch, stream, fn)
+        with torch.cuda.stream(stream):
+            g.replay()
+        once = time_graph(torch, stream, g, 1)
+        reps = max(3, int(seconds / max(1e-6, once)))
+        us[name] = time_graph(torch, stream, g, reps) / (reps * nsets) * 1e6
+        del g
+    del sets
+    torch.cuda.synchronize()
+    best = min(us, key=us.get)
+    sec = us[best] * 1e-6
+    return {"us_per_step": us[best], "schedule": best,
+            "us_per_step_by_schedule": us, "env_steps_per_s": N * T / sec,
+            "gbs": step_bytes / sec / 1e9, "bytes_per_step": step_bytes,
+            "estimators": list(ests), "rotating_sets": nsets,
+            "footprint_over_l2": nsets * step_bytes / l2}
 
 
 def time_diag(torch, rl, n_arrays, dev, stream, l2, N, T, empty, seconds=0.1):

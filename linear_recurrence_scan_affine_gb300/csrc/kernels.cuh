@@ -73,6 +73,13 @@ struct ChunkShape {
 // ---------------------------------------------------------------------------
 // Small helpers
 // ---------------------------------------------------------------------------
+// q = a / b for 0 <= a, 0 < b: in 32 bits when both fit (the usual case),
+// a fraction of the cost of the 64-bit routine.
+__device__ __forceinline__ int64_t div_nonneg(int64_t a, int64_t b) {
+  if ((((uint64_t)a | (uint64_t)b) >> 32) == 0) return (int64_t)((uint32_t)a / (uint32_t)b);
+  return a / b;
+}
+
 __device__ __forceinline__ float4 f4zero() { return make_float4(0.f, 0.f, 0.f, 0.f); }
 
 __device__ __forceinline__ float f4get(const float4 &v, int i) {
@@ -704,7 +711,7 @@ __global__ void __launch_bounds__(kChunkThreads) block_chunk_kernel(Params p, Ch
   // block order closely; exact when Q == 1), issued before the dependency
   // wait so it overlaps the previous grid. A wrong guess only costs traffic.
   if (vec && tid == 0) {
-    const int64_t g = blockIdx.x, grow = g / Q, gk = g - grow * Q;
+    const int64_t g = blockIdx.x, grow = div_nonneg(g, Q), gk = g - grow * Q;
     const int64_t gq = E::kBackward ? (Q - 1 - gk) : gk;
     const int64_t gt0 = gq * C;
     const int64_t glen = (T - gt0 < C) ? (T - gt0) : C;
@@ -728,7 +735,7 @@ __global__ void __launch_bounds__(kChunkThreads) block_chunk_kernel(Params p, Ch
     s_ticket = ticket;
     s_ok = ok;
     if (ok && vec) {
-      const int64_t row = ticket / Q, kk = ticket - row * Q;
+      const int64_t row = div_nonneg(ticket, Q), kk = ticket - row * Q;
       const int64_t q = E::kBackward ? (Q - 1 - kk) : kk;
       const int64_t t0 = q * C;
       const int64_t len = (T - t0 < C) ? (T - t0) : C;
@@ -752,7 +759,7 @@ __global__ void __launch_bounds__(kChunkThreads) block_chunk_kernel(Params p, Ch
   if (!s_ok) return;  // uniform: a corrupted workspace handed out a bad ticket
 
   const int64_t ticket = s_ticket;
-  const int64_t row = ticket / Q, kk = ticket - row * Q;
+  const int64_t row = div_nonneg(ticket, Q), kk = ticket - row * Q;
   const int64_t q = E::kBackward ? (Q - 1 - kk) : kk;
   const int64_t t0 = q * C;
   const int64_t base = row * T;

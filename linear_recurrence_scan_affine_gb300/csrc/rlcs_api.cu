@@ -185,7 +185,7 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
   if (st != RLCS_OK) return st;
   WsHeader *wsh = nullptr;
   if (plan.shape != RLCS_SHAPE_WARP_ROW) {
-    if (N * plan.Q >= (int64_t)UINT32_MAX) return RLCS_ERR_INVALID_ARG;
+    if (N * plan.Q >= (int64_t)INT32_MAX) return RLCS_ERR_INVALID_ARG;  // grid x limit
     if (plan.Q > 1) {
       const size_t need =
           plan.shape == kShapeTimeMajor ? ws_bytes_tm(N, T) : ws_bytes_for(N, plan.Q);
