@@ -75,8 +75,9 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
     }
   }
   if (plan.shape == RLCS_SHAPE_WARP_ROW) {
-    const dim3 grid((unsigned)((p.N + kRowWarps - 1) / kRowWarps));
-    return launch_ex(warp_row_kernel<E, TRUNC, S>, grid, dim3(kRowWarps * 32), 0, s, plan.pdl, p);
+    constexpr int R = row_warps<E, TRUNC>();
+    const dim3 grid((unsigned)((p.N + R - 1) / R));
+    return launch_ex(warp_row_kernel<E, TRUNC, S>, grid, dim3(R * 32), 0, s, plan.pdl, p);
   }
   if constexpr ((E::kBF16Slots | E::kU8Slots) != 0u) {
     // compact inputs are never staged through shared memory: the tile shape
