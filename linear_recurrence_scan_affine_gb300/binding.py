@@ -120,7 +120,10 @@ def workspace_for(N, T, device, stream=None, need=None):
     with _ws_lock:
         ws = _ws_cache.get(key)
         if ws is None or ws.numel() < need:
-            ws = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=device)
+            # zeroed on the stream that will use it, so the fill is ordered
+            # before the first call (and the memory belongs to that stream)
+            with torch.cuda.stream(s):
+                ws = torch.zeros(max(need, 1 << 16), dtype=torch.uint8, device=device)
             _ws_cache[key] = ws
     return ws, ws.numel()
 

@@ -212,6 +212,20 @@ def test_side_stream_gets_its_own_workspace(rl, dev):
         compare("retrace", outs[s], want, TOL)
 
 
+def test_explicit_stream_argument_with_a_fresh_workspace(rl, dev):
+    # stream= names a stream other than the current one; its first call
+    # allocates and zeroes a workspace, which must be ordered on that stream
+    src = rollout(4, 30000, 98, p_term=0.001)
+    g = to_dev(src, dev)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    out = rl.rlcs_retrace(g["rewards"], g["values"], g["q_values"], g["log_rhos"],
+                          g["terminateds"], DEFAULT["gamma"], DEFAULT["lambda_"],
+                          DEFAULT["c_bar"], g["bootstrap_value"], stream=s)
+    s.synchronize()
+    compare("retrace", {"out": out}, run_oracle("retrace", src, DEFAULT, False), TOL)
+
+
 def test_cuda_graph_capture_and_replay(rl, dev):
     src = rollout(16, 6000, 96, p_term=0.002, p_trunc=0.001)
     g = to_dev(src, dev)
