@@ -673,9 +673,10 @@ def time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T, seconds=0.15):
 
 def time_step(torch, rl, ests, src, dev, stream, prm, l2, N, T, seconds=0.15):
     """The estimators of one step over rotating buffer sets that span >= 3x
-    the L2, in two schedules: each estimator on its own stream (as the
-    headline step) and all on one stream. Returns both and, as the step, the
-    faster: time per step and the step's algorithmic GB/s."""
+    the L2, in three schedules: each estimator on its own stream (as the
+    headline step), all on one stream, and one rlcs_run_group call. Returns
+    all three and, as the step, the fastest: time per step and the step's
+    algorithmic GB/s."""
     step_bytes = sum(bytes_per_launch(e, N, T) for e in ests)
     nsets = int(min(64, max(2, -(-3 * l2 // step_bytes))))
     sets = []
@@ -711,11 +712,18 @@ def time_step(torch, rl, ests, src, dev, stream, prm, l2, N, T, seconds=0.15):
             for est in ests:
                 launch(rl, est, st[est], prm)
 
-    with torch.cuda.stream(stream):  # the one-stream schedule's workspace
+    group_calls = [[(est, group_kwargs(est, st[est], prm)) for est in ests] for st in sets]
+
+    def grouped():
+        for calls in group_calls:
+            rl.rlcs_run_group(calls)
+
+    with torch.cuda.stream(stream):  # the one-stream schedules' workspaces
         serial()
+        grouped()
     torch.cuda.synchronize()
     us = {}
-    for name, fn in (("streams", concurrent), ("one_stream", serial)):
+    for name, fn in (("streams", concurrent), ("one_stream", serial), ("grouped", grouped)):
         g = capture(torch, stream, fn)
         with torch.cuda.stream(stream):
             g.replay()

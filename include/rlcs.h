@@ -302,13 +302,14 @@ rlcs_status rlcs_affine_scan_tm(const float *a, const float *b, const float *res
                                 const float *x_init, float *x, int64_t N, int64_t T, int reverse,
                                 void *workspace, size_t workspace_bytes, rlcs_stream_t stream);
 
-/* Grouped calls. Several estimator calls on short rows (T <= 512 each) run
- * in one kernel launch instead of one launch each: every call computes
+/* Grouped calls. Up to RLCS_MAX_GROUP estimator calls run in as few kernel
+ * launches as possible instead of one launch each: every call computes
  * exactly what its namesake entry point computes (same definitions, same
  * validation), on its own arrays and sizes. A launch has a fixed cost of a
  * few microseconds whatever its size, which dominates calls of a few MB
- * (4096 x 128 rows); one launch for the group pays it once. The paper has no
- * counterpart: it is a launch-level convenience for the seven estimators.
+ * (4096 x 128 rows), and each long-row launch ends in a partly idle wave;
+ * one grid for the group pays both once. The paper has no counterpart: it is
+ * a launch-level convenience for the seven estimators.
  *
  * rlcs_call: one call. `estimator` selects the namesake; the pointer fields
  * are that entry point's arguments (rewards holds x for the two forward
@@ -317,13 +318,23 @@ rlcs_status rlcs_affine_scan_tm(const float *a, const float *b, const float *res
  * fused call's returns). Fields the estimator does not take are ignored;
  * `reserved` must be 0. All pointers are device memory owned by the caller.
  *
- * Calls are grouped by strips per row (T <= 128, <= 256, <= 512) and by
- * whether their truncation inputs are present; each class is one launch, in
- * the order of first appearance, on `stream`. Errors: RLCS_ERR_INVALID_ARG
- * for more than RLCS_MAX_GROUP calls, a call with T > 512, any argument its
- * namesake would reject, or an output of one call overlapping any array of
- * another call (the calls run concurrently); nothing is launched then.
- * RLCS_ERR_CUDA if a launch fails. No workspace is used. */
+ * Classes and launches: short rows (T <= 512) are grouped by strips per row
+ * (T <= 128, <= 256, <= 512) and by whether their truncation inputs are
+ * present; long rows (T > 512) by tile length (chosen from the rows of all
+ * the group's long calls together) and the same flag. Each class is one
+ * launch, in the order of first appearance, on `stream`.
+ *
+ * Workspace: rlcs_group_workspace_bytes(calls, n) bytes (0 when no long call
+ * spans several tiles; NULL is then allowed), prepared like the other
+ * workspaces (zeroed once, one per stream, never shared by calls that may
+ * overlap). Long calls of one group share it.
+ *
+ * Errors: RLCS_ERR_INVALID_ARG for more than RLCS_MAX_GROUP calls, any
+ * argument a call's namesake would reject, an output of one call overlapping
+ * any array of another call (the calls run concurrently), or a workspace
+ * overlapping any array; RLCS_ERR_WORKSPACE for a missing, short or
+ * misaligned workspace; nothing is launched then. RLCS_ERR_CUDA if a launch
+ * fails. */
 #define RLCS_MAX_GROUP 16
 typedef enum {
   RLCS_EST_GAE = 0,
@@ -353,7 +364,9 @@ typedef struct {
   float gamma, lambda, rho_bar, c_bar;
 } rlcs_call;
 
-rlcs_status rlcs_run_group(const rlcs_call *calls, int n_calls, rlcs_stream_t stream);
+size_t rlcs_group_workspace_bytes(const rlcs_call *calls, int n_calls);
+rlcs_status rlcs_run_group(const rlcs_call *calls, int n_calls, void *workspace,
+                           size_t workspace_bytes, rlcs_stream_t stream);
 
 /* GAE for callers that cannot allocate device memory.
  * The paper has no counterpart: this is a library convenience. Some callers

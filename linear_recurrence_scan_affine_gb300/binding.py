@@ -59,7 +59,8 @@ def _load():
         "rlcs_eligibility_traces_tm": ([P] * 3 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
         "rlcs_episodic_prefix_sum_tm": ([P] * 3 + [I64, I64, P, SZ, P], ctypes.c_int),
         "rlcs_gae_and_returns_tm": ([P] * 8 + [I64, I64, F, F, P, SZ, P], ctypes.c_int),
-        "rlcs_run_group": ([P, ctypes.c_int, P], ctypes.c_int),
+        "rlcs_run_group": ([P, ctypes.c_int, P, SZ, P], ctypes.c_int),
+        "rlcs_group_workspace_bytes": ([P, ctypes.c_int], SZ),
         "rlcs_affine_scan_tm": ([P] * 5 + [I64, I64, ctypes.c_int, P, SZ, P], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -79,7 +80,8 @@ EXPORTED = ("rlcs_workspace_bytes", "rlcs_workspace_init", "rlcs_check_status",
             "rlcs_lambda_returns_tm",
             "rlcs_discounted_returns_tm", "rlcs_vtrace_tm", "rlcs_retrace_tm",
             "rlcs_eligibility_traces_tm", "rlcs_episodic_prefix_sum_tm",
-            "rlcs_gae_and_returns_tm", "rlcs_affine_scan_tm", "rlcs_run_group")
+            "rlcs_gae_and_returns_tm", "rlcs_affine_scan_tm", "rlcs_run_group",
+            "rlcs_group_workspace_bytes")
 
 
 def lib():
@@ -601,13 +603,13 @@ def _group_call(est, kw):
 
 
 def rlcs_run_group(calls, stream=None):
-    """Run up to MAX_GROUP estimator calls on short rows (T <= 512) in one
-    launch per class (rows up to 128 / 256 / 512 steps, truncation inputs
-    present or not). `calls` is a list of (estimator, kwargs) pairs: the
-    estimator is a key of GROUP_ESTIMATORS and kwargs are what its namesake
-    wrapper takes (x and dones for the two forward estimators). Returns the
-    namesakes' results, in order. No output may overlap another call's
-    arrays: the calls run concurrently."""
+    """Run up to MAX_GROUP estimator calls in one launch per class (short
+    rows by 128 / 256 / 512 steps, long rows by tile length; truncation
+    inputs present or not). `calls` is a list of (estimator, kwargs) pairs:
+    the estimator is a key of GROUP_ESTIMATORS and kwargs are what its
+    namesake wrapper takes (x and dones for the two forward estimators).
+    Returns the namesakes' results, in order. No output may overlap another
+    call's arrays: the calls run concurrently."""
     arr = (RlcsCall * max(1, len(calls)))()
     keep, results = [], []
     for i, (est, kw) in enumerate(calls):
@@ -615,7 +617,12 @@ def rlcs_run_group(calls, stream=None):
         arr[i] = c
         keep += k
         results.append(res)
-    _check(_lib.rlcs_run_group(ctypes.cast(arr, ctypes.c_void_p), len(calls), _stream(stream)),
+    ptr = ctypes.cast(arr, ctypes.c_void_p)
+    need = _lib.rlcs_group_workspace_bytes(ptr, len(calls)) if calls else 0
+    ws, wsb = None, 0
+    if need:
+        ws, wsb = workspace_for(0, 0, keep[0].device, stream, need=need)
+    _check(_lib.rlcs_run_group(ptr, len(calls), _ptr(ws), wsb, _stream(stream)),
            "rlcs_run_group")
     return results
 

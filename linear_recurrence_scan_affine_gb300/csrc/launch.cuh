@@ -82,12 +82,12 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
   if constexpr ((E::kBF16Slots | E::kU8Slots) != 0u) {
     // compact inputs are never staged through shared memory: the tile shape
     // serves every long-row plan
-    TileShape ts{plan.Q > 1 ? ws : nullptr, plan.Q, p.N * plan.Q};
+    TileShape ts{plan.Q > 1 ? ws : nullptr, plan.Q, p.N * plan.Q, 0};
     return launch_ex(block_tile_kernel<E, TRUNC, S>, dim3((unsigned)(p.N * plan.Q)),
                      dim3(kChunkThreads), 0, s, plan.pdl, p, ts);
   } else {
     if (plan.shape == RLCS_SHAPE_BLOCK_TILE) {
-      TileShape ts{plan.Q > 1 ? ws : nullptr, plan.Q, p.N * plan.Q};
+      TileShape ts{plan.Q > 1 ? ws : nullptr, plan.Q, p.N * plan.Q, 0};
       return launch_ex(block_tile_kernel<E, TRUNC, S>, dim3((unsigned)(p.N * plan.Q)),
                        dim3(kChunkThreads), 0, s, plan.pdl, p, ts);
     }
@@ -133,5 +133,7 @@ cudaError_t launch_affine_forward(const Params &, const Plan &, WsHeader *, cuda
 cudaError_t launch_affine_backward(const Params &, const Plan &, WsHeader *, cudaStream_t);
 // One launch of grouped warp-row calls sharing S and the optional-input flag.
 cudaError_t launch_group(const GroupParams &gp, int S, bool trunc, cudaStream_t s);
+// One launch of grouped long-row calls (block tiles) sharing S and the flag.
+cudaError_t launch_group_tiles(const GroupTileParams &gp, int S, bool trunc, cudaStream_t s);
 
 }  // namespace rlcs

@@ -43,8 +43,9 @@ bool overlaps(const Buf &a, const Buf &b) {
 struct GroupEntry {
   Params p;
   int kind;
-  int S;
+  int S;         // strips per warp (short rows) or tile length / 1024 (long rows)
   bool trunc;
+  bool long_row;  // T > kRowMaxT: block tiles, planned with the whole group
   Buf reads[kNumSlots + 1];  // input planes and the bootstrap array
   Buf writes[2];
 };
@@ -89,6 +90,28 @@ int64_t pick_chunk(int64_t N, int64_t T) {
   if (T <= 1024) return 1024;
   if (N * ceil_div(T, 4096) <= 2 * (int64_t)sm_count()) return 4096;
   return 2048;
+}
+
+// Tile length of a long-row call in a group: the single-call rule applied
+// to the rows of all the group's long calls together (they share the GPU in
+// one grid), unless a block-tile override names one.
+int64_t group_chunk(int64_t rows, int64_t T) {
+  const int ov = g_override_shape.load(std::memory_order_relaxed);
+  const int64_t forced = g_override_chunk.load(std::memory_order_relaxed);
+  if (ov == RLCS_SHAPE_BLOCK_TILE && forced != 0) return forced;
+  return pick_chunk(rows, T);
+}
+
+// Look-back records a group's long calls need: sum over calls whose rows
+// span several tiles of N * tiles per row. `Ns`, `Ts`: the long calls only.
+int64_t group_records(const int64_t *Ns, const int64_t *Ts, int n) {
+  int64_t rows = 0, recs = 0;
+  for (int i = 0; i < n; ++i) rows += Ns[i];
+  for (int i = 0; i < n; ++i) {
+    const int64_t Q = ceil_div(Ts[i], group_chunk(rows, Ts[i]));
+    if (Q > 1) recs += Ns[i] * Q;
+  }
+  return recs;
 }
 
 // Choose the launch shape for an [N, T] call.
@@ -166,13 +189,13 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
 
   if (t_group != nullptr) {  // record a grouped call instead of launching it
     const int kind = group_kind(launch);
-    if (kind < 0 || time_major || t_time_major || T > kRowMaxT || esize != nullptr)
-      return RLCS_ERR_INVALID_ARG;
+    if (kind < 0 || time_major || t_time_major || esize != nullptr) return RLCS_ERR_INVALID_ARG;
     if (t_group->n >= kMaxGroup) return RLCS_ERR_INVALID_ARG;
     GroupEntry &g = t_group->e[t_group->n++];
     g.p = p;
     g.kind = kind;
-    g.S = T <= 128 ? 1 : (T <= 256 ? 2 : 4);
+    g.long_row = T > kRowMaxT;
+    g.S = g.long_row ? 0 : (T <= 128 ? 1 : (T <= 256 ? 2 : 4));  // long rows: set later
     g.trunc = opt;
     for (int k = 0; k < kNumSlots; ++k) g.reads[k] = Buf{p.in[k], plane};
     g.reads[kNumSlots] = Buf{p.boot, (size_t)N * 4u};
@@ -633,7 +656,22 @@ struct GroupScope {
 }  // namespace
 }  // namespace rlcs
 
-extern "C" rlcs_status rlcs_run_group(const rlcs_call *calls, int n_calls, rlcs_stream_t stream) {
+extern "C" size_t rlcs_group_workspace_bytes(const rlcs_call *calls, int n_calls) {
+  if (calls == nullptr || n_calls <= 0 || n_calls > RLCS_MAX_GROUP) return 0;
+  int64_t Ns[kMaxGroup], Ts[kMaxGroup];
+  int n = 0;
+  for (int i = 0; i < n_calls; ++i)
+    if (calls[i].N > 0 && calls[i].T > kRowMaxT) {
+      Ns[n] = calls[i].N;
+      Ts[n] = calls[i].T;
+      ++n;
+    }
+  const int64_t recs = group_records(Ns, Ts, n);
+  return recs > 0 ? ws_bytes_for(recs, 1) : 0;
+}
+
+extern "C" rlcs_status rlcs_run_group(const rlcs_call *calls, int n_calls, void *workspace,
+                                      size_t workspace_bytes, rlcs_stream_t stream) {
   if (n_calls < 0 || n_calls > RLCS_MAX_GROUP || (n_calls > 0 && calls == nullptr))
     return RLCS_ERR_INVALID_ARG;
   if (n_calls == 0) return RLCS_OK;
@@ -659,26 +697,84 @@ extern "C" rlcs_status rlcs_run_group(const rlcs_call *calls, int n_calls, rlcs_
           if (overlaps(out, b)) return RLCS_ERR_INVALID_ARG;
       }
     }
+  // long rows: tile lengths from the whole group, then the workspace
+  int64_t long_rows = 0;
+  for (int i = 0; i < col.n; ++i)
+    if (col.e[i].long_row) long_rows += col.e[i].p.N;
+  int64_t Q[kMaxGroup] = {}, recs = 0;
+  for (int i = 0; i < col.n; ++i) {
+    GroupEntry &g = col.e[i];
+    if (!g.long_row) continue;
+    const int64_t chunk = group_chunk(long_rows, g.p.T);
+    g.S = (int)(chunk / kMinChunk);
+    Q[i] = ceil_div(g.p.T, chunk);
+    if (Q[i] > 1) recs += g.p.N * Q[i];
+  }
+  WsHeader *wsh = nullptr;
+  if (recs > 0) {
+    if (!workspace || workspace_bytes < ws_bytes_for(recs, 1) || !aligned16(workspace))
+      return RLCS_ERR_WORKSPACE;
+    const Buf wb{workspace, workspace_bytes};
+    for (int i = 0; i < col.n; ++i) {
+      for (const Buf &b : col.e[i].reads)
+        if (overlaps(wb, b)) return RLCS_ERR_INVALID_ARG;
+      for (const Buf &b : col.e[i].writes)
+        if (overlaps(wb, b)) return RLCS_ERR_INVALID_ARG;
+    }
+    wsh = static_cast<WsHeader *>(workspace);
+  }
   // one launch per class, calls in their given order within it
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   bool done[kMaxGroup] = {};
+  int64_t rec_off = 0;
   for (int i = 0; i < col.n; ++i) {
     if (done[i]) continue;
-    GroupParams gp;
-    std::memset(&gp, 0, sizeof(gp));
-    int64_t blocks = 0;
-    for (int j = i; j < col.n; ++j) {
-      if (done[j] || col.e[j].S != col.e[i].S || col.e[j].trunc != col.e[i].trunc) continue;
-      done[j] = true;
-      gp.kind[gp.n] = col.e[j].kind;
-      gp.p[gp.n] = col.e[j].p;
+    const GroupEntry &lead = col.e[i];
+    auto same_class = [&](const GroupEntry &g) {
+      return g.long_row == lead.long_row && g.S == lead.S && g.trunc == lead.trunc;
+    };
+    cudaError_t err;
+    if (!lead.long_row) {
+      GroupParams gp;
+      std::memset(&gp, 0, sizeof(gp));
+      int64_t blocks = 0;
+      for (int j = i; j < col.n; ++j) {
+        if (done[j] || !same_class(col.e[j])) continue;
+        done[j] = true;
+        gp.kind[gp.n] = col.e[j].kind;
+        gp.p[gp.n] = col.e[j].p;
+        gp.first_block[gp.n] = blocks;
+        blocks += ceil_div(col.e[j].p.N, kRowWarps);
+        ++gp.n;
+      }
       gp.first_block[gp.n] = blocks;
-      blocks += ceil_div(col.e[j].p.N, kRowWarps);
-      ++gp.n;
+      if (blocks >= (int64_t)INT32_MAX) return RLCS_ERR_INVALID_ARG;
+      err = launch_group(gp, lead.S, lead.trunc, s);
+    } else {
+      GroupTileParams gp;
+      std::memset(&gp, 0, sizeof(gp));
+      int64_t blocks = 0, chained = 0;
+      for (int j = i; j < col.n; ++j) {
+        if (done[j] || !same_class(col.e[j])) continue;
+        done[j] = true;
+        const int64_t tiles = col.e[j].p.N * Q[j];
+        gp.kind[gp.n] = col.e[j].kind;
+        gp.p[gp.n] = col.e[j].p;
+        gp.ts[gp.n] = TileShape{Q[j] > 1 ? wsh : nullptr, Q[j], 0, Q[j] > 1 ? rec_off : 0};
+        gp.first_block[gp.n] = blocks;
+        blocks += tiles;
+        if (Q[j] > 1) {
+          rec_off += tiles;
+          chained += tiles;
+        }
+        ++gp.n;
+      }
+      gp.first_block[gp.n] = blocks;
+      for (int c = 0; c < gp.n; ++c) gp.ts[c].total_tiles = chained;  // finish_launch count
+      if (blocks >= (int64_t)INT32_MAX) return RLCS_ERR_INVALID_ARG;
+      err = launch_group_tiles(gp, lead.S, lead.trunc, s);
     }
-    gp.first_block[gp.n] = blocks;
-    if (blocks >= (int64_t)INT32_MAX) return RLCS_ERR_INVALID_ARG;
-    if (launch_group(gp, col.e[i].S, col.e[i].trunc, s) != cudaSuccess) {
+    if (err != cudaSuccess) {
       cudaGetLastError();
       return RLCS_ERR_CUDA;
     }

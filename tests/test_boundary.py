@@ -225,21 +225,47 @@ def _call(est, N=4, T=8, **ptrs):
     return c
 
 
-def _group(lib, calls):
+def _group(lib, calls, ws=None, wsb=0):
     from linear_recurrence_scan_affine_gb300.binding import RlcsCall
     arr = (RlcsCall * max(1, len(calls)))(*calls)
-    return lib.rlcs_run_group(ctypes.cast(arr, ctypes.c_void_p), len(calls), None)
+    return lib.rlcs_run_group(ctypes.cast(arr, ctypes.c_void_p), len(calls), ws, wsb, None)
+
+
+def _group_ws(lib, calls):
+    from linear_recurrence_scan_affine_gb300.binding import RlcsCall
+    arr = (RlcsCall * max(1, len(calls)))(*calls)
+    return lib.rlcs_group_workspace_bytes(ctypes.cast(arr, ctypes.c_void_p), len(calls))
+
+
+def test_group_workspace_bytes(lib):
+    assert _group_ws(lib, []) == 0
+    a = [fake(i) for i in range(4)]
+    gae = dict(rewards=a[0], values=a[1], terminateds=a[2], out=a[3])
+    assert _group_ws(lib, [_call("gae", T=512, **gae)]) == 0       # short rows: none
+    assert _group_ws(lib, [_call("gae", T=1000, **gae)]) == 0      # one tile per row: none
+    # the tile length follows the group's rows: 4 rows alone take 4096-step
+    # tiles, 4 + 1000 rows 2048-step ones
+    one = _group_ws(lib, [_call("gae", N=4, T=16384, **gae)])
+    assert one == 64 + 32 * 4 * 4
+    two = _group_ws(lib, [_call("gae", N=4, T=16384, **gae),
+                          _call("gae", N=1000, T=600, **gae)])
+    assert two == 64 + 32 * 4 * 8
 
 
 def test_group_validation(lib):
     # every case is rejected before anything is launched
     a = [fake(i) for i in range(12)]
     gae = dict(rewards=a[0], values=a[1], terminateds=a[2], out=a[3])
-    assert lib.rlcs_run_group(None, 0, None) == OK            # nothing to do
-    assert lib.rlcs_run_group(None, 2, None) == INVALID
-    assert lib.rlcs_run_group(None, -1, None) == INVALID
+    assert lib.rlcs_run_group(None, 0, None, 0, None) == OK   # nothing to do
+    assert lib.rlcs_run_group(None, 2, None, 0, None) == INVALID
+    assert lib.rlcs_run_group(None, -1, None, 0, None) == INVALID
     assert _group(lib, [_call("gae", **gae)] * 17) == INVALID  # more than RLCS_MAX_GROUP
-    assert _group(lib, [_call("gae", T=513, **gae)]) == INVALID  # long rows are not grouped
+    # long rows that span several tiles need the group's workspace
+    long = [_call("gae", T=50000, **gae)]
+    assert _group_ws(lib, long) == 64 + 32 * 4 * 13  # 4096-step tiles: 13 per row
+    assert _group(lib, long) == WORKSPACE
+    assert _group(lib, long, fake(11, 1 << 30), _group_ws(lib, long) - 32) == WORKSPACE
+    assert _group(lib, long, ctypes.c_void_p(a[0].value + 16), 1 << 20) == INVALID  # overlaps
     assert _group(lib, [_call(99, **gae)]) == INVALID           # unknown estimator
     bad = _call("gae", **gae)
     bad.reserved = 1
