@@ -283,19 +283,6 @@ struct SmemSource {
   }
 };
 
-// One environment's column of a time-major tile in shared memory (one strip).
-struct ColumnSource {
-  const float *col[kNumSlots];  // per slot: this warp's column, 128 steps
-  float halo_next[kNumSlots];   // first step after the tile (scan order)
-  float halo_prev_d;            // done mask before the tile
-  int lane;
-  __device__ __forceinline__ float4 get(int k, int) const {
-    return *reinterpret_cast<const float4 *>(col[k] + 4 * lane);
-  }
-  __device__ __forceinline__ float following(int k, int) const { return halo_next[k]; }
-  __device__ __forceinline__ float preceding_d(int) const { return halo_prev_d; }
-};
-
 // ---------------------------------------------------------------------------
 // Strip engine for one warp's span of S strips.
 // ---------------------------------------------------------------------------

@@ -1,7 +1,7 @@
 """GPU parity for rlcs_run_group: several calls in one launch per class.
 Every call must meet the float64 oracle at the usual bar; short-row calls
-(and every prefix sum) must also equal their namesake's lone call bit for
-bit, since the same body runs. Covers all eight groupable estimators in one
+must also agree with their namesake's lone call to 1e-6 relative (the same
+body runs, compiled into another kernel), and every prefix sum bit for bit. Covers all eight groupable estimators in one
 group, mixed row lengths (all three strip classes and long rows, some
 chained by look-back) with and without truncation in one call list, ragged
 N, V-trace without pg, a full group of 16 calls, repeat calls on one
@@ -91,13 +91,18 @@ def check(rl, plan):
     for (est, N, T, trunc, seed), (_, kw), res, src in zip(plan, calls, got, srcs):
         tag = " [%s N=%d T=%d trunc=%s]" % (est, N, T, trunc)
         mine = as_dict(est, res)
-        # short rows run the lone call's body: identical bits; long rows are
-        # chained by look-back, whose combination order may differ in the
-        # last bits of floats
-        if T <= 512 or est == "episodic_prefix_sum":
-            ref = as_dict(est, alone(rl, est, kw))
-            for k in mine:
+        # The group runs the lone call's body, compiled into another kernel:
+        # the integer prefix sum repeats bit for bit; floats may round
+        # differently where the compiler fuses multiply-adds differently
+        # (and long rows are chained by look-back, whose combination order
+        # varies), so they must agree to a few ulps.
+        ref = as_dict(est, alone(rl, est, kw))
+        for k in mine:
+            if est == "episodic_prefix_sum":
                 assert torch.equal(mine[k], ref[k]), "group differs from the lone call" + tag
+            elif T <= 512:
+                diff = (mine[k] - ref[k]).abs() / ref[k].abs().clamp(min=1.0)
+                assert float(diff.max()) <= 1e-6, "group differs from the lone call" + tag
         compare("episodic_prefix_sum" if est == "episodic_prefix_sum" else est, mine,
                 oracle_of(est, src, trunc), TOL, tag)
 
