@@ -379,6 +379,25 @@ def time_graph(torch, stream, graph, reps):
     return start.elapsed_time(end) / 1e3
 
 
+def time_graph_each(torch, stream, graph, reps):
+    """Seconds of each of `reps` back-to-back replays (an event between
+    consecutive replays, all on `stream`)."""
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        evs[0].record(stream)
+        for i in range(reps):
+            graph.replay()
+            evs[i + 1].record(stream)
+    evs[-1].synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) / 1e3 for i in range(reps)]
+
+
+def percentile(xs, q):
+    ys = sorted(xs)
+    return ys[min(len(ys) - 1, max(0, int(round(q * (len(ys) - 1)))))]
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -527,12 +546,14 @@ def run_ours(args):
                 "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
                 "traffic": traffic, "bytes_per_launch": dom_bytes, "us_per_launch": dom_us,
+                "us_p10": None if grouped else per_est[dom]["us_p10"],
+                "us_p90": None if grouped else per_est[dom]["us_p90"],
                 "timing": ("the headline's timed region: one grouped launch per step on its "
                            "own buffer set (rotation >= 3x L2), CUDA events on the launching "
                            "stream" if grouped else
                            "kernel alone: CUDA graph of back-to-back launches, each on its own "
                            "buffer set (rotation >= 3x L2), CUDA events on the launching "
-                           "stream")}
+                           "stream; >= 20 replays")}
     # what any launch of this size and shape costs: the diagnostic copy of the
     # same bytes (for the group: 16-byte elements over as many rows as make
     # the step's bytes), and the same grid doing nothing
@@ -661,14 +682,38 @@ def time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T, seconds=0.15):
     with torch.cuda.stream(stream):
         g.replay()
     once = time_graph(torch, stream, g, 1)
-    reps = max(3, int(seconds / max(1e-6, once)))
+    reps = max(20, int(seconds / max(1e-6, once)))
+    # throughput from one continuous timed region; the spread from the same
+    # number of replays timed one by one (an event between replays breaks
+    # the launch overlap from one replay into the next, which adds about
+    # 2 us per replay, so those run slightly slower)
     sec = time_graph(torch, stream, g, reps) / (reps * nsets)
-    del g, sets
+    each = [t / nsets for t in time_graph_each(torch, stream, g, reps)]
+    # cold: one call after a write of 3x the L2 has flushed it (event timing)
+    flush = torch.empty(3 * l2, dtype=torch.uint8, device=dev)
+    cold = []
+    for i in range(3):
+        with torch.cuda.stream(stream):
+            flush.fill_(i)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            launch(rl, est, sets[i % nsets], prm)
+            b.record(stream)
+        b.synchronize()
+        cold.append(a.elapsed_time(b) / 1e3)
+    del g, sets, flush
     torch.cuda.synchronize()
-    return {"us_per_launch": sec * 1e6, "env_steps_per_s": N * T / sec,
+    return {"us_per_launch": sec * 1e6, "us_median_of_replays": percentile(each, 0.5) * 1e6,
+            "us_p10": percentile(each, 0.1) * 1e6, "us_p90": percentile(each, 0.9) * 1e6,
+            "replays": reps,
+            "us_cold_single_call": percentile(cold, 0.5) * 1e6,
+            "env_steps_per_s": N * T / sec,
             "gbs": bytes_per_launch(est, N, T) / sec / 1e9,
             "bytes_per_env_step": bytes_per_env_step(est), "rotating_sets": nsets,
-            "footprint_over_l2": nsets * set_bytes / l2}
+            "footprint_over_l2": nsets * set_bytes / l2,
+            "timing": "mean over one timed region of graph replays of back-to-back launches, "
+                      "one per rotating buffer set; median, p10, p90 of the replays timed one "
+                      "by one; cold = one call after an L2 flush"}
 
 
 def time_step(torch, rl, ests, src, dev, stream, prm, l2, N, T, seconds=0.15):
