@@ -935,6 +935,29 @@ def run_profile(args):
     prm = dict(gamma=w.gamma, lambda_=w.lambda_, rho_bar=w.rho_bar, c_bar=w.c_bar)
     src = rollout(N, w.T, w.seed, w.p_term)
     est = args.profile
+    if est == "group":  # the workload's estimators as one rlcs_run_group call
+        nsets = max(2, min(ROTATING_SETS, args.sets))
+        sets = []
+        for _ in range(nsets):
+            st = {}
+            for e_ in w.estimators:
+                ins, outs = ESTIMATORS[e_]
+                e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + ("bootstrap_value",)}
+                for o in outs:
+                    e[o] = torch.empty(e[ins[0]].shape, device=dev,
+                                       dtype=torch.int32 if e_ == "episodic_prefix_sum"
+                                       else torch.float32)
+                st[e_] = e
+            sets.append([(e_, group_kwargs(e_, st[e_], prm)) for e_ in w.estimators])
+        for i in range(args.warmup + args.steps):
+            rl.rlcs_run_group(sets[i % nsets])
+        torch.cuda.synchronize()
+        rl.check_all_workspaces()
+        print(json.dumps({"profile": "group", "workload": args.workload, "N": N, "T": w.T,
+                          "launches": args.warmup + args.steps,
+                          "bytes_per_launch": sum(bytes_per_launch(e_, N, w.T)
+                                                  for e_ in w.estimators)}))
+        return 0
     if est.endswith("_tm"):  # the same arrays stored time-major
         src = {k: (np.ascontiguousarray(v.T) if v.ndim == 2 else v) for k, v in src.items()}
     nsets = max(2, min(ROTATING_SETS, args.sets))
@@ -964,7 +987,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-long-t", action="store_true", help="skip the long-row sweep")
-    ap.add_argument("--profile", choices=tuple(SPECS), default=None,
+    ap.add_argument("--profile", choices=tuple(SPECS) + ("group",), default=None,
                     help="eager launches of one estimator only (for ncu)")
     ap.add_argument("--workload", default=WORKLOAD, choices=tuple(WORKLOADS))
     ap.add_argument("--rows", type=int, default=0, help="profile mode: rows (0 = workload's N)")
