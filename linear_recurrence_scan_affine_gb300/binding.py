@@ -603,13 +603,19 @@ def _group_call(est, kw):
 
 
 def rlcs_run_group(calls, stream=None):
-    """Run up to MAX_GROUP estimator calls in one launch per class (short
-    rows by 128 / 256 / 512 steps, long rows by tile length; truncation
-    inputs present or not). `calls` is a list of (estimator, kwargs) pairs:
-    the estimator is a key of GROUP_ESTIMATORS and kwargs are what its
-    namesake wrapper takes (x and dones for the two forward estimators).
-    Returns the namesakes' results, in order. No output may overlap another
-    call's arrays: the calls run concurrently."""
+    """Run estimator calls in one launch per class (short rows by 128 / 256
+    / 512 steps, long rows by tile length; truncation inputs present or not).
+    `calls` is a list of (estimator, kwargs) pairs: the estimator is a key of
+    GROUP_ESTIMATORS and kwargs are what its namesake wrapper takes (x and
+    dones for the two forward estimators). Returns the namesakes' results, in
+    order. A list longer than MAX_GROUP runs as consecutive groups of
+    MAX_GROUP on the same stream. Within a group no output may overlap
+    another call's arrays: the calls run concurrently."""
+    if len(calls) > MAX_GROUP:
+        out = []
+        for i in range(0, len(calls), MAX_GROUP):
+            out += rlcs_run_group(calls[i:i + MAX_GROUP], stream)
+        return out
     arr = (RlcsCall * max(1, len(calls)))()
     keep, results = [], []
     for i, (est, kw) in enumerate(calls):

@@ -1312,4 +1312,96 @@ __global__ void __launch_bounds__(tm_threads<L>()) time_major_kernel(Params p, T
   if (chained && threadIdx.x == 0) finish_launch(sh.ws, sh.groups * sh.chunks, s_epoch);
 }
 
+// Short time-major rows (T <= 128): one chunk, no look-back, and 16
+// environments per block so that the grid has twice the blocks of the
+// 32-environment shape. Lane l of warp w owns environment 16*g + (l % 16)
+// and the 8 steps 16*w + 8*(l / 16) .. +7; the two halves of a warp combine
+// with one shuffle, the 8 warps of the block in shared memory. Each warp
+// access reads two 64-byte row segments.
+constexpr int kTmShortEnvs = 16;
+constexpr int kTmShortWarps = 8;
+constexpr int kTmShortSteps = 8;  // per lane
+constexpr int kTmShortT = kTmShortWarps * 2 * kTmShortSteps;  // 128
+
+template <class E, bool TRUNC>
+__global__ void __launch_bounds__(kTmShortWarps * 32) time_major_short_kernel(Params p) {
+  static_assert((E::kBF16Slots | E::kU8Slots) == 0u, "time-major slots are 4-byte words");
+  using P = typename E::Pair;
+  using V = typename ValueOf<P>::type;
+  constexpr int L = kTmShortSteps;
+  __shared__ P s_agg[kTmShortWarps][kTmShortEnvs];
+  __shared__ V s_in[kTmShortWarps][kTmShortEnvs];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int el = lane % kTmShortEnvs, half = lane / kTmShortEnvs;
+  const int64_t N = p.N, T = p.T;
+  const int64_t g = blockIdx.x;
+  const int64_t n = g * kTmShortEnvs + el;
+  const bool env_ok = n < N;
+  const int64_t ts = (int64_t)warp * 2 * L + half * L;  // this lane's first step
+  const bool full = ts > 0 && ts + L < T && (g + 1) * kTmShortEnvs <= N;
+  const int64_t rowb = N * 4;
+  int64_t boff[L];
+  boff[0] = (ts * N + n) * 4;
+#pragma unroll
+  for (int j = 1; j < L; ++j) boff[j] = boff[j - 1] + rowb;
+
+  pdl_wait();
+  TmRaw<L> raw;
+  if (full)
+    tm_load<E, TRUNC, true, L>(p, boff, rowb, ts, T, env_ok, raw);
+  else
+    tm_load<E, TRUNC, false, L>(p, boff, rowb, ts, T, env_ok, raw);
+  const float boot = (E::kUsesRowValue && p.boot && env_ok) ? __ldg(p.boot + n) : 0.f;
+  pdl_launch_dependents();  // also keeps the loads above ahead of the arithmetic
+  P e[L];
+  float aux0[L], aux1[L];
+  if (full)
+    tm_build<E, TRUNC, true, L>(p, raw, ts, T, boot, e, aux0, aux1);
+  else
+    tm_build<E, TRUNC, false, L>(p, raw, ts, T, boot, e, aux0, aux1);
+
+  P agg = identity(P{});
+  if (E::kBackward) {
+#pragma unroll
+    for (int j = L - 1; j >= 0; --j) agg = compose(e[j], agg);
+  } else {
+#pragma unroll
+    for (int j = 0; j < L; ++j) agg = compose(e[j], agg);
+  }
+  // the other half of the warp (same environment, the neighbouring 8 steps)
+  P other;
+  other.m = __shfl_xor_sync(kFull, agg.m, kTmShortEnvs);
+  other.c = __shfl_xor_sync(kFull, agg.c, kTmShortEnvs);
+  // warp pair: outer = the half nearer the scan origin
+  const P first = half == 0 ? agg : other, second = half == 0 ? other : agg;
+  const P wagg = E::kBackward ? compose(first, second) : compose(second, first);
+  if (half == 0) s_agg[warp][el] = wagg;
+  __syncthreads();
+
+  if (warp == 0 && half == 0) {
+    V X = V(0);  // one chunk: nothing outside it
+    if (E::kBackward) {
+      for (int w = kTmShortWarps - 1; w >= 0; --w) {
+        s_in[w][el] = X;
+        X = apply(s_agg[w][el], X);
+      }
+    } else {
+      for (int w = 0; w < kTmShortWarps; ++w) {
+        s_in[w][el] = X;
+        X = apply(s_agg[w][el], X);
+      }
+    }
+  }
+  __syncthreads();
+
+  // value adjacent to this lane's 8 steps on the scan-origin side
+  const V Xw = s_in[warp][el];
+  const bool outer = E::kBackward ? (half == 1) : (half == 0);  // nearer the origin
+  const V nb = outer ? Xw : apply(other, Xw);
+  if (full)
+    tm_emit<E, true, L>(p, boff, ts, T, env_ok, nb, e, aux0, aux1);
+  else
+    tm_emit<E, false, L>(p, boff, ts, T, env_ok, nb, e, aux0, aux1);
+}
+
 }  // namespace rlcs

@@ -61,6 +61,11 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
     if constexpr ((E::kBF16Slots | E::kU8Slots) != 0u) {
       return cudaErrorInvalidValue;  // no time-major entry takes compact inputs
     } else {
+      if (p.T <= kTmShortT) {  // one chunk: 16 environments per block, twice the grid
+        const dim3 grid((unsigned)((p.N + kTmShortEnvs - 1) / kTmShortEnvs));
+        return launch_ex(time_major_short_kernel<E, TRUNC>, grid, dim3(kTmShortWarps * 32), 0, s,
+                         plan.pdl, p);
+      }
       const int64_t groups = (p.N + kTmEnvs - 1) / kTmEnvs;
       const TmShape sh{plan.Q > 1 ? ws : nullptr, groups, plan.Q};
       const dim3 grid((unsigned)(groups * plan.Q));

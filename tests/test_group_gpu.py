@@ -205,3 +205,7 @@ def test_long_group_repeats_on_one_workspace(rl):
     for _ in range(3):
         check(rl, plan)
     rl.check_all_workspaces()
+
+
+def test_more_than_sixteen_calls_run_as_consecutive_groups(rl):
+    check(rl, [(ALL[i % len(ALL)], 20 + i, 100 + 13 * i, False, 1000 + i) for i in range(21)])
