@@ -255,3 +255,28 @@ def test_outputs_are_deterministic_for_the_integer_path(rl, dev):
     for _ in range(5):
         again = run_gpu(rl, "episodic_prefix_sum", g, DEFAULT, False)["out"]
         assert torch.equal(first, again)
+
+
+@pytest.mark.parametrize("N,T", [(4096, 128), (64, 20000)])
+@pytest.mark.parametrize("bars", [(1.0, 1.0), (5.0, 2.0)])
+def test_extreme_ratios_and_magnitudes(rl, dev, N, T, bars):
+    # log-ratios spread so far that exp overflows float (clipped to the bar)
+    # or underflows (traces vanish and cut the carry); rewards and values of
+    # magnitude 1e4. The oracle evaluates exp in double: overflow clips to
+    # the same bar, underflow differs by less than 1e-38. Outputs are
+    # compared in units of the input scale: vs = V + A cancels terms of
+    # order 1e4, whose fp32 rounding no reordering avoids.
+    scale = 1e4
+    src = rollout(N, T, 99, p_term=0.01, p_trunc=0.005)
+    rng = np.random.default_rng(7)
+    src["log_rhos"] = (rng.standard_normal((N, T)) * 30.0).astype(np.float32)
+    for k in ("rewards", "values", "q_values", "next_values", "bootstrap_value"):
+        src[k] = (src[k] * scale).astype(np.float32)
+    prm = dict(DEFAULT, rho_bar=bars[0], c_bar=bars[1])
+    g = to_dev(src, dev)
+    for est in ("vtrace", "retrace"):
+        for trunc in (False, True):
+            got = {k: v / scale for k, v in run_gpu(rl, est, g, prm, trunc).items()}
+            want = {k: v / scale for k, v in run_oracle(est, src, prm, trunc).items()}
+            compare(est, got, want, TOL, " [%dx%d %s]" % (N, T, bars))
+    rl.check_all_workspaces()
