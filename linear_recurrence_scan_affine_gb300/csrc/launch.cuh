@@ -61,7 +61,10 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
     if constexpr ((E::kBF16Slots | E::kU8Slots) != 0u) {
       return cudaErrorInvalidValue;  // no time-major entry takes compact inputs
     } else {
-      if (p.T <= kTmShortT) {  // one chunk: 16 environments per block, twice the grid
+      // one chunk: 16 environments per block, twice the grid; measured
+      // faster for calls that move at most four arrays, slower for the
+      // heavier ones (V-trace, Retrace, the fused pair), as for the warp rows
+      if (p.T <= kTmShortT && row_warps<E, TRUNC>() == 8) {
         const dim3 grid((unsigned)((p.N + kTmShortEnvs - 1) / kTmShortEnvs));
         return launch_ex(time_major_short_kernel<E, TRUNC>, grid, dim3(kTmShortWarps * 32), 0, s,
                          plan.pdl, p);
