@@ -209,3 +209,40 @@ def test_long_group_repeats_on_one_workspace(rl):
 
 def test_more_than_sixteen_calls_run_as_consecutive_groups(rl):
     check(rl, [(ALL[i % len(ALL)], 20 + i, 100 + 13 * i, False, 1000 + i) for i in range(21)])
+
+
+def test_long_row_group_in_cuda_graph(rl):
+    dev = torch.device("cuda:0")
+    src = rollout(40, 9000, 1100, p_term=0.002)
+    g = to_dev(src, dev)
+    ests = ("gae", "vtrace", "episodic_prefix_sum")
+    outs, calls = {}, []
+    for e in ests:
+        kw = group_args(e, g, False)
+        outs[e] = torch.empty(40, 9000, device=dev,
+                              dtype=torch.int32 if e == "episodic_prefix_sum" else torch.float32)
+        kw["out"] = outs[e]
+        if e == "vtrace":
+            outs["pg"] = torch.empty(40, 9000, device=dev)
+            kw["out_pg"] = outs["pg"]
+        calls.append((e, kw))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        rl.rlcs_run_group(calls, stream=s)  # warm-up: workspace allocated outside capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        rl.rlcs_run_group(calls, stream=s)
+    for _ in range(3):
+        for o in outs.values():
+            o.zero_()
+        with torch.cuda.stream(s):
+            graph.replay()
+        torch.cuda.synchronize()
+        compare("gae", {"out": outs["gae"]}, oracle_of("gae", src, False), TOL)
+        compare("vtrace", {"vs": outs["vtrace"], "pg": outs["pg"]},
+                oracle_of("vtrace", src, False), TOL)
+        compare("episodic_prefix_sum", {"out": outs["episodic_prefix_sum"]},
+                oracle_of("episodic_prefix_sum", src, False), TOL)
+    rl.check_all_workspaces()

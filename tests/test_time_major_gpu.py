@@ -130,3 +130,33 @@ def test_time_major_repeat_calls(rl):
     for _ in range(3):
         assert torch.equal(rl.rlcs_episodic_prefix_sum_tm(g["x_int"], g["terminateds"]), first)
     rl.check_all_workspaces()
+
+
+def test_time_major_cuda_graph_capture_and_replay(rl):
+    # chained chunks inside a captured graph: every replay moves the
+    # workspace to a new epoch
+    N, T = 200, 3000
+    src = rollout(N, T, 16000, p_term=0.01, p_trunc=0.005)
+    g = {k: (tm(v) if v.ndim == 2 else torch.from_numpy(v).cuda()) for k, v in src.items()}
+    kw = dict(truncateds=g["truncateds"], next_values=g["next_values"])
+    out = torch.empty_like(g["rewards"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # warm-up: the stream's workspace exists before capture
+        rl.rlcs_gae_tm(g["rewards"], g["values"], g["terminateds"], 0.99, 0.95,
+                       g["bootstrap_value"], out=out, stream=s, **kw)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        rl.rlcs_gae_tm(g["rewards"], g["values"], g["terminateds"], 0.99, 0.95,
+                       g["bootstrap_value"], out=out, stream=s, **kw)
+    want = oracle.gae(src["rewards"], src["values"], src["terminateds"], 0.99, 0.95,
+                      src["bootstrap_value"], truncateds=src["truncateds"],
+                      next_values=src["next_values"])
+    for _ in range(4):
+        out.fill_(float("nan"))
+        with torch.cuda.stream(s):
+            graph.replay()
+        torch.cuda.synchronize()
+        compare("gae", {"out": back(out)}, {"out": want}, TOL)
+    rl.check_all_workspaces()
