@@ -927,7 +927,10 @@ __device__ __forceinline__ void tile_body(const Params &p, const TileShape &ts, 
     const int64_t th = t_span + (int64_t)kStrip * S;  // first step after the span
     halo[k] = (E::kBackward && (E::kNext & bit(k)) && th < T) ? load_slot1<E>(p, k, base + th) : 0.f;
   }
-  const float halo_d = (E::kPrevD && t_span > 0) ? load_slot1<E>(p, kD, base + t_span - 1) : 0.f;
+  // A span wholly past the row end (the last tile of a row longer than
+  // what is left) reads nothing: its halo is never used.
+  const float halo_d =
+      (E::kPrevD && t_span > 0 && t_span <= T) ? load_slot1<E>(p, kD, base + t_span - 1) : 0.f;
   const float boot = (E::kUsesRowValue && p.boot) ? __ldg(p.boot + row) : 0.f;
   if (tid == 0 && Q > 1) s_epoch = ld_relaxed_gpu(&ts.ws->epoch);  // after the loads issue
   pdl_launch_dependents();

@@ -72,7 +72,7 @@ def test_workload_with_truncations(rl, dev, name):
 
 ROW_TS = [1, 2, 3, 4, 5, 64, 127, 128, 129, 200, 255, 256, 257, 300, 511, 512]
 CHUNK_CASES = [(1024, T) for T in (1, 7, 1000, 1024, 1028, 3000, 5003)] + \
-              [(2048, T) for T in (2048, 4100, 9001)] + \
+              [(2048, T) for T in (1024, 2048, 2052, 4100, 9001)] + \
               [(4096, T) for T in (4096, 8192, 12289, 40000)]
 
 
