@@ -216,24 +216,34 @@ def cpu_threads():
 
 
 def time_oracle(src, prm, budget_s=10.0):
-    """The oracle as it stands, on all host cores, for about budget_s seconds."""
+    """The oracle as it stands, on all host cores for about budget_s seconds,
+    then on one thread for about a third of that (the single-thread figure
+    rides along under "single_thread")."""
     import concurrent.futures as cf
     import oracle
     threads = cpu_threads()
     N = src["rewards"].shape[0]
     T = src["rewards"].shape[1]
-    with cf.ThreadPoolExecutor(threads) as pool:
-        oracle_step(oracle, src, N, prm, pool, threads)  # warm (loads the library)
+
+    def timed(pool, nthreads, budget):
         reps, t0 = 0, time.perf_counter()
         while True:
-            oracle_step(oracle, src, N, prm, pool, threads)
+            oracle_step(oracle, src, N, prm, pool, nthreads)
             reps += 1
             el = time.perf_counter() - t0
-            if el >= budget_s or reps >= 10000:
-                break
+            if el >= budget or reps >= 10000:
+                return reps, el
+
+    with cf.ThreadPoolExecutor(threads) as pool:
+        oracle_step(oracle, src, N, prm, pool, threads)  # warm (loads the library)
+        reps, el = timed(pool, threads, budget_s)
+    with cf.ThreadPoolExecutor(1) as pool:
+        reps1, el1 = timed(pool, 1, budget_s / 3)
     return {"value": reps * N * T / el, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": "%d full %dx%d batches, all seven estimators, float64 C oracle, rows "
-                      "split over %d threads, %.1f s" % (reps, N, T, threads, el)}
+                      "split over %d threads, %.1f s" % (reps, N, T, threads, el),
+            "single_thread": {"value": reps1 * N * T / el1, "unit": UNIT, "cores": 1,
+                              "sample": "%d full batches on one thread, %.1f s" % (reps1, el1)}}
 
 
 # ---------------------------------------------------------------------------
