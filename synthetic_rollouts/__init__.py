@@ -153,3 +153,35 @@ def compact_rollout(N: int, T: int, seed: int, p_term: float, p_trunc: float = 0
             comp[k] = (src[k] != 0).astype(np.uint8)
             f32[k] = comp[k].astype(np.float32)
     return comp, f32
+
+
+def device_rollout(torch, N: int, T: int, seed: int, p_term: float, fields: Tuple[str, ...],
+                   device, time_major: bool = False, int_range: int = 100):
+    """Draw the named fields of a rollout directly in device memory, for sizes
+    too large to draw on the host (billions of elements). Same distributions
+    as ``rollout`` for those fields (rewards, values ~ N(0, 1); terminateds
+    Bernoulli(p_term) as 0/1 float32; x_int ~ U{-int_range..int_range} int32;
+    bootstrap_value ~ N(0, 1) per environment), drawn by torch's seeded device
+    generator, one generator per field seeded from ``seed`` and the field's
+    position in the fixed draw order. Arrays are [N, T], or [T, N] with
+    time_major. The values differ from ``rollout``'s for the same seed; any
+    row can be copied to the host for the oracle."""
+    shape = (T, N) if time_major else (N, T)
+    out = {}
+    for name in fields:
+        g = torch.Generator(device=device)
+        g.manual_seed(seed * 64 + _STREAMS.index("dones" if name == "terminateds" else name))
+        if name in ("rewards", "values", "q_values", "x"):
+            out[name] = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
+        elif name == "bootstrap_value":
+            out[name] = torch.randn((N,), generator=g, device=device, dtype=torch.float32)
+        elif name == "terminateds":
+            u = torch.rand(shape, generator=g, device=device, dtype=torch.float32)
+            out[name] = (u < p_term).to(torch.float32)
+            del u
+        elif name == "x_int":
+            out[name] = torch.randint(-int_range, int_range + 1, shape, generator=g,
+                                      device=device, dtype=torch.int32)
+        else:
+            raise ValueError("device_rollout draws no %r" % (name,))
+    return out
