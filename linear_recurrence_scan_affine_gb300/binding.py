@@ -176,12 +176,45 @@ def _finish(out, like):
     return out.reshape(like.shape)
 
 
+def _out(t, name, like, dtype=None):
+    """A caller-provided output, written in place. The library writes N*T
+    elements from its first address and cannot see the buffer's size, so it
+    must be a contiguous CUDA tensor on the inputs' device, with their element
+    count and the output's dtype (the inputs' unless stated)."""
+    dtype = like.dtype if dtype is None else dtype
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device != like.device:
+        raise ValueError("%s must be on %s, got %s" % (name, like.device, t.device))
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.numel() != like.numel() or not t.is_contiguous():
+        raise ValueError("%s must be a contiguous tensor of %d elements" % (name, like.numel()))
+    return t
+
+
+def _devices(main, *tensors, stream=None):
+    """Every array of a call on one CUDA device, the current one (the library
+    launches there), and the stream, if one is given, on that device too."""
+    dev = main.device
+    for t in tensors:
+        if t is not None and t.device != dev:
+            raise ValueError("every array of a call must be on %s; one is on %s" % (dev, t.device))
+    cur = torch.cuda.current_device()
+    if dev.index != cur:
+        raise ValueError("the arrays are on %s but the current CUDA device is cuda:%d; call under "
+                         "torch.cuda.device(%s)" % (dev, cur, dev))
+    if stream is not None and stream.device != dev:
+        raise ValueError("the stream is on %s, the arrays on %s" % (stream.device, dev))
+
+
 def rlcs_gae(rewards, values, terminateds, gamma=0.99, lambda_=0.95, bootstrap_value=None,
              truncateds=None, next_values=None, out=None, stream=None):
     N, T, (r, v, d) = _prep(rewards, [(values, "values"), (terminateds, "terminateds")])
     tr, nv = _opt(truncateds, "truncateds", N, T), _opt(next_values, "next_values", N, T)
     b = _boot(bootstrap_value, N)
-    o = torch.empty_like(r) if out is None else out
+    o = torch.empty_like(r) if out is None else _out(out, "out", r)
+    _devices(r, v, d, tr, nv, b, o, stream=stream)
     ws, wsb = workspace_for(N, T, r.device, stream)
     _check(_lib.rlcs_gae(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b), _ptr(o),
                          N, T, gamma, lambda_, _ptr(ws), wsb, _stream(stream)), "rlcs_gae")
@@ -194,7 +227,8 @@ def rlcs_lambda_returns(rewards, values, terminateds, gamma=0.99, lambda_=0.95,
     N, T, (r, v, d) = _prep(rewards, [(values, "values"), (terminateds, "terminateds")])
     tr, nv = _opt(truncateds, "truncateds", N, T), _opt(next_values, "next_values", N, T)
     b = _boot(bootstrap_value, N)
-    o = torch.empty_like(r) if out is None else out
+    o = torch.empty_like(r) if out is None else _out(out, "out", r)
+    _devices(r, v, d, tr, nv, b, o, stream=stream)
     ws, wsb = workspace_for(N, T, r.device, stream)
     _check(_lib.rlcs_lambda_returns(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
                                     _ptr(o), N, T, gamma, lambda_, _ptr(ws), wsb,
@@ -207,7 +241,8 @@ def rlcs_discounted_returns(rewards, terminateds, gamma=0.99, bootstrap_value=No
     N, T, (r, d) = _prep(rewards, [(terminateds, "terminateds")])
     tr, nv = _opt(truncateds, "truncateds", N, T), _opt(next_values, "next_values", N, T)
     b = _boot(bootstrap_value, N)
-    o = torch.empty_like(r) if out is None else out
+    o = torch.empty_like(r) if out is None else _out(out, "out", r)
+    _devices(r, d, tr, nv, b, o, stream=stream)
     ws, wsb = workspace_for(N, T, r.device, stream)
     _check(_lib.rlcs_discounted_returns(_ptr(r), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b), _ptr(o),
                                         N, T, gamma, _ptr(ws), wsb, _stream(stream)),
@@ -223,8 +258,9 @@ def rlcs_vtrace(rewards, values, log_rhos, terminateds, gamma=0.99, lambda_=1.0,
                                           (terminateds, "terminateds")])
     tr, nv = _opt(truncateds, "truncateds", N, T), _opt(next_values, "next_values", N, T)
     b = _boot(bootstrap_value, N)
-    vs = torch.empty_like(r) if out is None else out
-    pg = (torch.empty_like(r) if out_pg is None else out_pg) if with_pg else None
+    vs = torch.empty_like(r) if out is None else _out(out, "out", r)
+    pg = (torch.empty_like(r) if out_pg is None else _out(out_pg, "out_pg", r)) if with_pg else None
+    _devices(r, v, lr, d, tr, nv, b, vs, pg, stream=stream)
     ws, wsb = workspace_for(N, T, r.device, stream)
     _check(_lib.rlcs_vtrace(_ptr(r), _ptr(v), _ptr(lr), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
                             _ptr(vs), _ptr(pg), N, T, gamma, lambda_, rho_bar, c_bar,
@@ -240,7 +276,8 @@ def rlcs_retrace(rewards, values, q_values, log_rhos, terminateds, gamma=0.99, l
                                              (terminateds, "terminateds")])
     tr, nv = _opt(truncateds, "truncateds", N, T), _opt(next_values, "next_values", N, T)
     b = _boot(bootstrap_value, N)
-    o = torch.empty_like(r) if out is None else out
+    o = torch.empty_like(r) if out is None else _out(out, "out", r)
+    _devices(r, v, q, lr, d, tr, nv, b, o, stream=stream)
     ws, wsb = workspace_for(N, T, r.device, stream)
     _check(_lib.rlcs_retrace(_ptr(r), _ptr(v), _ptr(q), _ptr(lr), _ptr(d), _ptr(tr), _ptr(nv),
                              _ptr(b), _ptr(o), N, T, gamma, lambda_, c_bar, _ptr(ws), wsb,
@@ -250,7 +287,8 @@ def rlcs_retrace(rewards, values, q_values, log_rhos, terminateds, gamma=0.99, l
 
 def rlcs_eligibility_traces(x, dones, gamma=0.99, lambda_=0.95, out=None, stream=None):
     N, T, (xx, d) = _prep(x, [(dones, "dones")], rewards_name="x")
-    o = torch.empty_like(xx) if out is None else out
+    o = torch.empty_like(xx) if out is None else _out(out, "out", xx)
+    _devices(xx, d, o, stream=stream)
     ws, wsb = workspace_for(N, T, xx.device, stream)
     _check(_lib.rlcs_eligibility_traces(_ptr(xx), _ptr(d), _ptr(o), N, T, gamma, lambda_,
                                         _ptr(ws), wsb, _stream(stream)),
@@ -264,7 +302,8 @@ def rlcs_episodic_prefix_sum(x, dones, out=None, stream=None):
     d = _rows(dones, "dones")
     if d.shape != (N, T):
         raise ValueError("dones must have shape (%d, %d)" % (N, T))
-    o = torch.empty_like(xx) if out is None else out
+    o = torch.empty_like(xx) if out is None else _out(out, "out", xx)
+    _devices(xx, d, o, stream=stream)
     ws, wsb = workspace_for(N, T, xx.device, stream)
     _check(_lib.rlcs_episodic_prefix_sum(_ptr(xx), _ptr(d), _ptr(o), N, T, _ptr(ws), wsb,
                                          _stream(stream)), "rlcs_episodic_prefix_sum")
@@ -278,8 +317,9 @@ def rlcs_gae_and_returns(rewards, values, terminateds, gamma=0.99, lambda_=0.95,
     N, T, (r, v, d) = _prep(rewards, [(values, "values"), (terminateds, "terminateds")])
     tr, nv = _opt(truncateds, "truncateds", N, T), _opt(next_values, "next_values", N, T)
     b = _boot(bootstrap_value, N)
-    adv = torch.empty_like(r) if out is None else out
-    ret = torch.empty_like(r) if out_returns is None else out_returns
+    adv = torch.empty_like(r) if out is None else _out(out, "out", r)
+    ret = torch.empty_like(r) if out_returns is None else _out(out_returns, "out_returns", r)
+    _devices(r, v, d, tr, nv, b, adv, ret, stream=stream)
     ws, wsb = workspace_for(N, T, r.device, stream)
     _check(_lib.rlcs_gae_and_returns(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
                                      _ptr(adv), _ptr(ret), N, T, gamma, lambda_, _ptr(ws), wsb,
@@ -297,7 +337,8 @@ def rlcs_affine_scan(a, b, reset=None, x_init=None, reverse=False, out=None, str
         if not x0.is_cuda or x0.dtype != torch.float32 or x0.numel() != N:
             raise ValueError("x_init must be a float32 CUDA tensor of %d values" % N)
         x0 = x0.contiguous()
-    o = torch.empty_like(aa) if out is None else out
+    o = torch.empty_like(aa) if out is None else _out(out, "out", aa)
+    _devices(aa, bb, rr, x0, o, stream=stream)
     ws, wsb = workspace_for(N, T, aa.device, stream)
     _check(_lib.rlcs_affine_scan(_ptr(aa), _ptr(bb), _ptr(rr), _ptr(x0), _ptr(o), N, T,
                                  1 if reverse else 0, _ptr(ws), wsb, _stream(stream)),
@@ -335,7 +376,9 @@ def rlcs_gae_compact(rewards, values, terminateds, gamma=0.99, lambda_=0.95,
             raise ValueError("%s must have shape (%d, %d)" % (name, N, T))
     tr, nv = mask8(truncateds, "truncateds"), bits16(next_values, "next_values")
     b = _boot(bootstrap_value, N)
-    o = torch.empty((N, T), dtype=torch.float32, device=r.device) if out is None else out
+    o = (torch.empty((N, T), dtype=torch.float32, device=r.device) if out is None
+         else _out(out, "out", r, dtype=torch.float32))
+    _devices(r, v, d, tr, nv, b, o, stream=stream)
     ws, wsb = workspace_for(N, T, r.device, stream)
     _check(_lib.rlcs_gae_compact(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b), _ptr(o),
                                  N, T, gamma, lambda_, _ptr(ws), wsb, _stream(stream)),
@@ -346,9 +389,19 @@ def rlcs_gae_compact(rewards, values, terminateds, gamma=0.99, lambda_=0.95,
 def rlcs_diag_stream_copy(inputs, out, empty=False, stream=None):
     """Diagnostic: the warp-row launch shape moving the same bytes as an
     estimator without the scan (sum of the inputs into `out`)."""
-    ptrs = (ctypes.c_void_p * len(inputs))(*[t.data_ptr() for t in inputs])
+    if not isinstance(out, torch.Tensor) or out.dim() != 2 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [N, T] tensor")
+    out = _rows(out, "out")  # device and dtype; already contiguous, so not copied
     N, T = out.shape
-    _check(_lib.rlcs_diag_stream_copy(ctypes.cast(ptrs, ctypes.c_void_p), len(inputs), _ptr(out),
+    ins = []
+    for i, t in enumerate(inputs):
+        x = _rows(t, "inputs[%d]" % i)
+        if x.shape != (N, T):
+            raise ValueError("inputs[%d] must have shape (%d, %d)" % (i, N, T))
+        ins.append(x)
+    _devices(out, *ins, stream=stream)
+    ptrs = (ctypes.c_void_p * len(ins))(*[t.data_ptr() for t in ins])
+    _check(_lib.rlcs_diag_stream_copy(ctypes.cast(ptrs, ctypes.c_void_p), len(ins), _ptr(out),
                                       N, T, 1 if empty else 0, _stream(stream)),
            "rlcs_diag_stream_copy")
 
@@ -382,7 +435,8 @@ def rlcs_gae_tm(rewards, values, terminateds, gamma=0.99, lambda_=0.95, bootstra
                                   names=("rewards", "values", "terminateds", "truncateds",
                                          "next_values"))
     b = _boot(bootstrap_value, N)
-    o = torch.empty_like(r) if out is None else out
+    o = torch.empty_like(r) if out is None else _out(out, "out", r)
+    _devices(r, v, d, tr, nv, b, o, stream=stream)
     ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_gae_tm(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b), _ptr(o), N, T,
                             gamma, lambda_, _ptr(ws), wsb, _stream(stream)), "rlcs_gae_tm")
@@ -396,7 +450,8 @@ def rlcs_lambda_returns_tm(rewards, values, terminateds, gamma=0.99, lambda_=0.9
                                   names=("rewards", "values", "terminateds", "truncateds",
                                          "next_values"))
     b = _boot(bootstrap_value, N)
-    o = torch.empty_like(r) if out is None else out
+    o = torch.empty_like(r) if out is None else _out(out, "out", r)
+    _devices(r, v, d, tr, nv, b, o, stream=stream)
     ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_lambda_returns_tm(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
                                        _ptr(o), N, T, gamma, lambda_, _ptr(ws), wsb,
@@ -410,7 +465,8 @@ def rlcs_discounted_returns_tm(rewards, terminateds, gamma=0.99, bootstrap_value
     T, N, (r, d, tr, nv) = _tm(rewards, terminateds, truncateds, next_values,
                                names=("rewards", "terminateds", "truncateds", "next_values"))
     b = _boot(bootstrap_value, N)
-    o = torch.empty_like(r) if out is None else out
+    o = torch.empty_like(r) if out is None else _out(out, "out", r)
+    _devices(r, d, tr, nv, b, o, stream=stream)
     ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_discounted_returns_tm(_ptr(r), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b), _ptr(o),
                                            N, T, gamma, _ptr(ws), wsb, _stream(stream)),
@@ -426,8 +482,9 @@ def rlcs_vtrace_tm(rewards, values, log_rhos, terminateds, gamma=0.99, lambda_=1
                                       names=("rewards", "values", "log_rhos", "terminateds",
                                              "truncateds", "next_values"))
     b = _boot(bootstrap_value, N)
-    vs = torch.empty_like(r) if out is None else out
-    pg = (torch.empty_like(r) if out_pg is None else out_pg) if with_pg else None
+    vs = torch.empty_like(r) if out is None else _out(out, "out", r)
+    pg = (torch.empty_like(r) if out_pg is None else _out(out_pg, "out_pg", r)) if with_pg else None
+    _devices(r, v, lr, d, tr, nv, b, vs, pg, stream=stream)
     ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_vtrace_tm(_ptr(r), _ptr(v), _ptr(lr), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
                                _ptr(vs), _ptr(pg), N, T, gamma, lambda_, rho_bar, c_bar,
@@ -443,7 +500,8 @@ def rlcs_retrace_tm(rewards, values, q_values, log_rhos, terminateds, gamma=0.99
                                          names=("rewards", "values", "q_values", "log_rhos",
                                                 "terminateds", "truncateds", "next_values"))
     b = _boot(bootstrap_value, N)
-    o = torch.empty_like(r) if out is None else out
+    o = torch.empty_like(r) if out is None else _out(out, "out", r)
+    _devices(r, v, q, lr, d, tr, nv, b, o, stream=stream)
     ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_retrace_tm(_ptr(r), _ptr(v), _ptr(q), _ptr(lr), _ptr(d), _ptr(tr), _ptr(nv),
                                 _ptr(b), _ptr(o), N, T, gamma, lambda_, c_bar, _ptr(ws), wsb,
@@ -454,7 +512,8 @@ def rlcs_retrace_tm(rewards, values, q_values, log_rhos, terminateds, gamma=0.99
 
 def rlcs_eligibility_traces_tm(x, dones, gamma=0.99, lambda_=0.95, out=None, stream=None):
     T, N, (xx, d) = _tm(x, dones, names=("x", "dones"))
-    o = torch.empty_like(xx) if out is None else out
+    o = torch.empty_like(xx) if out is None else _out(out, "out", xx)
+    _devices(xx, d, o, stream=stream)
     ws, wsb = _tm_ws(N, T, xx.device, stream)
     _check(_lib.rlcs_eligibility_traces_tm(_ptr(xx), _ptr(d), _ptr(o), N, T, gamma, lambda_,
                                            _ptr(ws), wsb, _stream(stream)),
@@ -464,7 +523,8 @@ def rlcs_eligibility_traces_tm(x, dones, gamma=0.99, lambda_=0.95, out=None, str
 
 def rlcs_episodic_prefix_sum_tm(x, dones, out=None, stream=None):
     T, N, (xx, d) = _tm(x, dones, names=("x", "dones"), dtypes=(torch.int32, torch.float32))
-    o = torch.empty_like(xx) if out is None else out
+    o = torch.empty_like(xx) if out is None else _out(out, "out", xx)
+    _devices(xx, d, o, stream=stream)
     ws, wsb = _tm_ws(N, T, xx.device, stream)
     _check(_lib.rlcs_episodic_prefix_sum_tm(_ptr(xx), _ptr(d), _ptr(o), N, T, _ptr(ws), wsb,
                                             _stream(stream)),
@@ -479,8 +539,9 @@ def rlcs_gae_and_returns_tm(rewards, values, terminateds, gamma=0.99, lambda_=0.
                                   names=("rewards", "values", "terminateds", "truncateds",
                                          "next_values"))
     b = _boot(bootstrap_value, N)
-    adv = torch.empty_like(r) if out is None else out
-    ret = torch.empty_like(r) if out_returns is None else out_returns
+    adv = torch.empty_like(r) if out is None else _out(out, "out", r)
+    ret = torch.empty_like(r) if out_returns is None else _out(out_returns, "out_returns", r)
+    _devices(r, v, d, tr, nv, b, adv, ret, stream=stream)
     ws, wsb = _tm_ws(N, T, r.device, stream)
     _check(_lib.rlcs_gae_and_returns_tm(_ptr(r), _ptr(v), _ptr(d), _ptr(tr), _ptr(nv), _ptr(b),
                                         _ptr(adv), _ptr(ret), N, T, gamma, lambda_,
@@ -491,7 +552,8 @@ def rlcs_gae_and_returns_tm(rewards, values, terminateds, gamma=0.99, lambda_=0.
 def rlcs_affine_scan_tm(a, b, reset=None, x_init=None, reverse=False, out=None, stream=None):
     T, N, (aa, bb, rr) = _tm(a, b, reset, names=("a", "b", "reset"))
     x0 = None if x_init is None else _boot(x_init, N)
-    o = torch.empty_like(aa) if out is None else out
+    o = torch.empty_like(aa) if out is None else _out(out, "out", aa)
+    _devices(aa, bb, rr, x0, o, stream=stream)
     ws, wsb = _tm_ws(N, T, aa.device, stream)
     _check(_lib.rlcs_affine_scan_tm(_ptr(aa), _ptr(bb), _ptr(rr), _ptr(x0), _ptr(o), N, T,
                                     1 if reverse else 0, _ptr(ws), wsb, _stream(stream)),
@@ -578,14 +640,14 @@ def _group_call(est, kw):
     c.c_bar = kw.pop("c_bar", 1.0)
     c.N, c.T = N, T
     out = kw.pop("out", None)
-    out = torch.empty_like(lead) if out is None else out
+    out = torch.empty_like(lead) if out is None else _out(out, "out", lead)
     keep.append(out)
     c.out = out.data_ptr()
     result = out
     if est == "vtrace":
         pg = kw.pop("out_pg", None)
         if kw.pop("with_pg", True):
-            pg = torch.empty_like(lead) if pg is None else pg
+            pg = torch.empty_like(lead) if pg is None else _out(pg, "out_pg", lead)
             keep.append(pg)
             c.out2 = pg.data_ptr()
         else:
@@ -593,7 +655,7 @@ def _group_call(est, kw):
         result = (out, pg)
     elif est == "gae_and_returns":
         ret = kw.pop("out_returns", None)
-        ret = torch.empty_like(lead) if ret is None else ret
+        ret = torch.empty_like(lead) if ret is None else _out(ret, "out_returns", lead)
         keep.append(ret)
         c.out2 = ret.data_ptr()
         result = (out, ret)
@@ -623,6 +685,8 @@ def rlcs_run_group(calls, stream=None):
         arr[i] = c
         keep += k
         results.append(res)
+    if keep:
+        _devices(keep[0], *keep[1:], stream=stream)
     ptr = ctypes.cast(arr, ctypes.c_void_p)
     need = _lib.rlcs_group_workspace_bytes(ptr, len(calls)) if calls else 0
     ws, wsb = None, 0
