@@ -17,8 +17,12 @@
  * ---------------------------------------------------------------------------
  * Conventions common to every entry point
  * ---------------------------------------------------------------------------
- * Memory.    Every array pointer is DEVICE memory owned by the caller. The
- *            library allocates nothing and frees nothing.
+ * Memory.    Every array pointer is DEVICE memory owned by the caller, on
+ *            the current CUDA device (launches go there). The library
+ *            allocates nothing and frees nothing. Every per-step array,
+ *            outputs included, must hold N*T elements from its pointer: the
+ *            library cannot see a buffer's size, so a shorter output is
+ *            written past its end.
  * Layout.    Per-step arrays are [N, T], row-major, time-contiguous
  *            (element (n, t) at offset n*T + t). float32, except the prefix
  *            sum's int32 input and output. bootstrap_value is [N].
