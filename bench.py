@@ -728,10 +728,11 @@ def time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T, seconds=0.15):
 
 def time_step(torch, rl, ests, src, dev, stream, prm, l2, N, T, seconds=0.15):
     """The estimators of one step over rotating buffer sets that span >= 3x
-    the L2, in three schedules: each estimator on its own stream (as the
-    headline step), all on one stream, and one rlcs_run_group call. Returns
-    all three and, as the step, the fastest: time per step and the step's
-    algorithmic GB/s."""
+    the L2, in several schedules: each estimator on its own stream (as the
+    headline step), all on one stream, one rlcs_run_group call, and the
+    estimators split into 2 or 3 groups, each group's call on its own
+    stream. Returns all of them and, as the step, the fastest: time per step
+    and the step's algorithmic GB/s."""
     step_bytes = sum(bytes_per_launch(e, N, T) for e in ests)
     nsets = int(min(64, max(2, -(-3 * l2 // step_bytes))))
     sets = []
@@ -773,12 +774,33 @@ def time_step(torch, rl, ests, src, dev, stream, prm, l2, N, T, seconds=0.15):
         for calls in group_calls:
             rl.rlcs_run_group(calls)
 
+    # k groups, each one rlcs_run_group call per buffer set on its own stream
+    # (estimators dealt round-robin, heaviest first)
+    order = sorted(ests, key=lambda e: -bytes_per_launch(e, N, T))
+    split = {k: [order[i::k] for i in range(k)] for k in (2, 3) if len(ests) > k}
+    gside = {k: [torch.cuda.Stream(dev) for _ in range(k)] for k in split}
+
+    def groups_on_streams(k):
+        def run():
+            for part, s in zip(split[k], gside[k]):
+                s.wait_stream(stream)
+                with torch.cuda.stream(s):
+                    for st in sets:
+                        rl.rlcs_run_group([(e, group_kwargs(e, st[e], prm)) for e in part])
+            for s in gside[k]:
+                stream.wait_stream(s)
+        return run
+
     with torch.cuda.stream(stream):  # the one-stream schedules' workspaces
         serial()
         grouped()
+    for k in split:  # and the group streams' (created before capture)
+        groups_on_streams(k)()
     torch.cuda.synchronize()
     us = {}
-    for name, fn in (("streams", concurrent), ("one_stream", serial), ("grouped", grouped)):
+    schedules = [("streams", concurrent), ("one_stream", serial), ("grouped", grouped)]
+    schedules += [("groups_on_%d_streams" % k, groups_on_streams(k)) for k in split]
+    for name, fn in schedules:
         g = capture(torch, stream, fn)
         with torch.cuda.stream(stream):
             g.replay()
