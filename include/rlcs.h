@@ -31,6 +31,16 @@
  *            anything else takes a scalar path with the same results.
  * Masks.     terminateds / truncateds / dones are 0/1 float32; an entry
  *            counts as set when it is nonzero.
+ * Scalars.   gamma, lambda, rho_bar and c_bar are double. Every step is
+ *            computed in fp32 with the scalars rounded to fp32, but where
+ *            an estimator's multiplier between cuts is one constant beta
+ *            (discounted returns: gamma; GAE, TD(lambda) returns, traces:
+ *            gamma*lambda) the multiplier of a 4-, 8- or 16-step span is
+ *            beta^k raised in double and rounded once. Over long undamped
+ *            horizons (1/(1-beta) steps) the fp32 rounding of beta itself,
+ *            and of products of it, would otherwise add up: at gamma = 0.997
+ *            over 16384 steps the rounding of gamma alone moves discounted
+ *            returns by 2e-4 of max(1, |G|).
  * Boundary.  (Methodology 3 "Explicit Boundary Semantics".) The successor
  *            value of step t is: 0 if terminateds[t] is set; otherwise
  *            next_values[t] if truncateds[t] is set; otherwise
@@ -112,8 +122,8 @@ const char *rlcs_status_string(rlcs_status status);
 rlcs_status rlcs_gae(const float *rewards, const float *values,
                      const float *terminateds, const float *truncateds,
                      const float *next_values, const float *bootstrap_value,
-                     float *advantages, int64_t N, int64_t T, float gamma,
-                     float lambda, void *workspace, size_t workspace_bytes,
+                     float *advantages, int64_t N, int64_t T, double gamma,
+                     double lambda, void *workspace, size_t workspace_bytes,
                      rlcs_stream_t stream);
 
 /* TD(lambda) returns.
@@ -127,8 +137,8 @@ rlcs_status rlcs_lambda_returns(const float *rewards, const float *values,
                                 const float *truncateds,
                                 const float *next_values,
                                 const float *bootstrap_value, float *returns,
-                                int64_t N, int64_t T, float gamma,
-                                float lambda, void *workspace,
+                                int64_t N, int64_t T, double gamma,
+                                double lambda, void *workspace,
                                 size_t workspace_bytes, rlcs_stream_t stream);
 
 /* Discounted reward-to-go.
@@ -142,7 +152,7 @@ rlcs_status rlcs_discounted_returns(const float *rewards,
                                     const float *next_values,
                                     const float *bootstrap_value,
                                     float *returns, int64_t N, int64_t T,
-                                    float gamma, void *workspace,
+                                    double gamma, void *workspace,
                                     size_t workspace_bytes,
                                     rlcs_stream_t stream);
 
@@ -160,7 +170,7 @@ rlcs_status rlcs_vtrace(const float *rewards, const float *values,
                         const float *truncateds, const float *next_values,
                         const float *bootstrap_value, float *vs,
                         float *pg_advantages, int64_t N, int64_t T,
-                        float gamma, float lambda, float rho_bar, float c_bar,
+                        double gamma, double lambda, double rho_bar, double c_bar,
                         void *workspace, size_t workspace_bytes,
                         rlcs_stream_t stream);
 
@@ -177,8 +187,8 @@ rlcs_status rlcs_retrace(const float *rewards, const float *values,
                          const float *terminateds, const float *truncateds,
                          const float *next_values,
                          const float *bootstrap_value, float *q_ret,
-                         int64_t N, int64_t T, float gamma, float lambda,
-                         float c_bar, void *workspace, size_t workspace_bytes,
+                         int64_t N, int64_t T, double gamma, double lambda,
+                         double c_bar, void *workspace, size_t workspace_bytes,
                          rlcs_stream_t stream);
 
 /* Accumulating eligibility traces, forward in time.
@@ -188,7 +198,7 @@ rlcs_status rlcs_retrace(const float *rewards, const float *values,
  * them into dones. */
 rlcs_status rlcs_eligibility_traces(const float *x, const float *dones,
                                     float *traces, int64_t N, int64_t T,
-                                    float gamma, float lambda,
+                                    double gamma, double lambda,
                                     void *workspace, size_t workspace_bytes,
                                     rlcs_stream_t stream);
 
@@ -212,7 +222,7 @@ rlcs_status rlcs_gae_and_returns(const float *rewards, const float *values,
                                  const float *terminateds, const float *truncateds,
                                  const float *next_values, const float *bootstrap_value,
                                  float *advantages, float *returns, int64_t N, int64_t T,
-                                 float gamma, float lambda, void *workspace,
+                                 double gamma, double lambda, void *workspace,
                                  size_t workspace_bytes, rlcs_stream_t stream);
 
 /* GAE on compact inputs: the same estimator, conventions and fp32 output as
@@ -225,8 +235,8 @@ rlcs_status rlcs_gae_and_returns(const float *rewards, const float *values,
 rlcs_status rlcs_gae_compact(const uint16_t *rewards, const uint16_t *values,
                              const uint8_t *terminateds, const uint8_t *truncateds,
                              const uint16_t *next_values, const float *bootstrap_value,
-                             float *advantages, int64_t N, int64_t T, float gamma,
-                             float lambda, void *workspace, size_t workspace_bytes,
+                             float *advantages, int64_t N, int64_t T, double gamma,
+                             double lambda, void *workspace, size_t workspace_bytes,
                              rlcs_stream_t stream);
 
 /* Generic segmented first-order affine recurrence on raw coefficients.
@@ -264,33 +274,33 @@ size_t rlcs_workspace_bytes_tm(int64_t N, int64_t T);
 rlcs_status rlcs_gae_tm(const float *rewards, const float *values, const float *terminateds,
                         const float *truncateds, const float *next_values,
                         const float *bootstrap_value, float *advantages, int64_t N, int64_t T,
-                        float gamma, float lambda, void *workspace, size_t workspace_bytes,
+                        double gamma, double lambda, void *workspace, size_t workspace_bytes,
                         rlcs_stream_t stream);
 rlcs_status rlcs_lambda_returns_tm(const float *rewards, const float *values,
                                    const float *terminateds, const float *truncateds,
                                    const float *next_values, const float *bootstrap_value,
-                                   float *returns, int64_t N, int64_t T, float gamma,
-                                   float lambda, void *workspace, size_t workspace_bytes,
+                                   float *returns, int64_t N, int64_t T, double gamma,
+                                   double lambda, void *workspace, size_t workspace_bytes,
                                    rlcs_stream_t stream);
 rlcs_status rlcs_discounted_returns_tm(const float *rewards, const float *terminateds,
                                        const float *truncateds, const float *next_values,
                                        const float *bootstrap_value, float *returns, int64_t N,
-                                       int64_t T, float gamma, void *workspace,
+                                       int64_t T, double gamma, void *workspace,
                                        size_t workspace_bytes, rlcs_stream_t stream);
 rlcs_status rlcs_vtrace_tm(const float *rewards, const float *values, const float *log_rhos,
                            const float *terminateds, const float *truncateds,
                            const float *next_values, const float *bootstrap_value, float *vs,
-                           float *pg_advantages, int64_t N, int64_t T, float gamma,
-                           float lambda, float rho_bar, float c_bar, void *workspace,
+                           float *pg_advantages, int64_t N, int64_t T, double gamma,
+                           double lambda, double rho_bar, double c_bar, void *workspace,
                            size_t workspace_bytes, rlcs_stream_t stream);
 rlcs_status rlcs_retrace_tm(const float *rewards, const float *values, const float *q_values,
                             const float *log_rhos, const float *terminateds,
                             const float *truncateds, const float *next_values,
                             const float *bootstrap_value, float *q_ret, int64_t N, int64_t T,
-                            float gamma, float lambda, float c_bar, void *workspace,
+                            double gamma, double lambda, double c_bar, void *workspace,
                             size_t workspace_bytes, rlcs_stream_t stream);
 rlcs_status rlcs_eligibility_traces_tm(const float *x, const float *dones, float *traces,
-                                       int64_t N, int64_t T, float gamma, float lambda,
+                                       int64_t N, int64_t T, double gamma, double lambda,
                                        void *workspace, size_t workspace_bytes,
                                        rlcs_stream_t stream);
 rlcs_status rlcs_episodic_prefix_sum_tm(const int32_t *x, const float *dones, int32_t *out,
@@ -300,7 +310,7 @@ rlcs_status rlcs_gae_and_returns_tm(const float *rewards, const float *values,
                                     const float *terminateds, const float *truncateds,
                                     const float *next_values, const float *bootstrap_value,
                                     float *advantages, float *returns, int64_t N, int64_t T,
-                                    float gamma, float lambda, void *workspace,
+                                    double gamma, double lambda, void *workspace,
                                     size_t workspace_bytes, rlcs_stream_t stream);
 rlcs_status rlcs_affine_scan_tm(const float *a, const float *b, const float *reset,
                                 const float *x_init, float *x, int64_t N, int64_t T, int reverse,
@@ -365,7 +375,7 @@ typedef struct {
   void *out;
   float *out2;
   int64_t N, T;
-  float gamma, lambda, rho_bar, c_bar;
+  double gamma, lambda, rho_bar, c_bar;
 } rlcs_call;
 
 size_t rlcs_group_workspace_bytes(const rlcs_call *calls, int n_calls);
@@ -396,8 +406,8 @@ rlcs_status rlcs_run_group(const rlcs_call *calls, int n_calls, void *workspace,
 rlcs_status rlcs_gae_noalloc(const float *rewards, const float *values,
                              const float *terminateds, const float *truncateds,
                              const float *next_values, const float *bootstrap_value,
-                             float *advantages, int64_t N, int64_t T, float gamma,
-                             float lambda, rlcs_stream_t stream);
+                             float *advantages, int64_t N, int64_t T, double gamma,
+                             double lambda, rlcs_stream_t stream);
 
 /* Diagnostic, not an estimator: the warp-row shape's launch and data
  * movement with no scan, for measuring what a launch of a given size costs

@@ -32,7 +32,8 @@ def _load():
             "librlcs.so is not built (%s); run linear_recurrence_scan_affine_gb300.build.build()"
             % LIB_PATH)
     lib = ctypes.CDLL(LIB_PATH)
-    P, I64, F, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+    # F: the scalars (gamma, lambda, rho_bar, c_bar) travel as double
+    P, I64, F, SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double, ctypes.c_size_t
     sig = {
         "rlcs_workspace_bytes": ([I64, I64], SZ),
         "rlcs_workspace_bytes_tm": ([I64, I64], SZ),
@@ -573,8 +574,8 @@ class RlcsCall(ctypes.Structure):
                 ("next_values", ctypes.c_void_p), ("bootstrap_value", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("out2", ctypes.c_void_p),
                 ("N", ctypes.c_int64), ("T", ctypes.c_int64),
-                ("gamma", ctypes.c_float), ("lambda_", ctypes.c_float),
-                ("rho_bar", ctypes.c_float), ("c_bar", ctypes.c_float)]
+                ("gamma", ctypes.c_double), ("lambda_", ctypes.c_double),
+                ("rho_bar", ctypes.c_double), ("c_bar", ctypes.c_double)]
 
 
 GROUP_ESTIMATORS = {"gae": 0, "lambda_returns": 1, "discounted_returns": 2, "vtrace": 3,

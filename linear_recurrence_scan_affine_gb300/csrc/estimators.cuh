@@ -24,7 +24,11 @@ struct Params {
   void *out0;                  // [N, T] float (int32 for the prefix sum)
   float *out1;                 // [N, T] second output (V-trace pg) or NULL
   int64_t N, T;
-  float gamma, lambda, rho_bar, c_bar;
+  float gamma, lambda, rho_bar, c_bar;  // the call's scalars, rounded to fp32
+  // beta^4, beta^8, beta^16 for estimators whose multiplier between cuts is
+  // one constant beta (kConstBeta): raised in double from the call's double
+  // scalars and rounded once. Unused (0) for the others.
+  float beta4, beta8, beta16;
   int vec;                     // 1: rows 16-byte aligned (T % 4 == 0, aligned bases)
 };
 
@@ -54,12 +58,17 @@ constexpr uint32_t kTruncSlots = bit(kTau) | bit(kNV);
 struct F32Slots {
   static constexpr uint32_t kBF16Slots = 0u;
   static constexpr uint32_t kU8Slots = 0u;
+  // The multiplier between cuts is one constant beta (0 at a cut): spans of
+  // 4, 8 or 16 steps then take beta^k from Params instead of a product of k
+  // fp32 factors (see span_multiplier in kernels.cuh).
+  static constexpr bool kConstBeta = false;
 };
 
 // ---------------------------------------------------------------------------
 // GAE: alpha = r + gamma*S - V, beta = gamma*lambda (0 at a cut). Out: A.
 // ---------------------------------------------------------------------------
 struct Gae : F32Slots {
+  static constexpr bool kConstBeta = true;  // beta = gamma*lambda
   static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
   static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
   static constexpr bool kPrevD = false;         // reads the done mask at t-1
@@ -86,6 +95,7 @@ struct Gae : F32Slots {
 // at a cut alpha = r + gamma*S, beta = 0. Out: G.
 // ---------------------------------------------------------------------------
 struct LambdaReturns : F32Slots {
+  static constexpr bool kConstBeta = true;  // beta = gamma*lambda
   static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
   static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
   static constexpr bool kPrevD = false;         // reads the done mask at t-1
@@ -113,6 +123,7 @@ struct LambdaReturns : F32Slots {
 // ---------------------------------------------------------------------------
 struct DiscountedReturns : F32Slots {
   static constexpr uint32_t kOptSlots = kTruncSlots;  // slots added when the optional input is given
+  static constexpr bool kConstBeta = true;  // beta = gamma
   static constexpr bool kUsesRowValue = true;  // reads bootstrap_value[n]
   static constexpr bool kPrevD = false;         // reads the done mask at t-1
   static constexpr bool kBackward = true;
@@ -213,6 +224,7 @@ struct Retrace : F32Slots {
 // beta_0 = 0 (e_{-1} = 0). Out: e.
 // ---------------------------------------------------------------------------
 struct EligibilityTraces : F32Slots {
+  static constexpr bool kConstBeta = true;  // beta = gamma*lambda
   static constexpr uint32_t kOptSlots = 0u;  // slots added when the optional input is given
   static constexpr bool kUsesRowValue = false;  // reads bootstrap_value[n]
   static constexpr bool kPrevD = true;         // reads the done mask at t-1
@@ -258,6 +270,7 @@ struct EpisodicPrefixSum : F32Slots {
 // A_t and G_t = A_t + V_t (the identity TD(lambda) = GAE + V).
 // ---------------------------------------------------------------------------
 struct GaeAndReturns : F32Slots {
+  static constexpr bool kConstBeta = true;  // beta = gamma*lambda
   static constexpr uint32_t kOptSlots = kTruncSlots;
   static constexpr bool kUsesRowValue = true;
   static constexpr bool kPrevD = false;

@@ -235,6 +235,29 @@ __device__ __forceinline__ P lane_aggregate(const P (&e)[4], bool backward) {
   return a;
 }
 
+// Estimators with kConstBeta: the multiplier of k consecutive steps is
+// beta^k unless one of them is a cut (multiplier exactly 0). beta^k comes
+// from the host, raised in double from the call's scalars and rounded once,
+// so the span's multiplier carries neither the fp32 rounding of beta nor
+// k-1 fp32 roundings of a product. A product's roundings are the same in
+// every span without a cut, so over an undamped horizon of ~1/(1-beta)
+// steps they add up (discounted returns at gamma = 0.997: a plain four-step
+// product doubled the worst error). Identity padding past a row end (m = 1)
+// also reads as "no cut"; such spans only compose behind the row's last
+// step (a cut) or after every real step, so they never reach an output.
+template <int K>
+__device__ __forceinline__ float span_multiplier(const FPair (&e)[K], float beta_k) {
+  bool nz = true;
+#pragma unroll
+  for (int j = 0; j < K; ++j) nz = nz && (e[j].m != 0.0f);
+  return nz ? beta_k : 0.0f;
+}
+template <int K>
+__device__ __forceinline__ float const_beta_power(const Params &p) {
+  static_assert(K == 4 || K == 8 || K == 16, "the powers the host provides");
+  return K == 4 ? p.beta4 : (K == 8 ? p.beta8 : p.beta16);
+}
+
 template <class P> struct ValueOf;
 template <> struct ValueOf<FPair> { using type = float; };
 template <> struct ValueOf<IPair> { using type = uint32_t; };
@@ -295,6 +318,7 @@ struct Strips {
   P el[S][4];
   float aux0[S][4], aux1[S][4];
   P excl[S], tot[S];
+  float beta4;  // Params::beta4 (kConstBeta estimators)
 
   // t_span: the span's first step within the row; T: the row length.
   // ZERO_PAD: steps past the row end arrive as zeros (register-loaded spans).
@@ -306,6 +330,7 @@ struct Strips {
   template <bool ZERO_PAD = false, class Src>
   __device__ __forceinline__ void build(const Params &p, const Src &src, float boot,
                                         int64_t t_span, int64_t T, int lane) {
+    beta4 = p.beta4;
     // Per-element bounds in 32-bit offsets from the span start: steps left in
     // the row (clamped; a span is at most a few thousand steps long).
     const int64_t left = T - t_span;
@@ -367,7 +392,8 @@ struct Strips {
   __device__ __forceinline__ P scan(int lane) {
 #pragma unroll
     for (int j = 0; j < S; ++j) {
-      const P a = lane_aggregate(el[j], E::kBackward);
+      P a = lane_aggregate(el[j], E::kBackward);
+      if constexpr (E::kConstBeta) a.m = span_multiplier<4>(el[j], beta4);
       if (E::kBackward) {
         const P inc = warp_suffix_scan(a, lane);
         tot[j] = shfl_idx(inc, 0);
@@ -1287,6 +1313,7 @@ __global__ void __launch_bounds__(tm_threads<L>()) time_major_kernel(Params p, T
 #pragma unroll
     for (int j = 0; j < L; ++j) agg = compose(e[j], agg);
   }
+  if constexpr (E::kConstBeta) agg.m = span_multiplier<L>(e, const_beta_power<L>(p));
   s_agg[warp][lane] = agg;
   __syncthreads();
 
@@ -1380,6 +1407,7 @@ __global__ void __launch_bounds__(kTmShortWarps * 32) time_major_short_kernel(Pa
 #pragma unroll
     for (int j = 0; j < L; ++j) agg = compose(e[j], agg);
   }
+  if constexpr (E::kConstBeta) agg.m = span_multiplier<L>(e, const_beta_power<L>(p));
   // the other half of the warp (same environment, the neighbouring 8 steps)
   P other;
   other.m = __shfl_xor_sync(kFull, agg.m, kTmShortEnvs);

@@ -228,6 +228,16 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
   return RLCS_OK;
 }
 
+// Powers of beta, the multiplier between cuts of the estimators that have
+// one constant multiplier (discounted returns: gamma; GAE, TD(lambda) returns
+// and eligibility traces: gamma*lambda), raised in double and rounded once.
+void set_beta(Params &p, double beta) {
+  const double b4 = (beta * beta) * (beta * beta), b8 = b4 * b4;
+  p.beta4 = (float)b4;
+  p.beta8 = (float)b8;
+  p.beta16 = (float)(b8 * b8);
+}
+
 Params base_params(int64_t N, int64_t T, const float *boot) {
   Params p;
   std::memset(&p, 0, sizeof(p));
@@ -311,7 +321,7 @@ rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk) {
 rlcs_status rlcs_gae(const float *rewards, const float *values, const float *terminateds,
                      const float *truncateds, const float *next_values,
                      const float *bootstrap_value, float *advantages, int64_t N, int64_t T,
-                     float gamma, float lambda, void *workspace, size_t workspace_bytes,
+                     double gamma, double lambda, void *workspace, size_t workspace_bytes,
                      rlcs_stream_t stream) {
   if (!rewards || !values || !terminateds || !advantages) return RLCS_ERR_INVALID_ARG;
   Params p = base_params(N, T, bootstrap_value);
@@ -319,8 +329,9 @@ rlcs_status rlcs_gae(const float *rewards, const float *values, const float *ter
   p.in[kV] = values;
   p.in[kD] = terminateds;
   p.out0 = advantages;
-  p.gamma = gamma;
-  p.lambda = lambda;
+  p.gamma = (float)gamma;
+  p.lambda = (float)lambda;
+  set_beta(p, gamma * lambda);
   void *outs[1] = {advantages};
   return run(p, truncateds, next_values, outs, 1, workspace, workspace_bytes,
              reinterpret_cast<cudaStream_t>(stream), launch_gae, truncateds != nullptr);
@@ -329,7 +340,7 @@ rlcs_status rlcs_gae(const float *rewards, const float *values, const float *ter
 rlcs_status rlcs_lambda_returns(const float *rewards, const float *values,
                                 const float *terminateds, const float *truncateds,
                                 const float *next_values, const float *bootstrap_value,
-                                float *returns, int64_t N, int64_t T, float gamma, float lambda,
+                                float *returns, int64_t N, int64_t T, double gamma, double lambda,
                                 void *workspace, size_t workspace_bytes, rlcs_stream_t stream) {
   if (!rewards || !values || !terminateds || !returns) return RLCS_ERR_INVALID_ARG;
   Params p = base_params(N, T, bootstrap_value);
@@ -337,8 +348,9 @@ rlcs_status rlcs_lambda_returns(const float *rewards, const float *values,
   p.in[kV] = values;
   p.in[kD] = terminateds;
   p.out0 = returns;
-  p.gamma = gamma;
-  p.lambda = lambda;
+  p.gamma = (float)gamma;
+  p.lambda = (float)lambda;
+  set_beta(p, gamma * lambda);
   void *outs[1] = {returns};
   return run(p, truncateds, next_values, outs, 1, workspace, workspace_bytes,
              reinterpret_cast<cudaStream_t>(stream), launch_lambda_returns, truncateds != nullptr);
@@ -347,14 +359,15 @@ rlcs_status rlcs_lambda_returns(const float *rewards, const float *values,
 rlcs_status rlcs_discounted_returns(const float *rewards, const float *terminateds,
                                     const float *truncateds, const float *next_values,
                                     const float *bootstrap_value, float *returns, int64_t N,
-                                    int64_t T, float gamma, void *workspace,
+                                    int64_t T, double gamma, void *workspace,
                                     size_t workspace_bytes, rlcs_stream_t stream) {
   if (!rewards || !terminateds || !returns) return RLCS_ERR_INVALID_ARG;
   Params p = base_params(N, T, bootstrap_value);
   p.in[kR] = rewards;
   p.in[kD] = terminateds;
   p.out0 = returns;
-  p.gamma = gamma;
+  p.gamma = (float)gamma;
+  set_beta(p, gamma);
   void *outs[1] = {returns};
   return run(p, truncateds, next_values, outs, 1, workspace, workspace_bytes,
              reinterpret_cast<cudaStream_t>(stream), launch_discounted_returns, truncateds != nullptr);
@@ -363,8 +376,8 @@ rlcs_status rlcs_discounted_returns(const float *rewards, const float *terminate
 rlcs_status rlcs_vtrace(const float *rewards, const float *values, const float *log_rhos,
                         const float *terminateds, const float *truncateds,
                         const float *next_values, const float *bootstrap_value, float *vs,
-                        float *pg_advantages, int64_t N, int64_t T, float gamma, float lambda,
-                        float rho_bar, float c_bar, void *workspace, size_t workspace_bytes,
+                        float *pg_advantages, int64_t N, int64_t T, double gamma, double lambda,
+                        double rho_bar, double c_bar, void *workspace, size_t workspace_bytes,
                         rlcs_stream_t stream) {
   if (!rewards || !values || !log_rhos || !terminateds || !vs) return RLCS_ERR_INVALID_ARG;
   Params p = base_params(N, T, bootstrap_value);
@@ -374,10 +387,10 @@ rlcs_status rlcs_vtrace(const float *rewards, const float *values, const float *
   p.in[kD] = terminateds;
   p.out0 = vs;
   p.out1 = pg_advantages;
-  p.gamma = gamma;
-  p.lambda = lambda;
-  p.rho_bar = rho_bar;
-  p.c_bar = c_bar;
+  p.gamma = (float)gamma;
+  p.lambda = (float)lambda;
+  p.rho_bar = (float)rho_bar;
+  p.c_bar = (float)c_bar;
   void *outs[2] = {vs, pg_advantages};
   return run(p, truncateds, next_values, outs, 2, workspace, workspace_bytes,
              reinterpret_cast<cudaStream_t>(stream), launch_vtrace, truncateds != nullptr);
@@ -387,7 +400,7 @@ rlcs_status rlcs_retrace(const float *rewards, const float *values, const float 
                          const float *log_rhos, const float *terminateds,
                          const float *truncateds, const float *next_values,
                          const float *bootstrap_value, float *q_ret, int64_t N, int64_t T,
-                         float gamma, float lambda, float c_bar, void *workspace,
+                         double gamma, double lambda, double c_bar, void *workspace,
                          size_t workspace_bytes, rlcs_stream_t stream) {
   if (!rewards || !values || !q_values || !log_rhos || !terminateds || !q_ret)
     return RLCS_ERR_INVALID_ARG;
@@ -398,24 +411,25 @@ rlcs_status rlcs_retrace(const float *rewards, const float *values, const float 
   p.in[kLR] = log_rhos;
   p.in[kD] = terminateds;
   p.out0 = q_ret;
-  p.gamma = gamma;
-  p.lambda = lambda;
-  p.c_bar = c_bar;
+  p.gamma = (float)gamma;
+  p.lambda = (float)lambda;
+  p.c_bar = (float)c_bar;
   void *outs[1] = {q_ret};
   return run(p, truncateds, next_values, outs, 1, workspace, workspace_bytes,
              reinterpret_cast<cudaStream_t>(stream), launch_retrace, truncateds != nullptr);
 }
 
 rlcs_status rlcs_eligibility_traces(const float *x, const float *dones, float *traces, int64_t N,
-                                    int64_t T, float gamma, float lambda, void *workspace,
+                                    int64_t T, double gamma, double lambda, void *workspace,
                                     size_t workspace_bytes, rlcs_stream_t stream) {
   if (!x || !dones || !traces) return RLCS_ERR_INVALID_ARG;
   Params p = base_params(N, T, nullptr);
   p.in[kR] = x;
   p.in[kD] = dones;
   p.out0 = traces;
-  p.gamma = gamma;
-  p.lambda = lambda;
+  p.gamma = (float)gamma;
+  p.lambda = (float)lambda;
+  set_beta(p, gamma * lambda);
   void *outs[1] = {traces};
   return run(p, nullptr, nullptr, outs, 1, workspace, workspace_bytes,
              reinterpret_cast<cudaStream_t>(stream), launch_eligibility_traces, false);
@@ -440,8 +454,8 @@ extern "C" rlcs_status rlcs_gae_and_returns(const float *rewards, const float *v
                                             const float *terminateds, const float *truncateds,
                                             const float *next_values,
                                             const float *bootstrap_value, float *advantages,
-                                            float *returns, int64_t N, int64_t T, float gamma,
-                                            float lambda, void *workspace,
+                                            float *returns, int64_t N, int64_t T, double gamma,
+                                            double lambda, void *workspace,
                                             size_t workspace_bytes, rlcs_stream_t stream) {
   if (!rewards || !values || !terminateds || !advantages || !returns) return RLCS_ERR_INVALID_ARG;
   Params p = base_params(N, T, bootstrap_value);
@@ -450,8 +464,9 @@ extern "C" rlcs_status rlcs_gae_and_returns(const float *rewards, const float *v
   p.in[kD] = terminateds;
   p.out0 = advantages;
   p.out1 = returns;
-  p.gamma = gamma;
-  p.lambda = lambda;
+  p.gamma = (float)gamma;
+  p.lambda = (float)lambda;
+  set_beta(p, gamma * lambda);
   void *outs[2] = {advantages, returns};
   return run(p, truncateds, next_values, outs, 2, workspace, workspace_bytes,
              reinterpret_cast<cudaStream_t>(stream), launch_gae_and_returns,
@@ -462,7 +477,7 @@ extern "C" rlcs_status rlcs_gae_compact(const uint16_t *rewards, const uint16_t 
                                         const uint8_t *terminateds, const uint8_t *truncateds,
                                         const uint16_t *next_values,
                                         const float *bootstrap_value, float *advantages,
-                                        int64_t N, int64_t T, float gamma, float lambda,
+                                        int64_t N, int64_t T, double gamma, double lambda,
                                         void *workspace, size_t workspace_bytes,
                                         rlcs_stream_t stream) {
   if (!rewards || !values || !terminateds || !advantages) return RLCS_ERR_INVALID_ARG;
@@ -471,8 +486,9 @@ extern "C" rlcs_status rlcs_gae_compact(const uint16_t *rewards, const uint16_t 
   p.in[kV] = reinterpret_cast<const float *>(values);
   p.in[kD] = reinterpret_cast<const float *>(terminateds);
   p.out0 = advantages;
-  p.gamma = gamma;
-  p.lambda = lambda;
+  p.gamma = (float)gamma;
+  p.lambda = (float)lambda;
+  set_beta(p, gamma * lambda);
   void *outs[1] = {advantages};
   static const int esize[kNumSlots] = {2, 2, 4, 4, 1, 1, 2};  // R V Q LR D Tau NV
   return run(p, reinterpret_cast<const float *>(truncateds),
@@ -506,7 +522,7 @@ extern "C" {
 rlcs_status rlcs_gae_tm(const float *rewards, const float *values, const float *terminateds,
                         const float *truncateds, const float *next_values,
                         const float *bootstrap_value, float *advantages, int64_t N, int64_t T,
-                        float gamma, float lambda, void *workspace, size_t workspace_bytes,
+                        double gamma, double lambda, void *workspace, size_t workspace_bytes,
                         rlcs_stream_t stream) {
   TimeMajorScope tm;
   return rlcs_gae(rewards, values, terminateds, truncateds, next_values, bootstrap_value,
@@ -516,8 +532,8 @@ rlcs_status rlcs_gae_tm(const float *rewards, const float *values, const float *
 rlcs_status rlcs_lambda_returns_tm(const float *rewards, const float *values,
                                    const float *terminateds, const float *truncateds,
                                    const float *next_values, const float *bootstrap_value,
-                                   float *returns, int64_t N, int64_t T, float gamma,
-                                   float lambda, void *workspace, size_t workspace_bytes,
+                                   float *returns, int64_t N, int64_t T, double gamma,
+                                   double lambda, void *workspace, size_t workspace_bytes,
                                    rlcs_stream_t stream) {
   TimeMajorScope tm;
   return rlcs_lambda_returns(rewards, values, terminateds, truncateds, next_values,
@@ -528,7 +544,7 @@ rlcs_status rlcs_lambda_returns_tm(const float *rewards, const float *values,
 rlcs_status rlcs_discounted_returns_tm(const float *rewards, const float *terminateds,
                                        const float *truncateds, const float *next_values,
                                        const float *bootstrap_value, float *returns, int64_t N,
-                                       int64_t T, float gamma, void *workspace,
+                                       int64_t T, double gamma, void *workspace,
                                        size_t workspace_bytes, rlcs_stream_t stream) {
   TimeMajorScope tm;
   return rlcs_discounted_returns(rewards, terminateds, truncateds, next_values, bootstrap_value,
@@ -538,8 +554,8 @@ rlcs_status rlcs_discounted_returns_tm(const float *rewards, const float *termin
 rlcs_status rlcs_vtrace_tm(const float *rewards, const float *values, const float *log_rhos,
                            const float *terminateds, const float *truncateds,
                            const float *next_values, const float *bootstrap_value, float *vs,
-                           float *pg_advantages, int64_t N, int64_t T, float gamma,
-                           float lambda, float rho_bar, float c_bar, void *workspace,
+                           float *pg_advantages, int64_t N, int64_t T, double gamma,
+                           double lambda, double rho_bar, double c_bar, void *workspace,
                            size_t workspace_bytes, rlcs_stream_t stream) {
   TimeMajorScope tm;
   return rlcs_vtrace(rewards, values, log_rhos, terminateds, truncateds, next_values,
@@ -551,7 +567,7 @@ rlcs_status rlcs_retrace_tm(const float *rewards, const float *values, const flo
                             const float *log_rhos, const float *terminateds,
                             const float *truncateds, const float *next_values,
                             const float *bootstrap_value, float *q_ret, int64_t N, int64_t T,
-                            float gamma, float lambda, float c_bar, void *workspace,
+                            double gamma, double lambda, double c_bar, void *workspace,
                             size_t workspace_bytes, rlcs_stream_t stream) {
   TimeMajorScope tm;
   return rlcs_retrace(rewards, values, q_values, log_rhos, terminateds, truncateds, next_values,
@@ -560,7 +576,7 @@ rlcs_status rlcs_retrace_tm(const float *rewards, const float *values, const flo
 }
 
 rlcs_status rlcs_eligibility_traces_tm(const float *x, const float *dones, float *traces,
-                                       int64_t N, int64_t T, float gamma, float lambda,
+                                       int64_t N, int64_t T, double gamma, double lambda,
                                        void *workspace, size_t workspace_bytes,
                                        rlcs_stream_t stream) {
   TimeMajorScope tm;
@@ -579,7 +595,7 @@ rlcs_status rlcs_gae_and_returns_tm(const float *rewards, const float *values,
                                     const float *terminateds, const float *truncateds,
                                     const float *next_values, const float *bootstrap_value,
                                     float *advantages, float *returns, int64_t N, int64_t T,
-                                    float gamma, float lambda, void *workspace,
+                                    double gamma, double lambda, void *workspace,
                                     size_t workspace_bytes, rlcs_stream_t stream) {
   TimeMajorScope tm;
   return rlcs_gae_and_returns(rewards, values, terminateds, truncateds, next_values,
@@ -839,8 +855,8 @@ rlcs_status noalloc_scratch(void **out) {
 extern "C" rlcs_status rlcs_gae_noalloc(const float *rewards, const float *values,
                                         const float *terminateds, const float *truncateds,
                                         const float *next_values, const float *bootstrap_value,
-                                        float *advantages, int64_t N, int64_t T, float gamma,
-                                        float lambda, rlcs_stream_t stream) {
+                                        float *advantages, int64_t N, int64_t T, double gamma,
+                                        double lambda, rlcs_stream_t stream) {
   if (!rewards || !values || !terminateds || !advantages || N <= 0 || T <= 0)
     return RLCS_ERR_INVALID_ARG;
   if (rlcs_workspace_bytes(N, T) > kNoAllocBytes) return RLCS_ERR_WORKSPACE;

@@ -9,34 +9,6 @@ TOL = 1e-4          # |gpu - oracle| <= TOL * max(1, |oracle|) for T <= 16384
 TOL_VLONG = 1e-3    # same bound at T = 131072
 
 
-def f32(x):
-    """A float scalar as the C ABI hands it to the kernel: rounded to fp32
-    (round to nearest, as ctypes' c_float does).
-
-    The oracle is given these same values. A float64 oracle given the decimal
-    gamma = 0.997 solves a neighbouring problem: 0.997 is 2.1e-8 away from its
-    nearest fp32 value, and over 16384-step rows without lambda damping that
-    moves the exact discounted returns by up to 1.9e-4 of max(1, |G|), more
-    than the bar. The bar measures the kernel's arithmetic on the inputs it
-    receives, the float arrays and these scalars alike."""
-    return float(np.float32(x))
-
-
-class _OracleAtKernelScalars:
-    """The oracle module with every float scalar argument passed through f32."""
-
-    def __getattr__(self, name):
-        fn = getattr(oracle, name)
-
-        def call(*args, **kw):
-            args = [f32(a) if isinstance(a, float) else a for a in args]
-            kw = {k: (f32(v) if isinstance(v, float) else v) for k, v in kw.items()}
-            return fn(*args, **kw)
-        return call
-
-
-oracle_f32 = _OracleAtKernelScalars()
-
 BACKWARD = ("gae", "lambda_returns", "discounted_returns", "vtrace", "retrace")
 FORWARD = ("eligibility_traces", "episodic_prefix_sum")
 ALL = BACKWARD + FORWARD
@@ -85,8 +57,8 @@ def run_gpu(rl, est, g, prm, trunc):
 def run_oracle(est, src, prm, trunc):
     tr = dict(truncateds=src["truncateds"], next_values=src["next_values"]) if trunc else {}
     B = src.get("bootstrap_value")
-    gm, lm = f32(prm["gamma"]), f32(prm["lambda_"])
-    rho_bar, c_bar = f32(prm["rho_bar"]), f32(prm["c_bar"])
+    gm, lm = prm["gamma"], prm["lambda_"]
+    rho_bar, c_bar = prm["rho_bar"], prm["c_bar"]
     if est == "gae":
         return {"out": oracle.gae(src["rewards"], src["values"], src["terminateds"], gm, lm, B, **tr)}
     if est == "lambda_returns":

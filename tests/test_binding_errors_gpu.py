@@ -11,8 +11,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from synthetic_rollouts import rollout
-from tests.parity_common import TOL, compare, oracle_f32
+from tests.parity_common import TOL, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -107,7 +108,7 @@ def test_one_dimensional_row_and_non_contiguous_inputs(rl, g):
     d, src = g
     got = rl.rlcs_gae(d["rewards"][2], d["values"][2], d["terminateds"][2], 0.99, 0.95)
     assert got.shape == (300,)
-    want = oracle_f32.gae(src["rewards"][2:3], src["values"][2:3], src["terminateds"][2:3],
+    want = oracle.gae(src["rewards"][2:3], src["values"][2:3], src["terminateds"][2:3],
                           0.99, 0.95)
     compare("gae", {"out": got.reshape(1, 300)}, {"out": want}, TOL)
     # a transposed view is made contiguous by the binding before the call
@@ -115,7 +116,7 @@ def test_one_dimensional_row_and_non_contiguous_inputs(rl, g):
     vt = d["values"].T.contiguous().T
     assert not rt.is_contiguous()
     got = rl.rlcs_gae(rt, vt, d["terminateds"], 0.99, 0.95, d["bootstrap_value"])
-    want = oracle_f32.gae(src["rewards"], src["values"], src["terminateds"], 0.99, 0.95,
+    want = oracle.gae(src["rewards"], src["values"], src["terminateds"], 0.99, 0.95,
                           src["bootstrap_value"])
     compare("gae", {"out": got}, {"out": want}, TOL)
     assert np.isfinite(got.cpu().numpy()).all()

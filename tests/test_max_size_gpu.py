@@ -12,8 +12,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from synthetic_rollouts import device_rollout
-from tests.parity_common import TOL, compare, oracle_f32
+from tests.parity_common import TOL, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -57,21 +58,21 @@ def test_row_major_past_two_to_the_31(rl, N, T):
     out = rl.rlcs_gae(g["rewards"], g["values"], g["terminateds"], GAMMA, LAM,
                       g["bootstrap_value"])
     compare("gae", {"out": host(out, rows)},
-            {"out": oracle_f32.gae(r, v, d, GAMMA, LAM, B)}, TOL, " [%dx%d]" % (N, T))
+            {"out": oracle.gae(r, v, d, GAMMA, LAM, B)}, TOL, " [%dx%d]" % (N, T))
     del out, g["values"]
     out = rl.rlcs_discounted_returns(g["rewards"], g["terminateds"], GAMMA, g["bootstrap_value"])
     compare("discounted_returns", {"out": host(out, rows)},
-            {"out": oracle_f32.discounted_returns(r, d, GAMMA, B)}, TOL, " [%dx%d]" % (N, T))
+            {"out": oracle.discounted_returns(r, d, GAMMA, B)}, TOL, " [%dx%d]" % (N, T))
     del out, g["rewards"]
     x = device_rollout(torch, N, T, 9200 + T, 0.0, ("x_int",), dev)["x_int"]
     out = rl.rlcs_episodic_prefix_sum(x, g["terminateds"])
     compare("episodic_prefix_sum", {"out": host(out, rows)},
-            {"out": oracle_f32.episodic_prefix_sum(host(x, rows), d)}, TOL)
+            {"out": oracle.episodic_prefix_sum(host(x, rows), d)}, TOL)
     del out, x
     x = device_rollout(torch, N, T, 9300 + T, 0.0, ("x",), dev)["x"]
     out = rl.rlcs_eligibility_traces(x, g["terminateds"], GAMMA, LAM)
     compare("eligibility_traces", {"out": host(out, rows)},
-            {"out": oracle_f32.eligibility_traces(host(x, rows), d, GAMMA, LAM)}, TOL)
+            {"out": oracle.eligibility_traces(host(x, rows), d, GAMMA, LAM)}, TOL)
     rl.check_all_workspaces()
 
 
@@ -90,12 +91,12 @@ def test_time_major_past_two_to_the_31(rl):
     out = rl.rlcs_gae_tm(g["rewards"], g["values"], g["terminateds"], GAMMA, LAM,
                          g["bootstrap_value"])
     compare("gae", {"out": out[:, envs].T.cpu().numpy()},
-            {"out": oracle_f32.gae(cols["rewards"], cols["values"], cols["terminateds"], GAMMA,
+            {"out": oracle.gae(cols["rewards"], cols["values"], cols["terminateds"], GAMMA,
                                    LAM, B)}, TOL, " [tm %dx%d]" % (T, N))
     del out
     vs, pg = rl.rlcs_vtrace_tm(g["rewards"], g["values"], g["values"], g["terminateds"], GAMMA,
                                LAM, 1.0, 1.0, g["bootstrap_value"])
-    ovs, opg = oracle_f32.vtrace(cols["rewards"], cols["values"], cols["values"],
+    ovs, opg = oracle.vtrace(cols["rewards"], cols["values"], cols["values"],
                                  cols["terminateds"], GAMMA, LAM, 1.0, 1.0, B)
     compare("vtrace", {"vs": vs[:, envs].T.cpu().numpy(), "pg": pg[:, envs].T.cpu().numpy()},
             {"vs": ovs, "pg": opg}, TOL, " [tm %dx%d]" % (T, N))

@@ -11,8 +11,9 @@ Same bar as the estimators: |gpu - oracle| <= 1e-4 * max(1, |oracle|)
 import pytest
 import torch
 
+import oracle
 from synthetic_rollouts import WORKLOADS, affine_inputs, rollout, workload_inputs
-from tests.parity_common import TOL, TOL_VLONG, compare, oracle_f32, params_of, to_dev
+from tests.parity_common import TOL, TOL_VLONG, compare, params_of, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -33,9 +34,9 @@ def _fused(rl, src, g, prm, trunc, tol):
     trn = dict(truncateds=src["truncateds"], next_values=src["next_values"]) if trunc else {}
     adv, ret = rl.rlcs_gae_and_returns(g["rewards"], g["values"], g["terminateds"],
                                        prm["gamma"], prm["lambda_"], g["bootstrap_value"], **tr)
-    compare("gae", {"out": adv}, {"out": oracle_f32.gae(src["rewards"], src["values"],
+    compare("gae", {"out": adv}, {"out": oracle.gae(src["rewards"], src["values"],
             src["terminateds"], prm["gamma"], prm["lambda_"], src["bootstrap_value"], **trn)}, tol)
-    compare("lambda_returns", {"out": ret}, {"out": oracle_f32.lambda_returns(
+    compare("lambda_returns", {"out": ret}, {"out": oracle.lambda_returns(
         src["rewards"], src["values"], src["terminateds"], prm["gamma"], prm["lambda_"],
         src["bootstrap_value"], **trn)}, tol)
     rl.check_all_workspaces()
@@ -69,7 +70,7 @@ def _affine(rl, N, T, seed, reverse, with_reset, with_init, tol=TOL, offset=0):
     rs = g["reset"] if with_reset else None
     x0 = g["x_init"] if with_init else None
     got = rl.rlcs_affine_scan(g["a"], g["b"], rs, x0, reverse=reverse)
-    want = oracle_f32.affine_scan(src["a"], src["b"], src["reset"] if with_reset else None,
+    want = oracle.affine_scan(src["a"], src["b"], src["reset"] if with_reset else None,
                               src["x_init"] if with_init else None, reverse=reverse)
     compare("affine_scan", {"out": got}, {"out": want}, tol)
     rl.check_all_workspaces()
@@ -110,7 +111,7 @@ def _compact(rl, N, T, seed, trunc, offset=0):
                               g["bootstrap_value"], **kw)
     kwn = dict(truncateds=f32["truncateds"], next_values=f32["next_values"]) if trunc else {}
     # the oracle sees exactly the values the compact arrays encode
-    want = oracle_f32.gae(f32["rewards"], f32["values"], f32["terminateds"], 0.99, 0.95,
+    want = oracle.gae(f32["rewards"], f32["values"], f32["terminateds"], 0.99, 0.95,
                       f32["bootstrap_value"], **kwn)
     compare("gae", {"out": got}, {"out": want}, TOL)
     rl.check_all_workspaces()

@@ -14,8 +14,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from synthetic_rollouts import affine_inputs, rollout
-from tests.parity_common import TOL, TOL_VLONG, compare, oracle_f32
+from tests.parity_common import TOL, TOL_VLONG, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -51,24 +52,24 @@ def test_backward_estimators_time_major(rl, N, T, trunc):
     rn, vn, dn = src["rewards"], src["values"], src["terminateds"]
     gm, lm = PRM["gamma"], PRM["lambda_"]
     compare("gae", {"out": back(rl.rlcs_gae_tm(r, v, d, gm, lm, B, **kw))},
-            {"out": oracle_f32.gae(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
+            {"out": oracle.gae(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
     compare("lambda_returns", {"out": back(rl.rlcs_lambda_returns_tm(r, v, d, gm, lm, B, **kw))},
-            {"out": oracle_f32.lambda_returns(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
+            {"out": oracle.lambda_returns(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
     compare("discounted_returns",
             {"out": back(rl.rlcs_discounted_returns_tm(r, d, gm, B, **kw))},
-            {"out": oracle_f32.discounted_returns(rn, dn, gm, Bn, **kwn)}, TOL)
+            {"out": oracle.discounted_returns(rn, dn, gm, Bn, **kwn)}, TOL)
     vs, pg = rl.rlcs_vtrace_tm(r, v, g["log_rhos"], d, gm, lm, 1.0, 1.0, B, **kw)
-    ovs, opg = oracle_f32.vtrace(rn, vn, src["log_rhos"], dn, gm, lm, 1.0, 1.0, Bn, **kwn)
+    ovs, opg = oracle.vtrace(rn, vn, src["log_rhos"], dn, gm, lm, 1.0, 1.0, Bn, **kwn)
     compare("vtrace", {"vs": back(vs), "pg": back(pg)}, {"vs": ovs, "pg": opg}, TOL)
     compare("retrace",
             {"out": back(rl.rlcs_retrace_tm(r, v, g["q_values"], g["log_rhos"], d, gm, lm, 1.0,
                                             B, **kw))},
-            {"out": oracle_f32.retrace(rn, vn, src["q_values"], src["log_rhos"], dn, gm, lm, 1.0,
+            {"out": oracle.retrace(rn, vn, src["q_values"], src["log_rhos"], dn, gm, lm, 1.0,
                                    Bn, **kwn)}, TOL)
     adv, ret = rl.rlcs_gae_and_returns_tm(r, v, d, gm, lm, B, **kw)
-    compare("gae", {"out": back(adv)}, {"out": oracle_f32.gae(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
+    compare("gae", {"out": back(adv)}, {"out": oracle.gae(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
     compare("lambda_returns", {"out": back(ret)},
-            {"out": oracle_f32.lambda_returns(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
+            {"out": oracle.lambda_returns(rn, vn, dn, gm, lm, Bn, **kwn)}, TOL)
 
 
 @pytest.mark.parametrize("N,T", SIZES)
@@ -77,9 +78,9 @@ def test_forward_estimators_time_major(rl, N, T):
     d = tm(src["terminateds"])
     got = back(rl.rlcs_eligibility_traces_tm(tm(src["x"]), d, 0.9, 0.8))
     compare("eligibility_traces", {"out": got},
-            {"out": oracle_f32.eligibility_traces(src["x"], src["terminateds"], 0.9, 0.8)}, TOL)
+            {"out": oracle.eligibility_traces(src["x"], src["terminateds"], 0.9, 0.8)}, TOL)
     got = back(rl.rlcs_episodic_prefix_sum_tm(tm(src["x_int"]), d))
-    assert np.array_equal(got, oracle_f32.episodic_prefix_sum(src["x_int"], src["terminateds"]))
+    assert np.array_equal(got, oracle.episodic_prefix_sum(src["x_int"], src["terminateds"]))
 
 
 @pytest.mark.parametrize("N,T", SIZES)
@@ -88,7 +89,7 @@ def test_affine_scan_time_major(rl, N, T, reverse):
     src = affine_inputs(N, T, 13000 + N + T)
     got = back(rl.rlcs_affine_scan_tm(tm(src["a"]), tm(src["b"]), tm(src["reset"]),
                                       torch.from_numpy(src["x_init"]).cuda(), reverse=reverse))
-    want = oracle_f32.affine_scan(src["a"], src["b"], src["reset"], src["x_init"], reverse=reverse)
+    want = oracle.affine_scan(src["a"], src["b"], src["reset"], src["x_init"], reverse=reverse)
     compare("affine_scan", {"out": got}, {"out": want}, TOL)
 
 
@@ -99,12 +100,12 @@ def test_very_long_time_major_rows(rl):
     g = {k: (tm(v) if v.ndim == 2 else torch.from_numpy(v).cuda()) for k, v in src.items()}
     got = back(rl.rlcs_gae_tm(g["rewards"], g["values"], g["terminateds"], 0.999, 1.0,
                               g["bootstrap_value"]))
-    want = oracle_f32.gae(src["rewards"], src["values"], src["terminateds"], 0.999, 1.0,
+    want = oracle.gae(src["rewards"], src["values"], src["terminateds"], 0.999, 1.0,
                       src["bootstrap_value"])
     compare("gae", {"out": got}, {"out": want}, TOL_VLONG)
     vs, pg = rl.rlcs_vtrace_tm(g["rewards"], g["values"], g["log_rhos"], g["terminateds"],
                                0.999, 1.0, 1.0, 1.0, g["bootstrap_value"])
-    ovs, opg = oracle_f32.vtrace(src["rewards"], src["values"], src["log_rhos"], src["terminateds"],
+    ovs, opg = oracle.vtrace(src["rewards"], src["values"], src["log_rhos"], src["terminateds"],
                              0.999, 1.0, 1.0, 1.0, src["bootstrap_value"])
     compare("vtrace", {"vs": back(vs), "pg": back(pg)}, {"vs": ovs, "pg": opg}, TOL_VLONG)
 
@@ -118,7 +119,7 @@ def test_time_major_repeat_calls(rl):
     src = rollout(N, T, 15000, p_term=0.01, p_trunc=0.005)
     g = {k: (tm(v) if v.ndim == 2 else torch.from_numpy(v).cuda()) for k, v in src.items()}
     kw = dict(truncateds=g["truncateds"], next_values=g["next_values"])
-    want = oracle_f32.retrace(src["rewards"], src["values"], src["q_values"], src["log_rhos"],
+    want = oracle.retrace(src["rewards"], src["values"], src["q_values"], src["log_rhos"],
                           src["terminateds"], 0.99, 0.95, 1.0, src["bootstrap_value"],
                           truncateds=src["truncateds"], next_values=src["next_values"])
     for _ in range(3):
@@ -149,7 +150,7 @@ def test_time_major_cuda_graph_capture_and_replay(rl):
     with torch.cuda.graph(graph, stream=s):
         rl.rlcs_gae_tm(g["rewards"], g["values"], g["terminateds"], 0.99, 0.95,
                        g["bootstrap_value"], out=out, stream=s, **kw)
-    want = oracle_f32.gae(src["rewards"], src["values"], src["terminateds"], 0.99, 0.95,
+    want = oracle.gae(src["rewards"], src["values"], src["terminateds"], 0.99, 0.95,
                       src["bootstrap_value"], truncateds=src["truncateds"],
                       next_values=src["next_values"])
     for _ in range(4):

@@ -33,7 +33,7 @@ def lib():
     import linear_recurrence_scan_affine_gb300 as rl
     rl.rlcs_set_shape_override(rl.RLCS_SHAPE_AUTO, 0)
     c = rl.lib()
-    P, I64, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float
+    P, I64, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_double
     c.rlcs_gae_noalloc.argtypes = [P] * 7 + [I64, I64, F, F, P]
     c.rlcs_gae_noalloc.restype = ctypes.c_int
     return rl, c
