@@ -280,3 +280,15 @@ def test_extreme_ratios_and_magnitudes(rl, dev, N, T, bars):
             want = {k: v / scale for k, v in run_oracle(est, src, prm, trunc).items()}
             compare(est, got, want, TOL, " [%dx%d %s]" % (N, T, bars))
     rl.check_all_workspaces()
+
+
+def test_undamped_long_horizons(rl, dev):
+    """lambda = 1 and gamma = 0.997 over 16384 steps: GAE, TD(lambda) returns
+    and traces then have the horizon of discounted returns (about 333 steps
+    with no damping), where rounding the multiplier's powers in fp32 would
+    add up."""
+    src = rollout(64, 16384, 6100, p_term=0.001, p_trunc=0.0005)
+    prm = dict(gamma=0.997, lambda_=1.0, rho_bar=1.0, c_bar=1.0)
+    check_all(rl, src, to_dev(src, dev), prm,
+              ("gae", "lambda_returns", "discounted_returns", "eligibility_traces"), True,
+              tag=" [undamped]")

@@ -160,3 +160,29 @@ def test_time_major_cuda_graph_capture_and_replay(rl):
         torch.cuda.synchronize()
         compare("gae", {"out": back(out)}, {"out": want}, TOL)
     rl.check_all_workspaces()
+
+
+@pytest.mark.parametrize("name", ["longT_256x4096", "longT_256x16384"])
+def test_time_major_long_row_recipes(rl, name):
+    # the long-row recipes with their own scalars (gamma = 0.997, lambda = 0.95),
+    # stored time-major
+    from synthetic_rollouts import WORKLOADS, workload_inputs
+    w = WORKLOADS[name]
+    src = workload_inputs(w)
+    g = {k: (tm(v) if v.ndim == 2 else torch.from_numpy(v).cuda()) for k, v in src.items()}
+    gm, lm, B, Bn = w.gamma, w.lambda_, g["bootstrap_value"], src["bootstrap_value"]
+    r, v, d = g["rewards"], g["values"], g["terminateds"]
+    rn, vn, dn = src["rewards"], src["values"], src["terminateds"]
+    compare("discounted_returns", {"out": back(rl.rlcs_discounted_returns_tm(r, d, gm, B))},
+            {"out": oracle.discounted_returns(rn, dn, gm, Bn)}, TOL)
+    compare("gae", {"out": back(rl.rlcs_gae_tm(r, v, d, gm, lm, B))},
+            {"out": oracle.gae(rn, vn, dn, gm, lm, Bn)}, TOL)
+    compare("lambda_returns", {"out": back(rl.rlcs_lambda_returns_tm(r, v, d, gm, lm, B))},
+            {"out": oracle.lambda_returns(rn, vn, dn, gm, lm, Bn)}, TOL)
+    vs, pg = rl.rlcs_vtrace_tm(r, v, g["log_rhos"], d, gm, lm, 1.0, 1.0, B)
+    ovs, opg = oracle.vtrace(rn, vn, src["log_rhos"], dn, gm, lm, 1.0, 1.0, Bn)
+    compare("vtrace", {"vs": back(vs), "pg": back(pg)}, {"vs": ovs, "pg": opg}, TOL)
+    compare("eligibility_traces",
+            {"out": back(rl.rlcs_eligibility_traces_tm(tm(src["x"]), d, gm, lm))},
+            {"out": oracle.eligibility_traces(src["x"], dn, gm, lm)}, TOL)
+    rl.check_all_workspaces()
