@@ -787,6 +787,12 @@ extern "C" rlcs_status rlcs_run_group(const rlcs_call *calls, int n_calls, void 
       }
       gp.first_block[gp.n] = blocks;
       for (int c = 0; c < gp.n; ++c) gp.ts[c].total_tiles = chained;  // finish_launch count
+      // round-major block order when every call has the same rows and tiles
+      // per row (see GroupTileParams)
+      bool uniform = gp.n > 1;
+      for (int c = 1; c < gp.n && uniform; ++c)
+        uniform = gp.p[c].N == gp.p[0].N && gp.ts[c].tiles_per_row == gp.ts[0].tiles_per_row;
+      gp.round_rows = (uniform && gp.ts[0].tiles_per_row > 1) ? gp.p[0].N : 0;
       if (blocks >= (int64_t)INT32_MAX) return RLCS_ERR_INVALID_ARG;
       err = launch_group_tiles(gp, lead.S, lead.trunc, s);
     }
