@@ -1,4 +1,4 @@
-// The two launch shapes of the scan, templated on an estimator functor.
+// The launch shapes of the scan, templated on an estimator functor.
 //
 // Data layout on chip ("strip-major"): a warp walks its span of a row in
 // strips of 128 steps; in strip j lane l owns the four consecutive steps
@@ -7,16 +7,23 @@
 // sub-scan), a 5-round shuffle scan composes the lanes, and the strips of a
 // warp are chained by their totals.
 //
-//  * warp_row_kernel    one warp per row (T <= 128*S): inputs go straight
-//                       to registers with 128-bit loads; no shared memory.
-//  * block_chunk_kernel one 256-thread block per row chunk of 1024*S steps:
-//                       the chunk's inputs are staged into shared memory by
-//                       cp.async.bulk (1-D TMA) completing on an mbarrier;
-//                       warp aggregates are composed in shared memory; the
-//                       chunks of one row are chained in a single pass by
-//                       decoupled look-back through the workspace
-//                       (ticket-ordered chunks, epoch-tagged flags, bounded
-//                       waits).
+//  * warp_row_kernel    one warp per row (T <= 512): inputs go straight to
+//                       registers with 128-bit loads; no shared memory.
+//  * block_tile_kernel  the default for longer rows: one 256-thread block per
+//                       row tile of 1024*S steps, inputs in registers, warp
+//                       aggregates composed in shared memory, the tiles of a
+//                       row chained in a single pass by a decoupled look-back
+//                       through the workspace (self-validating 64-bit
+//                       records, epoch tags, bounded waits), tiles in
+//                       row-interleaved order.
+//  * block_chunk_kernel the selectable alternative: chunks staged into shared
+//                       memory by cp.async.bulk (1-D TMA) completing on an
+//                       mbarrier, chained in ticket order.
+//  * group_row_kernel, group_tile_kernel: several calls in one launch, the
+//                       warp-row or block-tile body per call.
+//  * time_major_kernel, time_major_short_kernel: [T, N] arrays, one
+//                       environment per lane, chunks of 128 steps chained
+//                       by a per-lane look-back (no look-back for T <= 128).
 #pragma once
 
 #include <type_traits>

@@ -1,6 +1,7 @@
 // Scan core: affine pairs, their composition, lane/warp scans and the PTX
-// helpers the block-chunk tier needs (acquire/release flags, mbarrier,
-// cp.async.bulk, globaltimer).
+// helpers the kernels need (relaxed and acquire/release global accesses for
+// the look-back, mbarrier, cp.async.bulk, L2 bulk prefetch, programmatic
+// dependent launch, globaltimer).
 //
 // The recurrence (rl-triton technical summary, Methodology 1):
 //   backward  A_t = alpha_t + beta_t * A_{t+1}
