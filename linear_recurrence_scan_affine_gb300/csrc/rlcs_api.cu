@@ -614,7 +614,8 @@ rlcs_status rlcs_affine_scan_tm(const float *a, const float *b, const float *res
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
-// Grouped calls on short rows: one launch per (strips, optional inputs) class.
+// Grouped calls: one launch per class (short rows by strips and optional inputs,
+// long rows by tile length and optional inputs).
 // ---------------------------------------------------------------------------
 namespace rlcs {
 namespace {
