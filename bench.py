@@ -13,7 +13,13 @@ Also reported: every estimator alone (graph of back-to-back launches on
 rotating buffers), the roofline of the dominant kernel against the measured
 HBM copy bandwidth, an end-to-end figure through host buffers (pinned H2D
 copies + kernels + D2H copies per step), SM clocks sampled during the timed
-region, and the float64 CPU oracle timed on the host cores as a baseline.
+region, and the float64 CPU oracle timed on the host cores as a baseline
+(all cores and one thread). The long-row sweep (256 x {1024, 4096, 16384},
+8 x 131072) times each estimator alone and each workload's estimators as one
+step in several schedules (seven streams, one stream, one rlcs_run_group
+call, 2 or 3 groups on their own streams), keeping the fastest; the extra
+entry points (fused GAE + returns, affine scan, compact GAE, the time-major
+estimators) are timed alone at 4096 x 128 and 256 x 16384.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
