@@ -286,3 +286,19 @@ def test_group_validation(lib):
     assert _group(lib, [_call("gae", **gae),
                         _call("discounted_returns", rewards=a[5], terminateds=a[7],
                               out=inner)]) == INVALID
+
+
+def test_device_rollout_draws_the_named_fields():
+    # the generator the size tests use on the GPU, exercised on the host
+    import torch
+    from synthetic_rollouts import device_rollout
+    g = device_rollout(torch, 5, 7, 3, 0.3, ("rewards", "terminateds", "x_int", "bootstrap_value"),
+                       "cpu")
+    assert g["rewards"].shape == (5, 7) and g["rewards"].dtype == torch.float32
+    assert g["x_int"].dtype == torch.int32 and int(g["x_int"].abs().max()) <= 100
+    assert set(g["terminateds"].unique().tolist()) <= {0.0, 1.0}
+    assert g["bootstrap_value"].shape == (5,)
+    tm = device_rollout(torch, 5, 7, 3, 0.3, ("rewards",), "cpu", time_major=True)
+    assert tm["rewards"].shape == (7, 5)
+    again = device_rollout(torch, 5, 7, 3, 0.3, ("rewards",), "cpu")
+    assert torch.equal(again["rewards"], g["rewards"])  # seeded

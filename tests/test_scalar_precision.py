@@ -44,3 +44,12 @@ def test_binding_passes_the_scalars_as_double():
     from linear_recurrence_scan_affine_gb300.binding import RlcsCall
     assert all(t is ctypes.c_double for f, t in RlcsCall._fields_
                if f in ("gamma", "lambda_", "rho_bar", "c_bar"))
+
+
+def test_header_declares_no_fp32_scalars():
+    import os
+    import re
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                            "include", "rlcs.h")).read()
+    assert not re.search(r"\bfloat\s+(gamma|lambda|rho_bar|c_bar)\b", hdr)
+    assert re.search(r"\bdouble\s+gamma\b", hdr)
