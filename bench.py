@@ -6,22 +6,25 @@ Retrace(lambda), eligibility traces and the episodic prefix sum, each on its
 own inputs (so no kernel reads another's data out of L2). value = env-steps
 per second with all seven outputs produced for every (env, t).
 
-Timing: CUDA graphs of the step's launches, replayed over 8 rotating sets of
-input/output buffers whose footprint is several times the L2, CUDA events on
+Timing: exactly --warmup untimed steps, then exactly --steps timed steps,
+replayed from CUDA graphs of whole steps over 8 rotating sets of
+input/output buffers whose footprint is several times the L2; CUDA events on
 the launching stream, barrier + synchronize on both sides, max over ranks.
-Also reported: every estimator alone (graph of back-to-back launches on
-rotating buffers), the roofline of the dominant kernel against the measured
-HBM copy bandwidth, an end-to-end figure through host buffers (pinned H2D
-copies + kernels + D2H copies per step), SM clocks sampled during the timed
-region, and the float64 CPU oracle timed on the host cores as a baseline
-(all cores and one thread). The long-row sweep (256 x {1024, 4096, 16384},
-8 x 131072) times each estimator alone and each workload's estimators as one
-step in several schedules (seven streams, one stream, one rlcs_run_group
-call, 2 or 3 groups on their own streams), keeping the fastest; the extra
-entry points (fused GAE + returns, affine scan, compact GAE, the time-major
-estimators) are timed alone at 4096 x 128 and 256 x 16384.
+A device-side delay queued before the start event lets the host enqueue the
+replays ahead, so host launch gaps do not enter the timed region.
+
+stdout gets ONE compact JSON line (the headline: value, roofline of the
+dominant kernel against the measured HBM copy bandwidth, the float64 CPU
+oracle as a baseline, an end-to-end figure through pinned host buffers, SM
+clocks sampled during the timed region). Everything else goes to the JSON
+file named by --detail: every estimator alone, the step in several schedules
+(seven streams, one stream, one rlcs_run_group call, 2 or 3 groups on their
+own streams), GAE at 64 x 512, the five truncated estimators at 4096 x 128,
+the long-row sweep (256 x {1024, 4096, 16384}, 8 x 131072) and the extra
+entry points (fused GAE + returns, affine scan, compact GAE, time-major).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--detail PATH] [--no-long-t]
 
 Under torchrun each rank processes its own batch (rows are independent: weak
 scaling, no collective on the data path).
@@ -63,6 +66,12 @@ ESTIMATORS = {
 }
 BACKWARD = ("gae", "lambda_returns", "discounted_returns", "vtrace", "retrace")
 
+# The five backward estimators with truncation inputs (a truncated step
+# bootstraps from next_values[t]): the same calls, 8 more bytes per step.
+TRUNC_IN = ("truncateds", "next_values")
+TRUNCATED = {est + "_trunc": (ESTIMATORS[est][0] + TRUNC_IN, ESTIMATORS[est][1])
+             for est in BACKWARD}
+
 # Entry points beyond the seven (timed alone, reported under "next_rows").
 EXTRA = {
     "gae_and_returns": (("rewards", "values", "terminateds"), ("out", "out2")),
@@ -72,9 +81,17 @@ EXTRA = {
 # The seven on time-major [T, N] arrays (the _tm entry points), same bytes.
 EXTRA.update({est + "_tm": spec for est, spec in ESTIMATORS.items()})
 ELEM_BYTES = {"rewards_bf16": 2, "values_bf16": 2, "terminateds_u8": 1}   # others: 4
-SPECS = dict(ESTIMATORS, **EXTRA)
-ROW_VALUE = BACKWARD + tuple(e + "_tm" for e in BACKWARD) + (
-    "gae_and_returns", "affine_scan", "gae_compact")  # one value per row
+SPECS = dict(ESTIMATORS, **TRUNCATED, **EXTRA)
+ROW_VALUE = BACKWARD + tuple(e + "_trunc" for e in BACKWARD) + tuple(
+    e + "_tm" for e in BACKWARD) + ("gae_and_returns", "affine_scan", "gae_compact")
+
+
+def base_name(est):
+    """The entry point's estimator: gae_trunc -> gae, vtrace_tm -> vtrace."""
+    for suffix in ("_trunc", "_tm"):
+        if est.endswith(suffix):
+            return est[:-len(suffix)]
+    return est
 
 
 def kernel_source_hash():
@@ -300,17 +317,17 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def make_sets(torch, rl, src, dev, nsets):
+def make_sets(torch, rl, src, dev, nsets, ests):
     """nsets independent device copies of every estimator's inputs and outputs."""
     sets = []
     for _ in range(nsets):
         st = {}
-        for est, (ins, outs) in ESTIMATORS.items():
-            e = {k: torch.from_numpy(src[k]).to(dev) for k in ins}
-            e["bootstrap_value"] = torch.from_numpy(src["bootstrap_value"]).to(dev)
-            like = e[ins[0]]
+        for est in ests:
+            ins, outs = SPECS[est]
+            e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + ("bootstrap_value",)}
+            odt = torch.int32 if base_name(est) == "episodic_prefix_sum" else torch.float32
             for o in outs:
-                e[o] = torch.empty_like(like)
+                e[o] = torch.empty(e[ins[0]].shape, dtype=odt, device=dev)
             st[est] = e
         sets.append(st)
     return sets
@@ -318,21 +335,24 @@ def make_sets(torch, rl, src, dev, nsets):
 
 def launch(rl, est, e, prm):
     g, lm = prm["gamma"], prm["lambda_"]
-    tm = est.endswith("_tm")  # the time-major entry point of the same estimator
-    base = est[:-3] if tm else est
-    f = getattr(rl, "rlcs_" + est)
+    base = base_name(est)
+    # the time-major entry point of the same estimator, else the row-major one
+    f = getattr(rl, "rlcs_" + (est if est.endswith("_tm") else base))
+    tr = {k: e[k] for k in TRUNC_IN if k in e}
     if base == "gae":
-        f(e["rewards"], e["values"], e["terminateds"], g, lm, e["bootstrap_value"], out=e["out"])
+        f(e["rewards"], e["values"], e["terminateds"], g, lm, e["bootstrap_value"], out=e["out"],
+          **tr)
     elif base == "lambda_returns":
-        f(e["rewards"], e["values"], e["terminateds"], g, lm, e["bootstrap_value"], out=e["out"])
+        f(e["rewards"], e["values"], e["terminateds"], g, lm, e["bootstrap_value"], out=e["out"],
+          **tr)
     elif base == "discounted_returns":
-        f(e["rewards"], e["terminateds"], g, e["bootstrap_value"], out=e["out"])
+        f(e["rewards"], e["terminateds"], g, e["bootstrap_value"], out=e["out"], **tr)
     elif base == "vtrace":
         f(e["rewards"], e["values"], e["log_rhos"], e["terminateds"], g, lm, prm["rho_bar"],
-          prm["c_bar"], e["bootstrap_value"], out=e["vs"], out_pg=e["pg"])
+          prm["c_bar"], e["bootstrap_value"], out=e["vs"], out_pg=e["pg"], **tr)
     elif base == "retrace":
         f(e["rewards"], e["values"], e["q_values"], e["log_rhos"], e["terminateds"], g, lm,
-          prm["c_bar"], e["bootstrap_value"], out=e["out"])
+          prm["c_bar"], e["bootstrap_value"], out=e["out"], **tr)
     elif base == "eligibility_traces":
         f(e["x"], e["terminateds"], g, lm, out=e["out"])
     elif base == "episodic_prefix_sum":
@@ -352,24 +372,26 @@ def launch(rl, est, e, prm):
 def group_kwargs(est, e, prm):
     """Keyword arguments of rlcs_run_group for one estimator's buffer set."""
     g, lm = prm["gamma"], prm["lambda_"]
-    if est in ("gae", "lambda_returns"):
+    tr = {k: e[k] for k in TRUNC_IN if k in e}
+    base = base_name(est)
+    if base in ("gae", "lambda_returns"):
         return dict(rewards=e["rewards"], values=e["values"], terminateds=e["terminateds"],
-                    gamma=g, lambda_=lm, bootstrap_value=e["bootstrap_value"], out=e["out"])
-    if est == "discounted_returns":
+                    gamma=g, lambda_=lm, bootstrap_value=e["bootstrap_value"], out=e["out"], **tr)
+    if base == "discounted_returns":
         return dict(rewards=e["rewards"], terminateds=e["terminateds"], gamma=g,
-                    bootstrap_value=e["bootstrap_value"], out=e["out"])
-    if est == "vtrace":
+                    bootstrap_value=e["bootstrap_value"], out=e["out"], **tr)
+    if base == "vtrace":
         return dict(rewards=e["rewards"], values=e["values"], log_rhos=e["log_rhos"],
                     terminateds=e["terminateds"], gamma=g, lambda_=lm, rho_bar=prm["rho_bar"],
                     c_bar=prm["c_bar"], bootstrap_value=e["bootstrap_value"], out=e["vs"],
-                    out_pg=e["pg"])
-    if est == "retrace":
+                    out_pg=e["pg"], **tr)
+    if base == "retrace":
         return dict(rewards=e["rewards"], values=e["values"], q_values=e["q_values"],
                     log_rhos=e["log_rhos"], terminateds=e["terminateds"], gamma=g, lambda_=lm,
-                    c_bar=prm["c_bar"], bootstrap_value=e["bootstrap_value"], out=e["out"])
-    if est == "eligibility_traces":
+                    c_bar=prm["c_bar"], bootstrap_value=e["bootstrap_value"], out=e["out"], **tr)
+    if base == "eligibility_traces":
         return dict(x=e["x"], dones=e["terminateds"], gamma=g, lambda_=lm, out=e["out"])
-    if est == "episodic_prefix_sum":
+    if base == "episodic_prefix_sum":
         return dict(x=e["x_int"], dones=e["terminateds"], out=e["out"])
     raise ValueError(est)
 
@@ -414,6 +436,42 @@ def percentile(xs, q):
     return ys[min(len(ys) - 1, max(0, int(round(q * (len(ys) - 1)))))]
 
 
+def replay_plan(n, block):
+    """n steps as (rem, full): one graph of rem steps, then full replays of a
+    graph of `block` steps (rem first, so that every later graph starts on
+    the rotating set after the one the previous graph ended on)."""
+    return n % block, n // block
+
+
+def headline_line(value, ms_per_step, steps, warmup, n_gpus, config, step_gbs, peak, roofline,
+                  cpu, e2e, launches, clocks, detail_path):
+    """The one JSON line the bench prints: the headline and the objects the
+    report needs, a few hundred bytes (the per-estimator and sweep figures go
+    to the detail file)."""
+    def r(x, nd=4):
+        return None if x is None else float("%.*g" % (nd, x))
+    line = {
+        "metric": METRIC, "value": r(value, 6), "unit": UNIT, "n_gpus": n_gpus,
+        "steps": steps, "warmup": warmup, "ms_per_step": r(ms_per_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": config,
+        "hbm_gbs": r(step_gbs), "hbm_frac_of_8tbs": r(step_gbs / NOMINAL_HBM_GBS),
+        "hbm_frac_of_measured": r(step_gbs / peak),
+        "roofline": {k: (r(v) if isinstance(v, float) else v) for k, v in roofline.items()},
+        "cpu_baseline": None if cpu is None else {
+            "value": r(cpu["value"]), "unit": cpu["unit"], "cores": cpu["cores"],
+            "kind": cpu["kind"], "sample": cpu["sample"]},
+        "e2e": {"value": r(e2e["value"]), "unit": e2e["unit"],
+                "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"]},
+        "gpu_launches": launches,
+        "clocks": {"sm_mhz": clocks.get("sm_mhz"), "sm_max_mhz": clocks.get("sm_max_mhz"),
+                   "reasons": clocks.get("reasons", [])},
+        "detail": detail_path,
+    }
+    return json.dumps(line, separators=(",", ":"))
+
+
 def run_ours(args):
     import torch
     world, rank, local = dist_env()
@@ -426,78 +484,77 @@ def run_ours(args):
     N, T = w.N, w.T
     prm = dict(gamma=w.gamma, lambda_=w.lambda_, rho_bar=w.rho_bar, c_bar=w.c_bar)
     src = rollout(N, T, w.seed + rank, w.p_term)
-    sets = make_sets(torch, rl, src, dev, ROTATING_SETS)
+    order = list(ESTIMATORS)
+    sets = make_sets(torch, rl, src, dev, ROTATING_SETS, order)
     footprint = sum(t.numel() * t.element_size() for st in sets for e in st.values()
                     for t in e.values())
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     stream = torch.cuda.Stream(dev)
-    order = list(ESTIMATORS)
-
     # One side stream per estimator: the seven calls of a step are independent,
-    # so the concurrent schedule lets their fixed per-launch latencies overlap.
+    # so this schedule lets their fixed per-launch latencies overlap.
     side = {est: torch.cuda.Stream(dev) for est in order}
 
-    def step(i):
+    def one_step(i):
         st = sets[i % ROTATING_SETS]
-        for est in order:
-            launch(rl, est, st[est], prm)
+        if args.schedule == "grouped":
+            rl.rlcs_run_group([(est, group_kwargs(est, st[est], prm)) for est in order])
+        else:
+            for est in order:
+                launch(rl, est, st[est], prm)
 
-    # eager warm-up on every stream used below: loads the kernels and
-    # allocates each stream's workspace outside any capture
+    def steps_fn(n, start):
+        """Steps start .. start+n-1 (buffer set i % ROTATING_SETS for step i)."""
+        def fn():
+            if args.schedule == "streams":
+                for est in order:
+                    side[est].wait_stream(stream)
+                    with torch.cuda.stream(side[est]):
+                        for i in range(start, start + n):
+                            launch(rl, est, sets[i % ROTATING_SETS][est], prm)
+                for est in order:
+                    stream.wait_stream(side[est])
+            else:
+                for i in range(start, start + n):
+                    one_step(i)
+        return fn
+
+    # Set-up, not steps: one eager call of each estimator on every stream the
+    # graphs use (loads the kernels, creates any workspace outside capture).
     for s_ in [stream] + list(side.values()):
         s_.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(s_):
-            for i in range(ROTATING_SETS):
-                step(i)
+            one_step(0)
     torch.cuda.synchronize()
     rl.check_all_workspaces()
 
-    # one graph = BLOCK steps cycling through the rotating sets
+    # graphs of whole steps; K and W are met exactly by a remainder graph
+    # plus replays of a BLOCK-step graph
     BLOCK = 8 * ROTATING_SETS
+    K, W = max(1, args.steps), max(0, args.warmup)
+    graphs = {}
 
-    def serial_block():
-        for i in range(BLOCK):
-            step(i)
+    def graph(n, start):
+        key = (n, start % ROTATING_SETS)
+        if key not in graphs:
+            graphs[key] = capture(torch, stream, steps_fn(n, key[1]))
+        return graphs[key]
 
-    def concurrent_block():
-        for est in order:
-            side[est].wait_stream(stream)
-            with torch.cuda.stream(side[est]):
-                for i in range(BLOCK):
-                    launch(rl, est, sets[i % ROTATING_SETS][est], prm)
-        for est in order:
-            stream.wait_stream(side[est])
+    def sequence(n, cursor):
+        rem, full = replay_plan(n, BLOCK)
+        seq = []
+        if rem:
+            seq.append(graph(rem, cursor))
+            cursor += rem
+        seq += [graph(BLOCK, cursor)] * full
+        return seq, cursor + full * BLOCK
 
-    # the seven calls of a step as one grouped launch (rlcs_run_group)
-    group_calls = [[(est, group_kwargs(est, sets[i][est], prm)) for est in order]
-                   for i in range(ROTATING_SETS)]
-    with torch.cuda.stream(stream):
-        for i in range(ROTATING_SETS):
-            rl.rlcs_run_group(group_calls[i])
+    warm_seq, cursor = sequence(W, 0)
+    timed_seq, _ = sequence(K, cursor)
     torch.cuda.synchronize()
-
-    def grouped_block():
-        for i in range(BLOCK):
-            rl.rlcs_run_group(group_calls[i % ROTATING_SETS])
-
-    graphs = {"serial": capture(torch, stream, serial_block),
-              "concurrent": capture(torch, stream, concurrent_block),
-              "grouped": capture(torch, stream, grouped_block)}
-    K = max(args.steps, 1)
-    reps = (K + BLOCK - 1) // BLOCK
-    K = reps * BLOCK
-    wreps = max(1, (max(args.warmup, 3) + BLOCK - 1) // BLOCK)
     with torch.cuda.stream(stream):
-        for g_ in graphs.values():
-            for _ in range(wreps):
-                g_.replay()
+        for g_ in warm_seq:
+            g_.replay()
     torch.cuda.synchronize()
-
-    # every schedule timed once; the fastest is timed again as the headline,
-    # with the clocks sampled (the others are reported beside it)
-    sched_sec = {k: time_graph(torch, stream, g_, reps) / K for k, g_ in graphs.items()}
-    serial_sec = sched_sec["serial"]
-    headline = min(("concurrent", "grouped"), key=lambda k: sched_sec[k])
 
     sampler = ClockSampler(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ
                            else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
@@ -509,9 +566,12 @@ def run_ours(args):
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        # a ~1 ms device-side delay ahead of the start event: the host queues
+        # every replay meanwhile, so the timed region holds device work only
+        torch.cuda._sleep(2_000_000)
         t_start.record(stream)
-        for _ in range(reps):
-            graphs[headline].replay()
+        for g_ in timed_seq:
+            g_.replay()
         t_end.record(stream)
     torch.cuda.synchronize()
     if dist is not None:
@@ -520,23 +580,12 @@ def run_ours(args):
     elapsed = t_start.elapsed_time(t_end) / 1e3
     elapsed = max_over_ranks(dist, elapsed, dev)
     rl.check_all_workspaces()
-    del graphs
+    del graphs, warm_seq, timed_seq
 
     step_bytes = sum(bytes_per_launch(e, N, T) for e in order)
     value = world * N * T * K / elapsed
     step_gbs = step_bytes * K / elapsed / 1e9
 
-    # every estimator alone: a graph of back-to-back launches, each on its own
-    # buffer set, with enough sets that the rotation spans >= 3x the L2
-    per_est = {}
-    for est in order:
-        per_est[est] = time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T)
-    # the dominant kernel: the grouped kernel when it is the headline (one
-    # launch per step), else the slowest estimator alone
-    grouped = headline == "grouped"
-    dom = "group" if grouped else max(per_est, key=lambda e: per_est[e]["us_per_launch"])
-    dom_bytes = step_bytes if grouped else bytes_per_launch(dom, N, T)
-    dom_us = 1e6 * elapsed / K if grouped else per_est[dom]["us_per_launch"]
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
@@ -544,9 +593,19 @@ def run_ours(args):
     except (OSError, ValueError):
         pass
     peak = peaks.get("hbm_gbs")
-    peak_src = "measured (MEASURED_PEAKS.json hbm_gbs, copy burst)"
+    peak_src = "measured hbm_gbs (copy burst)"
     if not peak:
         peak, peak_src = 6800.0, "fallback 6.8 TB/s"
+
+    # every estimator alone: a graph of back-to-back launches, each on its own
+    # buffer set, with enough sets that the rotation spans >= 3x the L2
+    per_est = {est: time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T) for est in order}
+    for r_ in per_est.values():
+        r_["frac_of_measured_hbm"] = r_["gbs"] / peak
+    # the dominant kernel: the slowest estimator alone
+    dom = max(per_est, key=lambda e: per_est[e]["us_per_launch"])
+    dom_bytes = bytes_per_launch(dom, N, T)
+    dom_us = per_est[dom]["us_per_launch"]
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tr_path):
@@ -556,41 +615,55 @@ def run_ours(args):
         if tr.get("kernel_source_sha256_16") == kernel_source_hash():
             traffic = tr.get("%s_%dx%d" % (dom, N, T))
     achieved = dom_bytes / (dom_us * 1e-6) / 1e9
-    roofline = {"bound": "hbm",
-                "kernel": ("group_row_kernel: the seven estimators in one launch" if grouped
-                           else dom),
-                "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_src,
-                "traffic": traffic, "bytes_per_launch": dom_bytes, "us_per_launch": dom_us,
-                "us_p10": None if grouped else per_est[dom]["us_p10"],
-                "us_p90": None if grouped else per_est[dom]["us_p90"],
-                "timing": ("the headline's timed region: one grouped launch per step on its "
-                           "own buffer set (rotation >= 3x L2), CUDA events on the launching "
-                           "stream" if grouped else
-                           "kernel alone: CUDA graph of back-to-back launches, each on its own "
-                           "buffer set (rotation >= 3x L2), CUDA events on the launching "
-                           "stream; >= 20 replays")}
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": dom,
+                "bytes_per_launch": dom_bytes, "us_per_launch": dom_us,
+                "peak_source": peak_src}
+    detail = {"per_estimator_4096x128": per_est,
+              "roofline": dict(roofline, timing=(
+                  "kernel alone: CUDA graph of back-to-back launches, each on its own buffer "
+                  "set (rotation >= 3x L2), CUDA events on the launching stream; >= 20 "
+                  "replays"))}
     # what any launch of this size and shape costs: the diagnostic copy of the
-    # same bytes (for the group: 16-byte elements over as many rows as make
-    # the step's bytes), and the same grid doing nothing
-    if grouped:
-        n_arrays, n_rows = 4, step_bytes // (16 * T)
-    else:
-        n_arrays, n_rows = len(SPECS[dom][0]) + len(SPECS[dom][1]), N
-    copy_us = time_diag(torch, rl, n_arrays, dev, stream, l2, n_rows, T, False)
-    empty_us = time_diag(torch, rl, n_arrays, dev, stream, l2, n_rows, T, True)
-    roofline["reference"] = {
+    # same bytes, and the same grid doing nothing
+    n_arrays = len(SPECS[dom][0]) + len(SPECS[dom][1])
+    copy_us = time_diag(torch, rl, n_arrays, dev, stream, l2, N, T, False)
+    empty_us = time_diag(torch, rl, n_arrays, dev, stream, l2, N, T, True)
+    detail["roofline"]["reference"] = {
         "stream_copy_us": copy_us, "empty_launch_us": empty_us,
         "stream_copy_frac": dom_bytes / (copy_us * 1e-6) / 1e9 / peak,
         "kernel_over_copy": dom_us / copy_us,
         "what": "rlcs_diag_stream_copy: the warp-row launch shape moving the same bytes "
                 "(%d arrays x %d rows x %d steps) with no scan (same prefetch and programmatic "
                 "dependent launch); empty = the same grid that only waits and exits"
-                % (n_arrays, n_rows, T)}
+                % (n_arrays, N, T)}
+    # the same step in every schedule
+    detail["schedules_4096x128"] = time_step(torch, rl, order, src, dev, stream, prm, l2, N, T)
+
+    # GAE alone at 64 x 512, and the five truncated estimators at 4096 x 128
+    w1 = WORKLOADS["gae_64x512"]
+    src1 = rollout(w1.N, w1.T, w1.seed, w1.p_term)
+    prm1 = dict(gamma=w1.gamma, lambda_=w1.lambda_, rho_bar=w1.rho_bar, c_bar=w1.c_bar)
+    r_ = time_alone(torch, rl, "gae", src1, dev, stream, prm1, l2, w1.N, w1.T)
+    r_["frac_of_measured_hbm"] = r_["gbs"] / peak
+    detail["gae_64x512"] = r_
+    w3 = WORKLOADS["trunc5_4096x128"]
+    src3 = rollout(w3.N, w3.T, w3.seed, w3.p_term, w3.p_trunc)
+    prm3 = dict(gamma=w3.gamma, lambda_=w3.lambda_, rho_bar=w3.rho_bar, c_bar=w3.c_bar)
+    ests3 = [e + "_trunc" for e in w3.estimators]
+    res3 = {}
+    for est in ests3:
+        r_ = time_alone(torch, rl, est, src3, dev, stream, prm3, l2, w3.N, w3.T)
+        r_["frac_of_measured_hbm"] = r_["gbs"] / peak
+        res3[est] = r_
+    step3 = time_step(torch, rl, ests3, src3, dev, stream, prm3, l2, w3.N, w3.T)
+    step3["frac_of_measured_hbm"] = step3["gbs"] / peak
+    detail["trunc5_4096x128"] = {"alone": res3, "step": step3}
+    del src1, src3
 
     # the long-row recipes, every estimator alone (same method as above)
-    long_t = {}
     if not args.no_long_t:
+        long_t = {}
         for name in ("longT_256x1024", "longT_256x4096", "longT_256x16384", "vlong_8x131072"):
             wl = WORKLOADS[name]
             prm_l = dict(gamma=wl.gamma, lambda_=wl.lambda_, rho_bar=wl.rho_bar, c_bar=wl.c_bar)
@@ -607,11 +680,11 @@ def run_ours(args):
             long_t[name] = {"step": step_l, "alone": res}
             del src_l
         rl.check_all_workspaces()
+        detail["long_t_sweep"] = long_t
 
-    # entry points beyond the seven, alone, at the bench size and one long size
-    next_rows = {}
-    if not args.no_long_t:
+        # entry points beyond the seven, alone, at the bench size and one long size
         from synthetic_rollouts import affine_inputs, compact_rollout
+        next_rows = {}
         for (nN, nT, seed) in ((N, T, w.seed), (256, 16384, 1004)):
             srcn = dict(rollout(nN, nT, seed, w.p_term), **affine_inputs(nN, nT, seed + 7))
             comp, _ = compact_rollout(nN, nT, seed + 9, w.p_term)
@@ -629,49 +702,42 @@ def run_ours(args):
             next_rows["%dx%d" % (nN, nT)] = res
             del srcn, srcn_tm
         rl.check_all_workspaces()
+        detail["next_rows"] = next_rows
 
     e2e = run_e2e(torch, rl, src, dev, stream, prm, order, max(32, min(K, 512)), N, T)
     e2e["value"] *= world
+    detail["e2e"] = e2e
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = time_oracle(src, prm, budget_s=args.cpu_seconds)
+        detail["cpu_baseline"] = cpu
 
     if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-            "warmup": wreps * BLOCK, "ms_per_step": 1e3 * elapsed / K, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "num_envs": N, "seq_len": T, "estimators": 7,
-                       "env_step": "one (env, t) element through all seven estimators",
-                       "bytes_per_step_algorithmic": step_bytes,
-                       "l2": "inputs larger than L2: %d rotating buffer sets, %.0f MB footprint "
-                             "= %.1fx L2" % (ROTATING_SETS, footprint / 1e6, footprint / l2),
-                       "launch": ("CUDA graph of %d steps; each step one rlcs_run_group "
-                                  "call: the seven estimators in one launch, programmatic "
-                                  "dependent launch between steps" % BLOCK if grouped else
-                                  "CUDA graph of %d steps; the seven estimators on seven "
-                                  "streams (fork/join), programmatic dependent launch "
-                                  "within each stream" % BLOCK),
-                       "schedules": {k: {"ms_per_step": v * 1e3,
-                                         "value": world * N * T / v,
-                                         "launches_per_step": 1 if k == "grouped" else 7}
-                                     for k, v in sched_sec.items()},
-                       "schedule_notes": {"serial": "seven rlcs_* calls on one stream",
-                                          "concurrent": "seven rlcs_* calls on seven streams",
-                                          "grouped": "one rlcs_run_group call"},
-                       "serial_schedule": {"ms_per_step": serial_sec * 1e3,
-                                           "value": world * N * T / serial_sec,
-                                           "note": "same steps, all seven calls on one "
-                                                   "stream"},
-                       "parallelism": "weak: each rank its own batch"},
-            "hbm_gbs": step_gbs, "hbm_frac_of_8tbs": step_gbs / NOMINAL_HBM_GBS,
-            "hbm_frac_of_measured": step_gbs / peak,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": (1 if grouped else 7) * K, "clocks": clocks, "per_estimator": per_est,
-            "long_t_sweep": long_t, "next_rows": next_rows,
-        }
-        print(json.dumps(line), flush=True)
+        launches = (1 if args.schedule == "grouped" else len(order)) * K
+        launch_desc = {
+            "streams": "seven rlcs_* calls per step on seven streams (fork/join per graph)",
+            "serial": "seven rlcs_* calls per step on one stream",
+            "grouped": "one rlcs_run_group call per step (the seven in one launch)"}
+        config = {"workload": WORKLOAD, "num_envs": N, "seq_len": T, "estimators": 7,
+                  "bytes_per_step": step_bytes,
+                  "l2": "inputs larger than L2: %d rotating buffer sets, %.0f MB = %.1fx L2"
+                        % (ROTATING_SETS, footprint / 1e6, footprint / l2),
+                  "launch": launch_desc[args.schedule] + "; CUDA graphs of whole steps",
+                  "parallelism": "weak: each rank its own batch"}
+        detail["headline"] = {"schedule": args.schedule, "steps": K, "warmup": W,
+                              "elapsed_s": elapsed, "clocks": clocks, "config": config}
+        detail["kernel_source_sha256_16"] = kernel_source_hash()
+        detail_path = args.detail
+        try:
+            d = os.path.dirname(os.path.abspath(detail_path))
+            os.makedirs(d, exist_ok=True)
+            with open(detail_path, "w") as fh:
+                json.dump(detail, fh, indent=1)
+        except OSError as exc:
+            detail_path = "not written: %s" % exc
+        print(headline_line(value, 1e3 * elapsed / K, K, W, world, config, step_gbs, peak,
+                            roofline, cpu, e2e, launches, clocks, detail_path), flush=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -741,17 +807,7 @@ def time_step(torch, rl, ests, src, dev, stream, prm, l2, N, T, seconds=0.15):
     and the step's algorithmic GB/s."""
     step_bytes = sum(bytes_per_launch(e, N, T) for e in ests)
     nsets = int(min(64, max(2, -(-3 * l2 // step_bytes))))
-    sets = []
-    for _ in range(nsets):
-        st = {}
-        for est in ests:
-            ins, outs = ESTIMATORS[est]
-            e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + ("bootstrap_value",)}
-            odt = torch.int32 if est == "episodic_prefix_sum" else torch.float32
-            for o in outs:
-                e[o] = torch.empty(e[ins[0]].shape, dtype=odt, device=dev)
-            st[est] = e
-        sets.append(st)
+    sets = make_sets(torch, rl, src, dev, nsets, ests)
     side = {est: torch.cuda.Stream(dev) for est in ests}
     for est in ests:  # warm-up: every side stream's workspace exists before capture
         side[est].wait_stream(torch.cuda.current_stream())
@@ -774,7 +830,8 @@ def time_step(torch, rl, ests, src, dev, stream, prm, l2, N, T, seconds=0.15):
             for est in ests:
                 launch(rl, est, st[est], prm)
 
-    group_calls = [[(est, group_kwargs(est, st[est], prm)) for est in ests] for st in sets]
+    group_calls = [[(base_name(est), group_kwargs(est, st[est], prm)) for est in ests]
+                   for st in sets]
 
     def grouped():
         for calls in group_calls:
@@ -792,7 +849,8 @@ def time_step(torch, rl, ests, src, dev, stream, prm, l2, N, T, seconds=0.15):
                 s.wait_stream(stream)
                 with torch.cuda.stream(s):
                     for st in sets:
-                        rl.rlcs_run_group([(e, group_kwargs(e, st[e], prm)) for e in part])
+                        rl.rlcs_run_group([(base_name(e), group_kwargs(e, st[e], prm))
+                                           for e in part])
             for s in gside[k]:
                 stream.wait_stream(s)
         return run
@@ -971,8 +1029,9 @@ def run_profile(args):
     w = WORKLOADS[args.workload]
     N = args.rows or w.N
     prm = dict(gamma=w.gamma, lambda_=w.lambda_, rho_bar=w.rho_bar, c_bar=w.c_bar)
-    src = rollout(N, w.T, w.seed, w.p_term)
     est = args.profile
+    p_trunc = (w.p_trunc or 0.005) if est.endswith("_trunc") else 0.0
+    src = rollout(N, w.T, w.seed, w.p_term, p_trunc)
     if est == "group":  # the workload's estimators as one rlcs_run_group call
         nsets = max(2, min(ROTATING_SETS, args.sets))
         sets = []
@@ -1019,12 +1078,17 @@ def run_profile(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=256)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-long-t", action="store_true", help="skip the long-row sweep")
+    ap.add_argument("--no-long-t", action="store_true",
+                    help="skip the long-row sweep and the extra entry points")
+    ap.add_argument("--schedule", choices=("streams", "serial", "grouped"), default="streams",
+                    help="how the headline step issues its seven calls")
+    ap.add_argument("--detail", default="bench_detail.json",
+                    help="where to write the per-estimator and sweep figures (JSON)")
     ap.add_argument("--profile", choices=tuple(SPECS) + ("group",), default=None,
                     help="eager launches of one estimator only (for ncu)")
     ap.add_argument("--workload", default=WORKLOAD, choices=tuple(WORKLOADS))

@@ -9,3 +9,11 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line(
         "markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
+
+
+def pytest_sessionstart(session):
+    # Build the CUDA library and the float64 oracle before collection: test
+    # modules import the package, which refuses to load without librlcs.so.
+    # Both builds skip what is already up to date.
+    import __graft_entry__
+    __graft_entry__.build()
