@@ -113,8 +113,9 @@ rlcs_status rlcs_check_status(void *workspace, rlcs_stream_t stream);
 const char *rlcs_status_string(rlcs_status status);
 
 /* Generalized Advantage Estimation.
- * rl-triton README, Kernels table, compute_gae ("backward scan over
- * delta + gamma*lambda*A"); boundary rules of Methodology 3.
+ * rl-triton README, Kernels table, compute_gae: the one-step TD errors
+ * accumulated backward with weight gamma*lambda; boundary rules of
+ * Methodology 3.
  *   delta_t = r_t + gamma*S_t - V_t          (S_t: successor value above)
  *   A_t     = delta_t + gamma*lambda*A_{t+1} (nothing carried across a cut)
  * Inputs rewards, values, terminateds [N,T]; optional truncateds and
@@ -127,8 +128,8 @@ rlcs_status rlcs_gae(const float *rewards, const float *values,
                      rlcs_stream_t stream);
 
 /* TD(lambda) returns.
- * README Kernels table, compute_lambda_returns ("lambda-return targets
- * mixing one-step TD and Monte Carlo"):
+ * README Kernels table, compute_lambda_returns: the lambda-weighted blend
+ * of n-step returns, written as a backward recursion:
  *   G_t = r_t + gamma*((1-lambda)*V_{t+1} + lambda*G_{t+1})
  *   G_t = r_t + gamma*S_t                                   at a cut
  * Same inputs as rlcs_gae; output returns [N,T] (equals GAE + values). */
@@ -157,8 +158,9 @@ rlcs_status rlcs_discounted_returns(const float *rewards,
                                     rlcs_stream_t stream);
 
 /* V-trace targets and policy-gradient advantages.
- * README Kernels table, compute_vtrace ("IS-weighted targets and
- * advantages"); definition of IMPALA V-trace with lambda in the trace:
+ * README Kernels table, compute_vtrace: value targets and advantages
+ * corrected by clipped importance ratios; definition of IMPALA V-trace with
+ * lambda in the trace:
  *   ratio_t = exp(log_rhos_t), rho_t = min(rho_bar, ratio_t),
  *   c_t = lambda*min(c_bar, ratio_t)
  *   vs_t - V_t = rho_t*(r_t + gamma*S_t - V_t) + gamma*c_t*(vs_{t+1} - V_{t+1})
@@ -175,8 +177,8 @@ rlcs_status rlcs_vtrace(const float *rewards, const float *values,
                         rlcs_stream_t stream);
 
 /* Retrace(lambda) targets.
- * README Kernels table, compute_retrace ("off-policy return estimate with
- * truncated IS ratios"); definition of Munos et al. (2016):
+ * README Kernels table, compute_retrace: an off-policy Q target whose
+ * traces are clipped importance ratios; definition of Munos et al. (2016):
  *   c_t = lambda*min(c_bar, exp(log_rhos_t))
  *   Q_t = r_t + gamma*(values_{t+1} + c_{t+1}*(Q_{t+1} - q_values_{t+1}))
  *   Q_t = r_t + gamma*S_t                                     at a cut
@@ -203,8 +205,8 @@ rlcs_status rlcs_eligibility_traces(const float *x, const float *dones,
                                     rlcs_stream_t stream);
 
 /* Episodic prefix sum, forward in time, int32.
- * README Kernels table, compute_episodic_prefix_sum ("episodic cumulative
- * sum with done-mask resets"); reset index as for the traces:
+ * README Kernels table, compute_episodic_prefix_sum: a running sum that
+ * restarts after every done step; reset index as for the traces:
  *   s_t = x_t + (1 - d_{t-1})*s_{t-1},   s_{-1} = 0,   modulo 2^32.
  * Bit-exact. Inputs x (int32) and dones (float) [N,T]; output out (int32). */
 rlcs_status rlcs_episodic_prefix_sum(const int32_t *x, const float *dones,
@@ -401,45 +403,27 @@ rlcs_status rlcs_run_group(const rlcs_call *calls, int n_calls, void *workspace,
  *  - Sharing: every call on a device uses the same array and leaves its
  *    contents behind, so calls that can overlap on the GPU (other streams,
  *    other threads) race; the caller must serialise them. Device-side wait
- *    timeouts are recorded in the array, where rlcs_check_status cannot see
- *    them. */
+ *    timeouts are recorded in the array; read them, and repair the array,
+ *    with rlcs_gae_noalloc_recover. */
 rlcs_status rlcs_gae_noalloc(const float *rewards, const float *values,
                              const float *terminateds, const float *truncateds,
                              const float *next_values, const float *bootstrap_value,
                              float *advantages, int64_t N, int64_t T, double gamma,
                              double lambda, rlcs_stream_t stream);
 
-/* Diagnostic, not an estimator: the warp-row shape's launch and data
- * movement with no scan, for measuring what a launch of a given size costs
- * before any estimator work. Reads n_inputs [N,T] float32 arrays (1..7,
- * 16-byte aligned, T % 4 == 0) and writes their elementwise sum to `out`,
- * with the same L2 prefetch and programmatic dependent launch as the
- * estimators; with `empty` nonzero the same grid only waits and exits.
- * Asynchronous on `stream`; RLCS_ERR_INVALID_ARG for bad arguments. */
-rlcs_status rlcs_diag_stream_copy(const float *const *inputs, int n_inputs, float *out,
-                                  int64_t N, int64_t T, int empty, rlcs_stream_t stream);
-
-/* Launch-shape selection, exposed for testing and tuning. The library picks
- * a shape from (N, T) and the SM count:
- *   RLCS_SHAPE_WARP_ROW    one warp per row, inputs in registers (T <= 512);
- *   RLCS_SHAPE_BLOCK_TILE  one 256-thread block per row tile, inputs loaded
- *                          into registers, tiles of a row chained by
- *                          decoupled look-back through the workspace;
- *   RLCS_SHAPE_BLOCK_CHUNK one 256-thread block per row chunk, the chunk
- *                          staged into shared memory by bulk copy (TMA),
- *                          chunks chained by decoupled look-back.
- * Setting an override forces a shape and, for the two block shapes, a tile
- * or chunk length of 1024, 2048 or 4096 steps (0 lets the library choose),
- * for every later call in this process until reset with RLCS_SHAPE_AUTO.
- * Not thread-safe with concurrent calls. Returns RLCS_ERR_INVALID_ARG for an
- * unknown shape or length. */
-typedef enum {
-  RLCS_SHAPE_AUTO = 0,
-  RLCS_SHAPE_WARP_ROW = 1,
-  RLCS_SHAPE_BLOCK_CHUNK = 2,
-  RLCS_SHAPE_BLOCK_TILE = 3
-} rlcs_shape;
-rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk);
+/* Status and repair of rlcs_gae_noalloc's scratch array on the current
+ * device (the paper has no counterpart). Synchronises `stream`, reads the
+ * status that earlier rlcs_gae_noalloc calls recorded in the array
+ * (RLCS_ERR_TIMEOUT when a bounded wait ran out, RLCS_ERR_WORKSPACE when the
+ * array's counters were found inconsistent), then zeroes the whole array on
+ * `stream` and waits for that, which returns it to its initial state: the
+ * header counters and every chunk record, so no flag of an earlier call can
+ * match a later one. Returns the status it read (RLCS_OK if none), or
+ * RLCS_ERR_CUDA if a CUDA call failed. Call it after a call reported an
+ * error, after calls may have overlapped, or whenever a caller wants to
+ * check; no rlcs_gae_noalloc call may be in flight on the device meanwhile.
+ * It allocates nothing. */
+rlcs_status rlcs_gae_noalloc_recover(rlcs_stream_t stream);
 
 #ifdef __cplusplus
 }

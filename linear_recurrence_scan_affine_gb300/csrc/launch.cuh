@@ -4,7 +4,7 @@
 #include <mutex>
 
 #include "kernels.cuh"
-#include "rlcs.h"
+#include "rlcs_internal.h"
 
 namespace rlcs {
 

@@ -1,5 +1,6 @@
 // C ABI entry points: argument validation, launch-shape planning and the
-// workspace/status helpers declared in include/rlcs.h.
+// workspace/status helpers declared in include/rlcs.h, and the test and
+// tuning hooks declared in include/rlcs_internal.h.
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -872,4 +873,36 @@ extern "C" rlcs_status rlcs_gae_noalloc(const float *rewards, const float *value
   if (st != RLCS_OK) return st;
   return rlcs_gae(rewards, values, terminateds, truncateds, next_values, bootstrap_value,
                   advantages, N, T, gamma, lambda, scratch, kNoAllocBytes, stream);
+}
+
+// Status and repair of the scratch array. Reading the status needs the
+// stream's work done; the zeroing covers the whole array, records included:
+// a header-only reset would restart the epoch at 0, whose tag the records of
+// the earliest calls still carry.
+extern "C" rlcs_status rlcs_gae_noalloc_recover(rlcs_stream_t stream) {
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  void *scratch = nullptr;
+  const rlcs_status st = noalloc_scratch(&scratch);
+  if (st != RLCS_OK) return st;
+  if (cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return RLCS_ERR_CUDA;
+  }
+  uint32_t code = 0;
+  const WsHeader *h = static_cast<const WsHeader *>(scratch);
+  if (cudaMemcpy(&code, &h->status, sizeof(code), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemsetAsync(scratch, 0, kNoAllocBytes, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return RLCS_ERR_CUDA;
+  }
+  return static_cast<rlcs_status>(code);
+}
+
+extern "C" rlcs_status rlcs_internal_noalloc_scratch(void **device_ptr, size_t *bytes) {
+  if (!device_ptr || !bytes) return RLCS_ERR_INVALID_ARG;
+  const rlcs_status st = noalloc_scratch(device_ptr);
+  if (st != RLCS_OK) return st;
+  *bytes = kNoAllocBytes;
+  return RLCS_OK;
 }

@@ -13,6 +13,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "rlcs.h")
+INTERNAL = os.path.join(ROOT, "include", "rlcs_internal.h")
 
 OK, INVALID, MISALIGNED, WORKSPACE, CUDA, TIMEOUT = 0, 1, 2, 3, 4, 5
 
@@ -25,10 +26,22 @@ def lib():
     return binding.lib()
 
 
-def declared_functions():
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(rlcs_[a-z_]+)\s*\(", src)))
+def declared_functions(path=None):
+    """Functions the headers declare (both, unless one path is given)."""
+    names = set()
+    for p in ([path] if path else [HEADER, INTERNAL]):
+        src = re.sub(r"/\*.*?\*/", "", open(p).read(), flags=re.S)
+        names |= set(re.findall(r"\b(rlcs_[a-z_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_test_hooks_live_outside_the_product_header():
+    product = declared_functions(HEADER)
+    internal = declared_functions(INTERNAL)
+    for name in ("rlcs_set_shape_override", "rlcs_diag_stream_copy",
+                 "rlcs_internal_noalloc_scratch"):
+        assert name in internal and name not in product, name
+    assert "rlcs_gae_noalloc" in product and "rlcs_gae_noalloc_recover" in product
 
 
 def test_header_declares_the_seven_estimators():
