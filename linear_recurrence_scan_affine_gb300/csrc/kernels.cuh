@@ -1132,76 +1132,121 @@ struct TmShape {
   int64_t chunks;  // chunks per environment = ceil(T / kTmChunk)
 };
 
-// Decoupled look-back with one chain per lane (warp-wide call): lane l's
-// record for this chunk is self + l, its predecessors in scan order are
-// self + l - j*stride for j = 1..npred. Inactive lanes (environments past N)
-// neither publish nor wait. Returns the value just outside the chunk on its
-// scan-origin side. Every wait is bounded; on timeout the status word records
-// RLCS_ERR_TIMEOUT and missing aggregates count as the identity.
+// Decoupled look-back of the time-major tier, one chain per lane
+// (environment), run by the whole block. Lane l's record for this chunk is
+// self + l; its predecessors in scan order are self + l - d*stride for
+// d = 1..npred. Warp 0 publishes the chunk aggregate of every lane. Then, round
+// by round, the block's warps read every lane's predecessor records at the
+// distances d0 + 1 .. d0 + W (W / kWarps distances each; the kernel uses one
+// per warp), so one L2 round trip brings a window of W predecessors for every
+// environment into shared memory, and warp 0 composes each lane's
+// window nearest first until it meets an inclusive value. (Many chunks of an
+// environment are in flight at once when there are few environment groups;
+// walking them one record per round trip was the time-major tier's main
+// cost.) A record still unpublished when its window was read is re-read by
+// warp 0 with a bounded wait; on timeout the status word records
+// RLCS_ERR_TIMEOUT and the missing aggregates count as the identity.
+// Inactive lanes (environments past N) neither publish nor wait. Every
+// thread of the block calls this; the value just outside the chunk on its
+// scan-origin side is returned in warp 0, which also publishes the chunk's
+// inclusive value.
+template <class P, int W>
+struct TmWindow {
+  uint32_t state[W][32];  // 0: unpublished, kStateAgg or kStateInc
+  P pay[W][32];           // the aggregate, or the inclusive value in .c
+  uint32_t more;          // some lane of warp 0 still walks
+};
+
 template <class P, class V>
-__device__ V lookback_lanes(WsHeader *ws, int64_t self, int64_t stride, int64_t npred, P agg,
-                            uint32_t tag, int lane, bool active) {
-  WsRecord *rec = reinterpret_cast<WsRecord *>(ws + 1) + self + lane;
+__device__ __forceinline__ uint32_t tm_read_record(const WsRecord *r, uint32_t tagA, uint32_t tagP,
+                                                   P &pv) {
+  const uint64_t wi = ld_relaxed_gpu_u64(&r->inc);
+  if ((uint32_t)(wi >> 32) == tagP) {
+    vfrom((uint32_t)wi, pv.c);
+    return kStateInc;
+  }
+  const uint64_t wm = ld_relaxed_gpu_u64(&r->m), wc = ld_relaxed_gpu_u64(&r->c);
+  if ((uint32_t)(wm >> 32) == tagA && (uint32_t)(wc >> 32) == tagA) {
+    vfrom((uint32_t)wm, pv.m);
+    vfrom((uint32_t)wc, pv.c);
+    return kStateAgg;
+  }
+  return 0u;
+}
+
+template <class P, class V, int W, int kWarps>
+__device__ V tm_lookback(WsHeader *ws, int64_t self, int64_t stride, int64_t npred, P agg,
+                         uint32_t tag, int lane, int warp, bool active, TmWindow<P, W> &win) {
+  WsRecord *mine = reinterpret_cast<WsRecord *>(ws + 1) + self + lane;
   const uint32_t tagA = (tag << 2) | kStateAgg, tagP = (tag << 2) | kStateInc;
   if (npred == 0) {  // the scan origin: nothing before it
-    if (active) st_relaxed_gpu_u64(&rec->inc, tagged(tagP, vbits(apply(agg, V(0)))));
+    if (warp == 0 && active) st_relaxed_gpu_u64(&mine->inc, tagged(tagP, vbits(apply(agg, V(0)))));
     return V(0);
   }
-  if (active) {
-    st_relaxed_gpu_u64(&rec->m, tagged(tagA, vbits(agg.m)));
-    st_relaxed_gpu_u64(&rec->c, tagged(tagA, vbits(agg.c)));
+  if (warp == 0 && active) {
+    st_relaxed_gpu_u64(&mine->m, tagged(tagA, vbits(agg.m)));
+    st_relaxed_gpu_u64(&mine->c, tagged(tagA, vbits(agg.c)));
   }
   P acc = identity(P{});
   V X = V(0);
   bool done = !active, timed_out = false;
-  int64_t j = 1;  // distance of the predecessor this lane reads next
-  uint64_t start = 0;
-  unsigned backoff = 64;
-  while (!__all_sync(kFull, done)) {
-    bool moved = false;
-    if (!done) {
-      const WsRecord *r = rec - j * stride;
-      const uint64_t wi = ld_relaxed_gpu_u64(&r->inc);
-      if ((uint32_t)(wi >> 32) == tagP) {
-        V incv;
-        vfrom((uint32_t)wi, incv);
-        X = apply(acc, incv);
-        done = moved = true;
-      } else {
-        const uint64_t wm = ld_relaxed_gpu_u64(&r->m), wc = ld_relaxed_gpu_u64(&r->c);
-        if ((uint32_t)(wm >> 32) == tagA && (uint32_t)(wc >> 32) == tagA) {
-          P a;
-          vfrom((uint32_t)wm, a.m);
-          vfrom((uint32_t)wc, a.c);
-          acc = compose(acc, a);
-          moved = true;
-          if (++j > npred) {  // the origin publishes an inclusive value: not reached
+  constexpr int R = W / kWarps;  // distances each warp reads per round
+  static_assert(R * kWarps == W, "whole rows of the window per warp");
+  for (int64_t d0 = 0;; d0 += W) {
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const int slot = warp * R + i;
+      const int64_t d = d0 + slot + 1;
+      P pv = identity(P{});
+      uint32_t st = 0u;
+      if (active && d <= npred) st = tm_read_record<P, V>(mine - d * stride, tagA, tagP, pv);
+      win.state[slot][lane] = st;
+      win.pay[slot][lane] = pv;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      for (int w = 0; w < W && !done; ++w) {
+        const int64_t dd = d0 + w + 1;
+        if (dd > npred) {  // the origin publishes an inclusive value: not reached
+          X = apply(acc, V(0));
+          done = true;
+          break;
+        }
+        uint32_t s = win.state[w][lane];
+        P e = win.pay[w][lane];
+        if (s == 0u) {  // not yet published when the window was read: wait for it
+          const WsRecord *r = mine - dd * stride;
+          const uint64_t t0 = globaltimer_ns();
+          unsigned backoff = 64;
+          while ((s = tm_read_record<P, V>(r, tagA, tagP, e)) == 0u) {
+            if (globaltimer_ns() - t0 > kWaitLimitNs) break;
+            __nanosleep(backoff);
+            if (backoff < 1024) backoff <<= 1;
+          }
+          if (s == 0u) {
+            timed_out = true;
             X = apply(acc, V(0));
             done = true;
+            break;
           }
         }
+        if (s == kStateInc) {
+          X = apply(acc, e.c);
+          done = true;
+        } else {
+          acc = compose(acc, e);
+        }
       }
+      const bool more = __any_sync(kFull, !done);
+      if (lane == 0) win.more = more ? 1u : 0u;
     }
-    if (__any_sync(kFull, moved)) {
-      start = 0;
-      backoff = 64;
-      continue;
-    }
-    const uint64_t now = globaltimer_ns();
-    if (start == 0) start = now;
-    if (__any_sync(kFull, now - start > kWaitLimitNs)) {
-      if (!done) {
-        X = apply(acc, V(0));
-        done = true;
-      }
-      timed_out = true;
-      break;
-    }
-    __nanosleep(backoff);  // leave issue slots to the warps doing work
-    if (backoff < 1024) backoff <<= 1;
+    __syncthreads();
+    if (!win.more) break;
   }
-  if (timed_out && lane == 0) set_status(ws, kStatusTimeout);
-  if (active) st_relaxed_gpu_u64(&rec->inc, tagged(tagP, vbits(apply(agg, X))));
+  if (warp == 0) {
+    if (timed_out) set_status(ws, kStatusTimeout);
+    if (active) st_relaxed_gpu_u64(&mine->inc, tagged(tagP, vbits(apply(agg, X))));
+  }
   return X;
 }
 
@@ -1209,7 +1254,7 @@ __device__ __forceinline__ float ldg_at(const void *base, int64_t byte_off) {
   return __ldg(reinterpret_cast<const float *>(static_cast<const char *>(base) + byte_off));
 }
 
-// One warp's span of L steps for its 32 environments. boff[j]: byte
+// One warp's span of L steps for its 32 environments. b0 + j*rowb: byte
 // offset of step ts+j of this lane's environment; rowb: bytes per row (4N).
 // FULL: the span holds neither step 0 nor step T-1 and every lane's
 // environment exists, so no step needs a bounds check or an edge flag.
@@ -1222,7 +1267,7 @@ struct TmRaw {
 
 // Issue every load of the span (nothing here waits for one).
 template <class E, bool TRUNC, bool FULL, int L>
-__device__ __forceinline__ void tm_load(const Params &p, const int64_t (&boff)[L], int64_t rowb,
+__device__ __forceinline__ void tm_load(const Params &p, int64_t b0, int64_t rowb,
                                         int64_t ts, int64_t T, bool env_ok, TmRaw<L> &raw) {
   constexpr uint32_t kUse = E::kSlots | (TRUNC ? E::kOptSlots : 0u);
 #pragma unroll
@@ -1230,7 +1275,7 @@ __device__ __forceinline__ void tm_load(const Params &p, const int64_t (&boff)[L
 #pragma unroll
     for (int j = 0; j < L; ++j) {
       const bool ok = FULL || (env_ok && ts + j < T);
-      raw.v[k][j] = ((kUse & bit(k)) && ok) ? ldg_at(p.in[k], boff[j]) : 0.f;
+      raw.v[k][j] = ((kUse & bit(k)) && ok) ? ldg_at(p.in[k], b0 + j * rowb) : 0.f;
     }
   }
   // a span wholly past T (last chunk) reads neither neighbour
@@ -1238,10 +1283,10 @@ __device__ __forceinline__ void tm_load(const Params &p, const int64_t (&boff)[L
 #pragma unroll
   for (int k = 0; k < kNumSlots; ++k)
     raw.next[k] = (E::kBackward && (E::kNext & bit(k)) && next_ok)
-                      ? ldg_at(p.in[k], boff[L - 1] + rowb)
+                      ? ldg_at(p.in[k], b0 + L * rowb)
                       : 0.f;
   const bool prev_ok = FULL || (env_ok && ts > 0 && ts <= T);
-  raw.prev_d = (E::kPrevD && prev_ok) ? ldg_at(p.in[kD], boff[0] - rowb) : 0.f;
+  raw.prev_d = (E::kPrevD && prev_ok) ? ldg_at(p.in[kD], b0 - rowb) : 0.f;
 }
 
 // Build every step's pair; steps past T become the identity (never stored).
@@ -1275,7 +1320,7 @@ __device__ __forceinline__ void tm_build(const Params &p, const TmRaw<L> &raw, i
 // Walk the span from the value adjacent to it on the scan-origin side and
 // store every step's output(s).
 template <class E, bool FULL, int L>
-__device__ __forceinline__ void tm_emit(const Params &p, const int64_t (&boff)[L], int64_t ts,
+__device__ __forceinline__ void tm_emit(const Params &p, int64_t b0, int64_t rowb, int64_t ts,
                                         int64_t T, bool env_ok,
                                         typename ValueOf<typename E::Pair>::type nb,
                                         const typename E::Pair (&e)[L], const float (&aux0)[L],
@@ -1289,12 +1334,12 @@ __device__ __forceinline__ void tm_emit(const Params &p, const int64_t (&boff)[L
     const V A = apply(e[j], nb);
     if (FULL || (env_ok && ts + j < T)) {
       if constexpr (std::is_same<V, uint32_t>::value) {
-        *reinterpret_cast<uint32_t *>(out0 + boff[j]) = A;
+        *reinterpret_cast<uint32_t *>(out0 + b0 + j * rowb) = A;
       } else {
-        *reinterpret_cast<float *>(out0 + boff[j]) = E::out0(A, nb, e[j], aux0[j], aux1[j]);
+        *reinterpret_cast<float *>(out0 + b0 + j * rowb) = E::out0(A, nb, e[j], aux0[j], aux1[j]);
         if constexpr (E::kOuts > 1) {
           if (out1)
-            *reinterpret_cast<float *>(out1 + boff[j]) = E::out1(A, nb, e[j], aux0[j], aux1[j]);
+            *reinterpret_cast<float *>(out1 + b0 + j * rowb) = E::out1(A, nb, e[j], aux0[j], aux1[j]);
         }
       }
     }
@@ -1311,6 +1356,7 @@ __global__ void __launch_bounds__(tm_threads<L>()) time_major_kernel(Params p, T
   constexpr int kWarps = kTmChunk / L;
   __shared__ P s_agg[kWarps][kTmEnvs];
   __shared__ V s_in[kWarps][kTmEnvs];
+  __shared__ TmWindow<P, kWarps> s_win;
   __shared__ uint32_t s_epoch;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t N = p.N, T = p.T;
@@ -1324,17 +1370,14 @@ __global__ void __launch_bounds__(tm_threads<L>()) time_major_kernel(Params p, T
   // uniform across the warp: an interior span of a full group of environments
   const bool full = ts > 0 && ts + L < T && (g + 1) * kTmEnvs <= N;
   const int64_t rowb = N * 4;
-  int64_t boff[L];
-  boff[0] = (ts * N + n) * 4;
-#pragma unroll
-  for (int j = 1; j < L; ++j) boff[j] = boff[j - 1] + rowb;
+  const int64_t b0 = (ts * N + n) * 4;  // byte offset of step ts of this lane's environment
 
   pdl_wait();
   TmRaw<L> raw;
   if (full)
-    tm_load<E, TRUNC, true, L>(p, boff, rowb, ts, T, env_ok, raw);
+    tm_load<E, TRUNC, true, L>(p, b0, rowb, ts, T, env_ok, raw);
   else
-    tm_load<E, TRUNC, false, L>(p, boff, rowb, ts, T, env_ok, raw);
+    tm_load<E, TRUNC, false, L>(p, b0, rowb, ts, T, env_ok, raw);
   const float boot = (E::kUsesRowValue && p.boot && env_ok) ? __ldg(p.boot + n) : 0.f;
   if (chained && threadIdx.x == 0) s_epoch = ld_relaxed_gpu(&sh.ws->epoch);
   // Besides letting the next grid launch, this instruction keeps the
@@ -1360,18 +1403,20 @@ __global__ void __launch_bounds__(tm_threads<L>()) time_major_kernel(Params p, T
   s_agg[warp][lane] = agg;
   __syncthreads();
 
+  // the chunk's pair (warp 0): warps in order outer-first from the scan origin side
+  P cagg = identity(P{});
   if (warp == 0) {
-    // the chunk's pair: warps in order outer-first from the scan origin side
-    P cagg = identity(P{});
     if (E::kBackward) {
       for (int w = kWarps - 1; w >= 0; --w) cagg = compose(s_agg[w][lane], cagg);
     } else {
       for (int w = 0; w < kWarps; ++w) cagg = compose(s_agg[w][lane], cagg);
     }
-    V X = V(0);
-    if (chained)
-      X = lookback_lanes<P, V>(sh.ws, (q * sh.groups + g) * kTmEnvs, sh.groups * kTmEnvs, q,
-                               cagg, s_epoch & kTagMask, lane, env_ok);
+  }
+  V X = V(0);
+  if (chained)  // uniform over the block: every thread takes part
+    X = tm_lookback<P, V, kWarps, kWarps>(sh.ws, (q * sh.groups + g) * kTmEnvs, sh.groups * kTmEnvs, q,
+                                  cagg, s_epoch & kTagMask, lane, warp, env_ok, s_win);
+  if (warp == 0) {
     if (E::kBackward) {
       for (int w = kWarps - 1; w >= 0; --w) {
         s_in[w][lane] = X;
@@ -1388,9 +1433,9 @@ __global__ void __launch_bounds__(tm_threads<L>()) time_major_kernel(Params p, T
 
   const V nb = s_in[warp][lane];  // value adjacent to this warp's span, scan-origin side
   if (full)
-    tm_emit<E, true, L>(p, boff, ts, T, env_ok, nb, e, aux0, aux1);
+    tm_emit<E, true, L>(p, b0, rowb, ts, T, env_ok, nb, e, aux0, aux1);
   else
-    tm_emit<E, false, L>(p, boff, ts, T, env_ok, nb, e, aux0, aux1);
+    tm_emit<E, false, L>(p, b0, rowb, ts, T, env_ok, nb, e, aux0, aux1);
   if (chained && threadIdx.x == 0) finish_launch(sh.ws, sh.groups * sh.chunks, s_epoch);
 }
 
@@ -1422,17 +1467,14 @@ __global__ void __launch_bounds__(kTmShortWarps * 32) time_major_short_kernel(Pa
   const int64_t ts = (int64_t)warp * 2 * L + half * L;  // this lane's first step
   const bool full = ts > 0 && ts + L < T && (g + 1) * kTmShortEnvs <= N;
   const int64_t rowb = N * 4;
-  int64_t boff[L];
-  boff[0] = (ts * N + n) * 4;
-#pragma unroll
-  for (int j = 1; j < L; ++j) boff[j] = boff[j - 1] + rowb;
+  const int64_t b0 = (ts * N + n) * 4;  // byte offset of step ts of this lane's environment
 
   pdl_wait();
   TmRaw<L> raw;
   if (full)
-    tm_load<E, TRUNC, true, L>(p, boff, rowb, ts, T, env_ok, raw);
+    tm_load<E, TRUNC, true, L>(p, b0, rowb, ts, T, env_ok, raw);
   else
-    tm_load<E, TRUNC, false, L>(p, boff, rowb, ts, T, env_ok, raw);
+    tm_load<E, TRUNC, false, L>(p, b0, rowb, ts, T, env_ok, raw);
   const float boot = (E::kUsesRowValue && p.boot && env_ok) ? __ldg(p.boot + n) : 0.f;
   pdl_launch_dependents();  // also keeps the loads above ahead of the arithmetic
   P e[L];
@@ -1482,9 +1524,9 @@ __global__ void __launch_bounds__(kTmShortWarps * 32) time_major_short_kernel(Pa
   const bool outer = E::kBackward ? (half == 1) : (half == 0);  // nearer the origin
   const V nb = outer ? Xw : apply(other, Xw);
   if (full)
-    tm_emit<E, true, L>(p, boff, ts, T, env_ok, nb, e, aux0, aux1);
+    tm_emit<E, true, L>(p, b0, rowb, ts, T, env_ok, nb, e, aux0, aux1);
   else
-    tm_emit<E, false, L>(p, boff, ts, T, env_ok, nb, e, aux0, aux1);
+    tm_emit<E, false, L>(p, b0, rowb, ts, T, env_ok, nb, e, aux0, aux1);
 }
 
 }  // namespace rlcs
