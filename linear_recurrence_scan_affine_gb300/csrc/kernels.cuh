@@ -1125,6 +1125,14 @@ template <int L>
 constexpr int tm_threads() {
   return kTmChunk / L * 32;
 }
+// Resident blocks per SM the compiler must allow: 2 for the 8-warp shape
+// (16 steps per lane), which caps its heaviest instances at 128 registers
+// (measured on GB300: Retrace at 256 x 16384 took 42.7 us uncapped and
+// 31.5 us capped; the others unchanged; 4 blocks per SM was slower for all).
+template <int L>
+constexpr int tm_min_blocks() {
+  return L >= 16 ? 2 : 1;
+}
 
 struct TmShape {
   WsHeader *ws;    // workspace header; NULL when one chunk covers T
@@ -1348,7 +1356,8 @@ __device__ __forceinline__ void tm_emit(const Params &p, int64_t b0, int64_t row
 }
 
 template <class E, bool TRUNC, int L>
-__global__ void __launch_bounds__(tm_threads<L>()) time_major_kernel(Params p, TmShape sh) {
+__global__ void __launch_bounds__(tm_threads<L>(), tm_min_blocks<L>())
+    time_major_kernel(Params p, TmShape sh) {
   static_assert((E::kBF16Slots | E::kU8Slots) == 0u, "time-major slots are 4-byte words");
   static_assert(kTmChunk % L == 0 && kTmChunk / L <= 32, "whole warps per chunk");
   using P = typename E::Pair;
