@@ -71,7 +71,8 @@ static double row_boot(const float *bootstrap, int64_t n) {
   return bootstrap != NULL ? (double)bootstrap[n] : 0.0;
 }
 
-/* GAE (README Kernels table, "backward scan over delta + gamma*lambda*A"):
+/* GAE (README Kernels table, compute_gae: one-step TD errors accumulated
+ * backward with weight gamma*lambda):
  *   delta_t = r_t + gamma*S_t - V_t
  *   A_t     = delta_t + gamma*lambda*A_{t+1}   (A_{t+1} dropped at a cut). */
 void oracle_gae(int64_t N, int64_t T, const float *rewards,
@@ -98,8 +99,8 @@ void oracle_gae(int64_t N, int64_t T, const float *rewards,
   }
 }
 
-/* TD(lambda) returns (README Kernels table, "lambda-return targets mixing
- * one-step TD and Monte Carlo"), recursive form of the lambda-return:
+/* TD(lambda) returns (README Kernels table, compute_lambda_returns: the
+ * lambda-weighted blend of n-step returns), recursive form:
  *   G_t = r_t + gamma*((1-lambda)*V_{t+1} + lambda*G_{t+1})   not a cut
  *   G_t = r_t + gamma*S_t                                       at a cut  */
 void oracle_lambda_returns(int64_t N, int64_t T, const float *rewards,
@@ -158,7 +159,8 @@ void oracle_discounted_returns(int64_t N, int64_t T, const float *rewards,
   }
 }
 
-/* V-trace (README Kernels table, "IS-weighted targets and advantages";
+/* V-trace (README Kernels table, compute_vtrace: value targets and
+ * advantages corrected by clipped importance ratios;
  * IMPALA eq. 1 in recursive form, lambda folded into the trace weight):
  *   rho_t = min(rho_bar, exp(log_rho_t)),  c_t = lambda*min(c_bar, exp(log_rho_t))
  *   vs_t - V_t = rho_t*(r_t + gamma*S_t - V_t)
@@ -201,8 +203,9 @@ void oracle_vtrace(int64_t N, int64_t T, const float *rewards,
   }
 }
 
-/* Retrace(lambda) (README Kernels table, "off-policy return estimate with
- * truncated IS ratios"; Munos et al. 2016 in recursive form):
+/* Retrace(lambda) (README Kernels table, compute_retrace: an off-policy Q
+ * target with clipped importance-ratio traces; Munos et al. 2016 in
+ * recursive form):
  *   values_t = E_pi Q(s_t, .),  q_values_t = Q(s_t, a_t)
  *   c_{t+1} = lambda*min(c_bar, exp(log_rho_{t+1}))
  *   Qret_t = r_t + gamma*(values_{t+1} + c_{t+1}*(Qret_{t+1} - q_values_{t+1}))
@@ -256,8 +259,9 @@ void oracle_eligibility_traces(int64_t N, int64_t T, const float *x,
   }
 }
 
-/* Episodic prefix sum, forward in time (README Kernels table, "episodic
- * cumulative sum with done-mask resets"), same reset index as the traces:
+/* Episodic prefix sum, forward in time (README Kernels table,
+ * compute_episodic_prefix_sum: a running sum restarted after each done
+ * step), same reset index as the traces:
  *   s_t = x_t + (1 - d_{t-1})*s_{t-1},   s_{-1} = 0,   modulo 2^32. */
 void oracle_episodic_prefix_sum(int64_t N, int64_t T, const int32_t *x,
                                 const float *dones, int32_t *out) {

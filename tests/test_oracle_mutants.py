@@ -45,6 +45,18 @@ MUTANTS = {
     "affine_init_dropped": ("double prev = x_init ? (double)x_init[n] : 0.0;", "double prev = 0.0;"),
     "psum_reset_same_step": ("if (t > 0 && !SET(d, t - 1)) s += s_prev;",
                              "if (t > 0 && !SET(d, t)) s += s_prev;"),
+    "truncation_does_not_cut": ("  if (trunc != NULL && SET(trunc, t)) return 1;",
+                                "  if (trunc != NULL && SET(trunc, t)) return 0;"),
+    "gae_carries_across_cut": ("if (!is_cut(d, tr, t, T)) a += gamma * lambda * a_next;",
+                               "a += gamma * lambda * a_next;"),
+    "vtrace_rho_uses_c_bar": ("double rho = fmin(rho_bar, ratio);", "double rho = fmin(c_bar, ratio);"),
+    "vtrace_pg_drops_rho": ("pg_row[t] = rho * ((double)r[t] + gamma * w - (double)v[t]);",
+                            "pg_row[t] = (double)r[t] + gamma * w - (double)v[t];"),
+    "vtrace_diff_uses_own_value": ("if (!cut) diff += gamma * c * (vs_next - v_next);",
+                                   "if (!cut) diff += gamma * c * (vs_next - (double)v[t]);"),
+    "elig_drops_gamma": ("if (t > 0 && !SET(d, t - 1)) e += gamma * lambda * e_prev;",
+                         "if (t > 0 && !SET(d, t - 1)) e += lambda * e_prev;"),
+    "affine_direction_ignored": ("int64_t t = reverse ? T - 1 - i : i;", "int64_t t = i;"),
 }
 
 
