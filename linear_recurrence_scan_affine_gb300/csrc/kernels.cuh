@@ -9,9 +9,10 @@
 //
 //  * warp_row_kernel    one warp per row (T <= 512): inputs go straight to
 //                       registers with 128-bit loads; no shared memory.
-//  * block_tile_kernel  the default for longer rows: one 256-thread block per
-//                       row tile of 1024*S steps, inputs in registers, warp
-//                       aggregates composed in shared memory, the tiles of a
+//  * block_tile_kernel  the default for longer rows: one block per row tile
+//                       (8 warps of 1 or 2 strips: 1024 or 2048 steps; 16
+//                       warps of 2 strips: 4096 steps), inputs in registers,
+//                       warp aggregates composed in shared memory, the tiles of a
 //                       row chained in a single pass by a decoupled look-back
 //                       through the workspace (self-validating 64-bit
 //                       records, epoch tags, bounded waits), tiles in
@@ -912,33 +913,64 @@ struct TileShape {
   int64_t rec_off;        // first workspace record of this call (0 for a single call)
 };
 
-// Resident blocks per SM the compiler must allow (measured on GB300):
-// 4096-step tiles keep more state per thread and are used when the whole
-// grid fits in about one wave (2 per SM); 2048-step tiles are capped at 64
-// registers (4 per SM) and 1024-step tiles at 40 (6 per SM), so one block's
-// look-back overlaps the others' loads.
-template <int S> struct TileMinBlocks { static constexpr int value = S >= 4 ? 2 : (S == 2 ? 4 : 6); };
-// Single calls of estimators that move at most four arrays: 2048-step tiles
-// at 5 blocks/SM (48 registers, a few bytes spilled). Measured on GB300 at
-// 256 x 16384: discounted returns 14.3 against 15.5 us, eligibility traces
-// 13.2 against 14.1, prefix sum 13.5 against 14.7. (The grouped launch keeps
-// 4 blocks/SM: a separate launch for its light calls was slower overall.)
-template <class E, bool TRUNC, int S> struct CallTileMinBlocks {
+// Tile layouts: W warps of S strips, W * 128 * S steps per tile. 1024- and
+// 2048-step tiles are 8 warps of 1 or 2 strips; 4096-step tiles are 16
+// warps of 2 strips, which keeps the per-thread state of the 2048-step tile
+// (measured on GB300 against 8 warps of 4 strips at 2 blocks/SM: 256 x 4096
+// single calls 3-28% faster, where a row is one tile and needs no
+// look-back, 8 x 131072 4-10% faster; the 256 x 4096 grouped step 25.6
+// against 26.5 us).
+template <int S>
+constexpr int tile_warps() {
+  return S >= 4 ? 16 : kChunkWarps;
+}
+template <int S>
+constexpr int tile_strips() {
+  return S >= 4 ? 2 : S;
+}
+
+// Resident blocks per SM the compiler must allow (measured on GB300): 2 for
+// 16-warp tiles and 4 for 8 warps of 2 strips (64 registers), 6 for 1024-step
+// tiles (40), so one block's look-back overlaps the others' loads.
+template <int S, int W> struct TileMinBlocks {
+  static constexpr int value = W >= 16 ? 2 : (S >= 2 ? 4 : 6);
+};
+// Single calls of estimators that move at most four arrays: 8-warp 2048-step
+// tiles at 5 blocks/SM (48 registers, a few bytes spilled). Measured on
+// GB300 at 256 x 16384: discounted returns 14.3 against 15.5 us, eligibility
+// traces 13.2 against 14.1, prefix sum 13.5 against 14.7. (The grouped
+// launch keeps 4 blocks/SM: a separate launch for its light calls was slower
+// overall.)
+// 16-warp tiles of calls that move three arrays (discounted returns,
+// eligibility traces, the prefix sum) run at 3 blocks/SM (40 registers, a
+// few bytes spilled) when the grid spans more than one wave: measured at
+// 4096 x 4096, 8-13% faster than at 2 blocks/SM; on one-wave grids
+// (256 x 4096) 32% slower, so those keep 2. Calls that move four arrays
+// were slower at 3 everywhere.
+template <class E, bool TRUNC>
+constexpr bool three_arrays() {
+  return __builtin_popcount(Strips<E, TRUNC, 1>::kUse) + E::kOuts <= 3;
+}
+template <class E, bool TRUNC, int S, int W, bool MANY_WAVES = false> struct CallTileMinBlocks {
   static constexpr int value =
-      (S == 2 && row_warps<E, TRUNC>() == 8) ? 5 : TileMinBlocks<S>::value;
+      (S == 2 && W == 8 && row_warps<E, TRUNC>() == 8) ? 5
+      : (W == 16 && MANY_WAVES && three_arrays<E, TRUNC>()) ? 3
+                                                             : TileMinBlocks<S, W>::value;
 };
 
-// Block b of one call's tiles (b counts from 0 within the call).
-template <class E, bool TRUNC, int S>
+// Block b of one call's tiles (b counts from 0 within the call); W warps of
+// S strips each.
+template <class E, bool TRUNC, int S, int W>
 __device__ __forceinline__ void tile_body(const Params &p, const TileShape &ts, int64_t b) {
+  static_assert(W <= 32, "warp 0 scans the warps' aggregates");
   using St = Strips<E, TRUNC, S>;
   using P = typename St::P;
   using V = typename St::V;
-  constexpr int C = kChunkWarps * kStrip * S;  // steps per tile
+  constexpr int C = W * kStrip * S;  // steps per tile
   constexpr uint32_t kUse = St::kUse;
 
-  __shared__ P s_warp[kChunkWarps];
-  __shared__ V s_carry[kChunkWarps];
+  __shared__ P s_warp[W];
+  __shared__ V s_carry[W];
   __shared__ uint32_t s_epoch;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1004,16 +1036,16 @@ __device__ __forceinline__ void tile_body(const Params &p, const TileShape &ts, 
   __syncthreads();
 
   if (warp == 0) {
-    const P w = (lane < kChunkWarps) ? s_warp[lane] : identity(P{});
+    const P w = (lane < W) ? s_warp[lane] : identity(P{});
     P inc, nb, tile_agg;
     if (E::kBackward) {
       inc = warp_suffix_scan(w, lane);
       tile_agg = shfl_idx(inc, 0);
       const P x = shfl_down(inc, 1);
-      nb = (lane >= kChunkWarps - 1) ? identity(P{}) : x;
+      nb = (lane >= W - 1) ? identity(P{}) : x;
     } else {
       inc = warp_prefix_scan(w, lane);
-      tile_agg = shfl_idx(inc, kChunkWarps - 1);
+      tile_agg = shfl_idx(inc, W - 1);
       const P x = shfl_up(inc, 1);
       nb = (lane == 0) ? identity(P{}) : x;
     }
@@ -1022,7 +1054,7 @@ __device__ __forceinline__ void tile_body(const Params &p, const TileShape &ts, 
       const uint32_t epoch = s_epoch;
       X = lookback<P, V>(ts.ws, ts.rec_off + b, N, r, tile_agg, epoch & kTagMask, lane, hint);
     }
-    if (lane < kChunkWarps) s_carry[lane] = apply(nb, X);
+    if (lane < W) s_carry[lane] = apply(nb, X);
   }
   __syncthreads();
 
@@ -1046,10 +1078,10 @@ __device__ __forceinline__ void tile_body(const Params &p, const TileShape &ts, 
   if (Q > 1 && tid == 0) finish_launch(ts.ws, ts.total_tiles, s_epoch);
 }
 
-template <class E, bool TRUNC, int S>
-__global__ void __launch_bounds__(kChunkThreads, CallTileMinBlocks<E, TRUNC, S>::value)
+template <class E, bool TRUNC, int S, int W, bool MANY_WAVES>
+__global__ void __launch_bounds__(W * 32, CallTileMinBlocks<E, TRUNC, S, W, MANY_WAVES>::value)
     block_tile_kernel(Params p, TileShape ts) {
-  tile_body<E, TRUNC, S>(p, ts, blockIdx.x);
+  tile_body<E, TRUNC, S, W>(p, ts, blockIdx.x);
 }
 
 // Grouped long-row launch: several calls' tiles in one grid, each call's
@@ -1076,8 +1108,8 @@ struct GroupTileParams {
   TileShape ts[kMaxGroup];
 };
 
-template <bool TRUNC, int S>
-__global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
+template <bool TRUNC, int S, int W>
+__global__ void __launch_bounds__(W * 32, TileMinBlocks<S, W>::value)
     group_tile_kernel(GroupTileParams gp) {
   int c = 0;  // uniform per block
   int64_t b;
@@ -1093,14 +1125,14 @@ __global__ void __launch_bounds__(kChunkThreads, TileMinBlocks<S>::value)
   const Params &p = gp.p[c];
   const TileShape &ts = gp.ts[c];
   switch (gp.kind[c]) {
-    case kGroupGae: tile_body<Gae, TRUNC, S>(p, ts, b); break;
-    case kGroupLambdaReturns: tile_body<LambdaReturns, TRUNC, S>(p, ts, b); break;
-    case kGroupDiscountedReturns: tile_body<DiscountedReturns, TRUNC, S>(p, ts, b); break;
-    case kGroupVTrace: tile_body<VTrace, TRUNC, S>(p, ts, b); break;
-    case kGroupRetrace: tile_body<Retrace, TRUNC, S>(p, ts, b); break;
-    case kGroupEligibilityTraces: tile_body<EligibilityTraces, false, S>(p, ts, b); break;
-    case kGroupEpisodicPrefixSum: tile_body<EpisodicPrefixSum, false, S>(p, ts, b); break;
-    case kGroupGaeAndReturns: tile_body<GaeAndReturns, TRUNC, S>(p, ts, b); break;
+    case kGroupGae: tile_body<Gae, TRUNC, S, W>(p, ts, b); break;
+    case kGroupLambdaReturns: tile_body<LambdaReturns, TRUNC, S, W>(p, ts, b); break;
+    case kGroupDiscountedReturns: tile_body<DiscountedReturns, TRUNC, S, W>(p, ts, b); break;
+    case kGroupVTrace: tile_body<VTrace, TRUNC, S, W>(p, ts, b); break;
+    case kGroupRetrace: tile_body<Retrace, TRUNC, S, W>(p, ts, b); break;
+    case kGroupEligibilityTraces: tile_body<EligibilityTraces, false, S, W>(p, ts, b); break;
+    case kGroupEpisodicPrefixSum: tile_body<EpisodicPrefixSum, false, S, W>(p, ts, b); break;
+    case kGroupGaeAndReturns: tile_body<GaeAndReturns, TRUNC, S, W>(p, ts, b); break;
     default: break;
   }
 }

@@ -18,6 +18,7 @@ struct Plan {
   bool trunc;      // the estimator's optional inputs are present (truncation,
                    // or the affine scan's reset mask)
   bool pdl;        // launch with programmatic stream serialization
+  bool many_waves;  // block tiles: the grid exceeds one wave of 2 blocks per SM
 };
 
 // Raise Kernel's dynamic shared-memory limit to `bytes` on the current
@@ -87,18 +88,22 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
     const dim3 grid((unsigned)((p.N + R - 1) / R));
     return launch_ex(warp_row_kernel<E, TRUNC, S>, grid, dim3(R * 32), 0, s, plan.pdl, p);
   }
-  if constexpr ((E::kBF16Slots | E::kU8Slots) != 0u) {
-    // compact inputs are never staged through shared memory: the tile shape
-    // serves every long-row plan
+  // register tiles: plan.S * 1024 steps as tile_warps warps of tile_strips strips
+  constexpr int TS = tile_strips<S>(), TW = tile_warps<S>();
+  constexpr bool kTwoTileKernels = TW == 16 && three_arrays<E, TRUNC>();
+  const bool tiles = (E::kBF16Slots | E::kU8Slots) != 0u || plan.shape == RLCS_SHAPE_BLOCK_TILE;
+  if (tiles) {  // compact inputs are never staged through shared memory
     TileShape ts{plan.Q > 1 ? ws : nullptr, plan.Q, p.N * plan.Q, 0};
-    return launch_ex(block_tile_kernel<E, TRUNC, S>, dim3((unsigned)(p.N * plan.Q)),
-                     dim3(kChunkThreads), 0, s, plan.pdl, p, ts);
-  } else {
-    if (plan.shape == RLCS_SHAPE_BLOCK_TILE) {
-      TileShape ts{plan.Q > 1 ? ws : nullptr, plan.Q, p.N * plan.Q, 0};
-      return launch_ex(block_tile_kernel<E, TRUNC, S>, dim3((unsigned)(p.N * plan.Q)),
-                       dim3(kChunkThreads), 0, s, plan.pdl, p, ts);
+    const dim3 grid((unsigned)(p.N * plan.Q)), block(TW * 32);
+    if constexpr (kTwoTileKernels) {
+      if (plan.many_waves)
+        return launch_ex(block_tile_kernel<E, TRUNC, TS, TW, true>, grid, block, 0, s, plan.pdl,
+                         p, ts);
     }
+    return launch_ex(block_tile_kernel<E, TRUNC, TS, TW, false>, grid, block, 0, s, plan.pdl, p,
+                     ts);
+  }
+  if constexpr ((E::kBF16Slots | E::kU8Slots) == 0u) {
     constexpr uint32_t kUse = Strips<E, TRUNC, S>::kUse;
     constexpr size_t smem = (size_t)__builtin_popcount(kUse) * kChunkWarps * kStrip * S * 4;
     if (const cudaError_t e = allow_dynamic_smem<block_chunk_kernel<E, TRUNC, S>>(smem)) return e;
@@ -106,6 +111,7 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
     return launch_ex(block_chunk_kernel<E, TRUNC, S>, dim3((unsigned)(p.N * plan.Q)),
                      dim3(kChunkThreads), smem, s, plan.pdl, p, cs);
   }
+  return cudaErrorInvalidValue;  // not reached: compact inputs always take tiles
 }
 
 template <class E, bool TRUNC>

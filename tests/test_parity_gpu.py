@@ -114,6 +114,24 @@ def test_block_shapes_many_rows(rl, dev, shape):
         rl.rlcs_set_shape_override(rl.RLCS_SHAPE_AUTO, 0)
 
 
+@pytest.mark.parametrize("N,T", [(200, 4000), (700, 3001), (40, 9000), (500, 8200)])
+def test_sixteen_warp_tiles_one_and_several_waves(rl, dev, N, T):
+    """4096-step tiles run as 16 warps of 2 strips, with a second, lighter
+    instance for three-array calls whose grid spans more than one wave.
+    These sizes (automatic choice for the first two, 4096-step tiles forced
+    for the others) take both instances, whole-row tiles (T <= 4096, no
+    look-back) and chained ones, with ragged tails."""
+    forced = T > 4096
+    if forced:
+        rl.rlcs_set_shape_override(rl.RLCS_SHAPE_BLOCK_TILE, 4096)
+    try:
+        src = rollout(N, T, 3200 + N + T, p_term=0.003, p_trunc=0.002)
+        check_all(rl, src, to_dev(src, dev), DEFAULT, ALL, True, tag=" [16 warps %dx%d]" % (N, T))
+        check_all(rl, src, to_dev(src, dev), DEFAULT, ALL, False, tag=" [16 warps %dx%d]" % (N, T))
+    finally:
+        rl.rlcs_set_shape_override(rl.RLCS_SHAPE_AUTO, 0)
+
+
 @pytest.mark.parametrize("shape,chunk,T", [(1, 0, 128), (1, 0, 300), (2, 1024, 3000),
                                            (2, 4096, 9000), (2, 2048, 2048), (3, 1024, 3000),
                                            (3, 4096, 9000), (3, 2048, 2048)])
