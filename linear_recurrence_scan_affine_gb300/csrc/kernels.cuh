@@ -976,7 +976,7 @@ __device__ __forceinline__ void tile_body(const Params &p, const TileShape &ts, 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool vec = p.vec != 0;
   const int64_t N = p.N, T = p.T, Q = ts.tiles_per_row;
-  const int64_t r = b / N, row = b - r * N;
+  const int64_t r = div_nonneg(b, N), row = b - r * N;
   const int64_t q = E::kBackward ? (Q - 1 - r) : r;
   const int64_t t0 = q * C;
   const int64_t base = row * T;
@@ -1114,8 +1114,8 @@ __global__ void __launch_bounds__(W * 32, TileMinBlocks<S, W>::value)
   int c = 0;  // uniform per block
   int64_t b;
   if (gp.round_rows > 0) {
-    const int64_t B = blockIdx.x, seg = B / gp.round_rows;  // (round, call) segment
-    const int64_t rnd = seg / gp.n;
+    const int64_t B = blockIdx.x, seg = div_nonneg(B, gp.round_rows);  // (round, call) segment
+    const int64_t rnd = div_nonneg(seg, (int64_t)gp.n);
     c = (int)(seg - rnd * gp.n);
     b = rnd * gp.round_rows + (B - seg * gp.round_rows);
   } else {
@@ -1401,8 +1401,8 @@ __global__ void __launch_bounds__(tm_threads<L>(), tm_min_blocks<L>())
   __shared__ uint32_t s_epoch;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int64_t N = p.N, T = p.T;
-  const int64_t g = blockIdx.x % sh.groups;
-  const int64_t q = blockIdx.x / sh.groups;  // chunk position in scan order
+  const int64_t q = div_nonneg((int64_t)blockIdx.x, sh.groups);  // chunk position in scan order
+  const int64_t g = (int64_t)blockIdx.x - q * sh.groups;
   const int64_t chunk = E::kBackward ? sh.chunks - 1 - q : q;
   const int64_t n = g * kTmEnvs + lane;
   const bool env_ok = n < N;
