@@ -51,6 +51,33 @@ typedef enum {
 } rlcs_shape;
 rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk);
 
+/* The launch plan the library chooses for an [N, T] call (time_major
+ * nonzero: a [T, N] call) with no shape override in force, computed by the
+ * same planner the entry points use and without launching anything, so the
+ * planner can be tested on a machine without a GPU (the SM count is then
+ * taken as 152, GB300's). Fields:
+ *   shape          an rlcs_shape, or RLCS_PLAN_TIME_MAJOR;
+ *   sms            the SM count the plan was made for;
+ *   tile           steps per warp row (128 * strips), row tile or chunk
+ *                  (time-major: 128 steps of 32 environments);
+ *   tiles_per_row  tiles (chunks) per row, chained by look-back when > 1;
+ *   warps          warps per block (warp rows: 1 per row);
+ *   strips         128-step strips per warp (time-major: steps per lane);
+ *   many_waves     block tiles: the grid exceeds one wave of 2 blocks per
+ *                  SM, so three-array calls take the 3-blocks/SM kernel.
+ * RLCS_ERR_INVALID_ARG for N <= 0, T <= 0 or a NULL `info`. */
+#define RLCS_PLAN_TIME_MAJOR 100
+typedef struct {
+  int shape;
+  int sms;
+  int64_t tile;
+  int64_t tiles_per_row;
+  int warps;
+  int strips;
+  int many_waves;
+} rlcs_plan_info;
+rlcs_status rlcs_internal_plan(int64_t N, int64_t T, int time_major, rlcs_plan_info *info);
+
 /* The device address and size of rlcs_gae_noalloc's scratch array on the
  * current device (performing that entry point's one-time set-up there if no
  * call has yet). Tests use it to corrupt the array's header from the host

@@ -9,7 +9,13 @@
 namespace rlcs {
 
 // Internal launch shape for time-major [T, N] inputs (not an rlcs_shape).
-constexpr int kShapeTimeMajor = 100;
+constexpr int kShapeTimeMajor = RLCS_PLAN_TIME_MAJOR;
+
+// Steps per lane of the time-major chunk kernel (measured on GB300): 16
+// warps of 8 steps for short rows, where more warps per chunk finish it
+// sooner; 8 warps of 16 steps from T = 1024, where more bytes in flight per
+// lane pay.
+inline int tm_lane_steps(int64_t T) { return T >= 1024 ? 16 : 8; }
 
 struct Plan {
   int shape;       // RLCS_SHAPE_WARP_ROW, RLCS_SHAPE_BLOCK_CHUNK or RLCS_SHAPE_BLOCK_TILE
@@ -73,10 +79,7 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
       const int64_t groups = (p.N + kTmEnvs - 1) / kTmEnvs;
       const TmShape sh{plan.Q > 1 ? ws : nullptr, groups, plan.Q};
       const dim3 grid((unsigned)(groups * plan.Q));
-      // Measured on GB300: 16 warps of 8 steps for short rows, where more
-      // warps per chunk finish it sooner; 8 warps of 16 steps from T = 1024,
-      // where more bytes in flight per lane pay.
-      if (p.T >= 1024)
+      if (tm_lane_steps(p.T) == 16)
         return launch_ex(time_major_kernel<E, TRUNC, 16>, grid, dim3(tm_threads<16>()), 0, s,
                          plan.pdl, p, sh);
       return launch_ex(time_major_kernel<E, TRUNC, 8>, grid, dim3(tm_threads<8>()), 0, s,

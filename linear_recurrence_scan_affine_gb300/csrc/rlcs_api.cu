@@ -322,6 +322,36 @@ rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk) {
   return RLCS_OK;
 }
 
+rlcs_status rlcs_internal_plan(int64_t N, int64_t T, int time_major, rlcs_plan_info *info) {
+  if (!info || N <= 0 || T <= 0) return RLCS_ERR_INVALID_ARG;
+  if (g_override_shape.load(std::memory_order_relaxed) != RLCS_SHAPE_AUTO)
+    return RLCS_ERR_INVALID_ARG;  // the automatic plan only
+  Plan plan;
+  const rlcs_status st = plan_call(N, T, false, plan, time_major != 0);
+  if (st != RLCS_OK) return st;
+  std::memset(info, 0, sizeof(*info));
+  info->shape = plan.shape;
+  info->sms = sm_count();
+  info->tiles_per_row = plan.Q;
+  info->many_waves = plan.many_waves ? 1 : 0;
+  if (plan.shape == RLCS_SHAPE_WARP_ROW) {
+    info->tile = kStrip * plan.S;
+    info->warps = 1;
+    info->strips = plan.S;
+  } else if (plan.shape == kShapeTimeMajor) {
+    const int L = tm_lane_steps(T);
+    info->tile = kTmChunk;
+    info->warps = kTmChunk / L;
+    info->strips = L;
+  } else {  // block tiles (the automatic long-row shape)
+    info->tile = kMinChunk * plan.S;
+    info->warps = plan.S == 1 ? tile_warps<1>() : (plan.S == 2 ? tile_warps<2>() : tile_warps<4>());
+    info->strips =
+        plan.S == 1 ? tile_strips<1>() : (plan.S == 2 ? tile_strips<2>() : tile_strips<4>());
+  }
+  return RLCS_OK;
+}
+
 rlcs_status rlcs_gae(const float *rewards, const float *values, const float *terminateds,
                      const float *truncateds, const float *next_values,
                      const float *bootstrap_value, float *advantages, int64_t N, int64_t T,

@@ -39,7 +39,7 @@ def test_test_hooks_live_outside_the_product_header():
     product = declared_functions(HEADER)
     internal = declared_functions(INTERNAL)
     for name in ("rlcs_set_shape_override", "rlcs_diag_stream_copy",
-                 "rlcs_internal_noalloc_scratch"):
+                 "rlcs_internal_noalloc_scratch", "rlcs_internal_plan"):
         assert name in internal and name not in product, name
     assert "rlcs_gae_noalloc" in product and "rlcs_gae_noalloc_recover" in product
 
