@@ -1055,15 +1055,23 @@ def run_profile(args):
                           "bytes_per_launch": sum(bytes_per_launch(e_, N, w.T)
                                                   for e_ in w.estimators)}))
         return 0
+    if est in EXTRA:  # the extra entry points' own inputs, drawn as in next_rows
+        from synthetic_rollouts import affine_inputs, compact_rollout
+        src.update(affine_inputs(N, w.T, w.seed + 7))
+        comp, _ = compact_rollout(N, w.T, w.seed + 9, w.p_term)
+        src.update(rewards_bf16=comp["rewards"], values_bf16=comp["values"],
+                   terminateds_u8=comp["terminateds"])
     if est.endswith("_tm"):  # the same arrays stored time-major
         src = {k: (np.ascontiguousarray(v.T) if v.ndim == 2 else v) for k, v in src.items()}
     nsets = max(2, min(ROTATING_SETS, args.sets))
     sets = []
+    row_key = "x_init" if est == "affine_scan" else "bootstrap_value"
     for _ in range(nsets):
         ins, outs = SPECS[est]
-        e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + ("bootstrap_value",)}
+        e = {k: torch.from_numpy(src[k]).to(dev) for k in ins + (row_key,)}
+        odt = torch.int32 if est.startswith("episodic_prefix_sum") else torch.float32
         for o in outs:
-            e[o] = torch.empty_like(e[ins[0]])
+            e[o] = torch.empty(e[ins[0]].shape, dtype=odt, device=dev)
         sets.append(e)
     for i in range(args.warmup + args.steps):
         launch(rl, est, sets[i % nsets], prm)

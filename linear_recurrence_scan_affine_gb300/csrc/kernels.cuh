@@ -1084,6 +1084,203 @@ __global__ void __launch_bounds__(W * 32, CallTileMinBlocks<E, TRUNC, S, W, MANY
   tile_body<E, TRUNC, S, W>(p, ts, blockIdx.x);
 }
 
+// ---------------------------------------------------------------------------
+// Compact-input tiles (backward estimators over bf16 values and uint8
+// masks): eight consecutive steps per lane, so a lane reads each bf16 input
+// with one 16-byte load and each mask with one 8-byte load, and a warp
+// covers 256 steps with one shuffle scan. Needs T % 8 == 0 (a lane's eight
+// steps never straddle two rows) and 16-byte aligned arrays.
+//  * T <= C (the tile length, W * 256 steps: 2048 or 4096): a tile holds
+//    R = C / T whole rows, scanned as one sequence. A row's last step is a
+//    cut (multiplier 0), so nothing carries from a row into the row before
+//    it, and a tile needs no look-back; when T divides 256 no row straddles
+//    two warps either, and the block skips its barrier and shared scan.
+//  * T > C: row tiles in row-interleaved order, chained by the decoupled
+//    look-back as the register tiles are.
+// Each layout comes in two register budgets: MINB = 4 (8 warps) or 2 (16
+// warps) blocks/SM without spills for grids of about one wave, 6 or 3 with
+// a few spilled bytes for larger grids, where resident blocks hide latency.
+// ---------------------------------------------------------------------------
+constexpr int kLane8 = 8;                   // steps per lane
+constexpr int kStrip8 = 32 * kLane8;        // steps per warp
+
+struct CompactShape {
+  WsHeader *ws;           // look-back workspace; NULL unless Q > 1
+  int64_t rows_per_tile;  // R when whole rows share a tile (Q == 1)
+  int64_t tiles_per_row;  // Q
+  int warp_rows;          // 256 % T == 0: every warp holds whole rows
+};
+
+// Eight consecutive elements of slot k from element offset `off` (a multiple
+// of 8, so every access is aligned), converted to float.
+template <class E>
+__device__ __forceinline__ void load8(const Params &p, int k, int64_t off, float (&x)[8]) {
+  if (E::kBF16Slots & bit(k)) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4 *>(
+        reinterpret_cast<const uint16_t *>(p.in[k]) + off));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = __uint_as_float(w[i] << 16);
+      x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  } else if (E::kU8Slots & bit(k)) {
+    const uint2 u = __ldg(reinterpret_cast<const uint2 *>(
+        reinterpret_cast<const uint8_t *>(p.in[k]) + off));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[i] = ((u.x >> (8 * i)) & 0xffu) ? 1.0f : 0.0f;
+      x[4 + i] = ((u.y >> (8 * i)) & 0xffu) ? 1.0f : 0.0f;
+    }
+  } else {
+    const float4 a = __ldg(reinterpret_cast<const float4 *>(p.in[k] + off));
+    const float4 b = __ldg(reinterpret_cast<const float4 *>(p.in[k] + off + 4));
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  }
+}
+
+template <class E, bool TRUNC, int W, int MINB>
+__global__ void __launch_bounds__(W * 32, MINB) compact_tile_kernel(Params p, CompactShape cs) {
+  static_assert(E::kBackward && !E::kPrevD && E::kOuts == 1,
+                "whole rows share a tile only where each row ends in a cut");
+  using P = typename E::Pair;
+  constexpr int C = W * kStrip8;
+  constexpr uint32_t kUse = E::kSlots | (TRUNC ? E::kOptSlots : 0u);
+  __shared__ P s_warp[W];
+  __shared__ float s_carry[W];
+  __shared__ uint32_t s_epoch;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t N = p.N, T = p.T, b = blockIdx.x, Q = cs.tiles_per_row;
+  const int off = warp * kStrip8 + lane * kLane8;  // lane's first step within the tile
+  // The lane's row, its first step's position in the row, and whether it
+  // holds steps at all; the tile's first element and length for the prefetch.
+  int64_t row, pos, r = 0, t_first, t_len;
+  bool valid;
+  if (Q == 1) {
+    const int64_t R = cs.rows_per_tile, row0 = b * R;
+    const int64_t rows = (N - row0 < R) ? (N - row0) : R;
+    const int o = off < (int)(R * T) ? off : 0;  // R * T <= C
+    row = row0 + o / (int)T;
+    pos = o - (row - row0) * T;
+    valid = off < rows * T;
+    t_first = row0 * T;
+    t_len = rows * T;
+  } else {
+    r = div_nonneg(b, N);
+    row = b - r * N;
+    const int64_t q = Q - 1 - r;  // backward: round 0 holds each row's last tile
+    pos = q * C + off;
+    valid = pos < T;
+    t_first = row * T + q * C;
+    t_len = (T - q * C < C) ? (T - q * C) : C;
+  }
+  const int64_t f0 = row * T + pos;  // element offset of the lane's first step
+  if (tid == 0) {
+#pragma unroll
+    for (int k = 0; k < kNumSlots; ++k)
+      if (kUse & bit(k)) prefetch_slot<E>(p, k, t_first, t_len);
+  }
+  pdl_wait();
+
+  float x[kNumSlots][kLane8];
+#pragma unroll
+  for (int k = 0; k < kNumSlots; ++k) {
+    if ((kUse & bit(k)) && valid) {
+      load8<E>(p, k, f0, x[k]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kLane8; ++i) x[k][i] = 0.f;
+    }
+  }
+  const bool row_end = valid && pos + kLane8 == T;  // the lane's last step ends its row
+  // successor values of the lane's last step: the next lane's first step,
+  // or (lane 31) the first step after the warp's span, read directly
+  float nxt[kNumSlots];
+#pragma unroll
+  for (int k = 0; k < kNumSlots; ++k) {
+    nxt[k] = 0.f;
+    if (E::kNext & bit(k)) {
+      const float down = __shfl_down_sync(kFull, x[k][0], 1);
+      if (lane < 31) nxt[k] = down;
+      else if (valid && !row_end) nxt[k] = load_slot1<E>(p, k, f0 + kLane8);
+    }
+  }
+  const float boot = (E::kUsesRowValue && p.boot && row_end) ? __ldg(p.boot + row) : 0.f;
+  if (tid == 0 && Q > 1) s_epoch = ld_relaxed_gpu(&cs.ws->epoch);  // after the loads issue
+  pdl_launch_dependents();
+
+  P e[kLane8];
+#pragma unroll
+  for (int i = 0; i < kLane8; ++i) {
+    StepIn s;
+    s.r = x[kR][i];
+    s.v = x[kV][i];
+    s.q = x[kQ][i];
+    s.lr = x[kLR][i];
+    s.d = x[kD][i];
+    s.tau = x[kTau][i];
+    s.nv = x[kNV][i];
+    s.vn = i + 1 < kLane8 ? x[kV][i + 1] : nxt[kV];
+    s.qn = i + 1 < kLane8 ? x[kQ][i + 1] : nxt[kQ];
+    s.lrn = i + 1 < kLane8 ? x[kLR][i + 1] : nxt[kLR];
+    s.dp = 0.f;
+    s.last = row_end && i == kLane8 - 1;
+    s.first = valid && pos + i == 0;
+    float a0 = 0.f, a1 = 0.f;
+    E::template coeff<TRUNC>(p, s, boot, e[i], a0, a1);
+  }
+  // Steps past a row end or the array end read zeros, so their pairs are
+  // finite; they only compose behind a row's last step (a cut, multiplier 0),
+  // so they never reach an output.
+  P agg = e[kLane8 - 1];
+#pragma unroll
+  for (int i = kLane8 - 2; i >= 0; --i) agg = compose(e[i], agg);
+  if constexpr (E::kConstBeta) agg.m = span_multiplier<kLane8>(e, p.beta8);
+  const P inc = warp_suffix_scan(agg, lane);
+  const P wtot = shfl_idx(inc, 0);
+  const P down = shfl_down(inc, 1);
+  const P excl = lane == 31 ? identity(P{}) : down;
+  // Rows that divide a warp's 256 steps never straddle two warps: each warp
+  // ends at a row end, so nothing passes between warps (uniform per launch).
+  float carry = 0.f;
+  if (!cs.warp_rows) {
+    uint64_t hint = 0;  // the nearest predecessor tile's inclusive word, read early
+    if (warp == 0 && lane == 0 && Q > 1 && r > 0)
+      hint = ld_relaxed_gpu_u64(&reinterpret_cast<WsRecord *>(cs.ws + 1)[b - N].inc);
+    if (lane == 0) s_warp[warp] = wtot;
+    __syncthreads();
+    if (warp == 0) {
+      const P w = (lane < W) ? s_warp[lane] : identity(P{});
+      const P winc = warp_suffix_scan(w, lane);
+      const P tile_agg = shfl_idx(winc, 0);
+      const P x1 = shfl_down(winc, 1);
+      const P nb = (lane >= W - 1) ? identity(P{}) : x1;
+      float X = 0.f;
+      if (Q > 1) X = lookback<P, float>(cs.ws, b, N, r, tile_agg, s_epoch & kTagMask, lane, hint);
+      if (lane < W) s_carry[lane] = apply(nb, X);
+    }
+    __syncthreads();
+    carry = s_carry[warp];
+  }
+
+  float o[kLane8];
+  float nbv = apply(excl, carry);  // the value just after the lane's steps
+#pragma unroll
+  for (int i = kLane8 - 1; i >= 0; --i) {
+    const float A = apply(e[i], nbv);
+    o[i] = E::out0(A, nbv, e[i], 0.f, 0.f);
+    nbv = A;
+  }
+  if (valid) {
+    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.out0) + f0);
+    dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+  }
+  if (Q > 1 && tid == 0) finish_launch(cs.ws, N * Q, s_epoch);
+}
+
 // Grouped long-row launch: several calls' tiles in one grid, each call's
 // tiles in its own row-interleaved order (block b of a call: round b / N of
 // row b % N). All calls share one workspace: a call's look-back records

@@ -210,6 +210,21 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
   Plan plan;
   const rlcs_status st = plan_call(N, T, opt, plan, time_major || t_time_major);
   if (st != RLCS_OK) return st;
+  // Compact inputs (the only calls with element sizes) in rows of whole
+  // 8-step groups take the compact tiles unless a shape is forced.
+  // The tile length follows the register tiles' rule, 2048 steps at least
+  // (8 warps of 256).
+  if (esize != nullptr && p.vec && T % 8 == 0 && !time_major && !t_time_major &&
+      g_override_shape.load(std::memory_order_relaxed) == RLCS_SHAPE_AUTO) {
+    const int64_t tile = pick_chunk(N, T) >= 4096 ? 4096 : 2048;
+    plan.shape = kShapeCompact;
+    plan.S = (int)(tile / kMinChunk);  // 2: 8 warps, 4: 16 warps
+    plan.Q = T <= tile ? 1 : ceil_div(T, tile);
+    plan.rows_per_tile = T <= tile ? tile / T : 0;
+    const int64_t blocks = plan.Q > 1 ? N * plan.Q : ceil_div(N, plan.rows_per_tile);
+    // one wave: 4 blocks of 8 warps or 2 of 16 per SM
+    plan.many_waves = blocks > (tile == 4096 ? 2 : 4) * (int64_t)sm_count();
+  }
   WsHeader *wsh = nullptr;
   if (plan.shape != RLCS_SHAPE_WARP_ROW) {
     if (N * plan.Q >= (int64_t)INT32_MAX) return RLCS_ERR_INVALID_ARG;  // grid x limit

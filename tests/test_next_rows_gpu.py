@@ -123,6 +123,22 @@ def test_gae_compact_sizes(rl, N, T, trunc):
     _compact(rl, N, T, 9000 + T, trunc)
 
 
+@pytest.mark.parametrize("N,T", [(1, 8), (300, 8), (37, 16), (33, 120), (7, 200), (300, 1000),
+                                 (5, 2040), (19, 2048), (3, 2056), (3, 3000), (400, 4096),
+                                 (41, 6000), (9, 8200), (2, 20000), (300, 6000), (20000, 128),
+                                 (37, 132), (9, 1028)])
+@pytest.mark.parametrize("trunc", [False, True])
+def test_gae_compact_eight_step_tiles(rl, N, T, trunc):
+    """The automatic shape for T % 8 == 0: whole rows packed into tiles of
+    8 warps (2048 steps, T <= 2048) or 16 warps (4096 steps, T <= 4096),
+    with a ragged last tile, rows of 8 steps and rows that fill a tile;
+    chained tiles beyond (ragged last tile per row); both register budgets
+    (one-wave and larger grids). T % 8 != 0 and unaligned arrays take the
+    other shapes."""
+    _compact(rl, N, T, 9300 + N + T, trunc)
+    _compact(rl, N, T, 9400 + N + T, trunc, offset=1)
+
+
 @pytest.mark.parametrize("shape,chunk", SHAPES)
 @pytest.mark.parametrize("T", [1, 3, 130, 511, 2049, 7000])
 def test_gae_compact_shapes(rl, shape, chunk, T):
