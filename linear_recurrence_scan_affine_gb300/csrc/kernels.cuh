@@ -20,6 +20,10 @@
 //  * block_chunk_kernel the selectable alternative: chunks staged into shared
 //                       memory by cp.async.bulk (1-D TMA) completing on an
 //                       mbarrier, chained in ticket order.
+//  * compact_tile_kernel compact inputs (bf16, uint8 masks) with T % 8 == 0:
+//                       eight steps per lane, whole rows packed into a tile
+//                       up to 4096 steps (no look-back), chained tiles
+//                       beyond.
 //  * group_row_kernel, group_tile_kernel: several calls in one launch, the
 //                       warp-row or block-tile body per call.
 //  * time_major_kernel, time_major_short_kernel: [T, N] arrays, one
