@@ -1361,10 +1361,18 @@ constexpr int tm_threads() {
 // Resident blocks per SM the compiler must allow: 2 for the 8-warp shape
 // (16 steps per lane), which caps its heaviest instances at 128 registers
 // (measured on GB300: Retrace at 256 x 16384 took 42.7 us uncapped and
-// 31.5 us capped; the others unchanged; 4 blocks per SM was slower for all).
-template <int L>
+// 31.5 us capped; the others unchanged; 4 blocks per SM was slower for
+// all). Calls that move four arrays (GAE, TD(lambda) returns) take 3
+// (80 registers): GAE 5-7% faster at 256 x 16384 and 1024 x 4096; V-trace
+// and Retrace spilled and slowed by up to 1.6x there, and the three-array
+// calls did not move, so they keep 2.
+template <class E, bool TRUNC, int L>
 constexpr int tm_min_blocks() {
-  return L >= 16 ? 2 : 1;
+  return L < 16 ? 1
+                : (__builtin_popcount(E::kSlots | (TRUNC ? E::kOptSlots : 0u)) + E::kOuts == 4 &&
+                           E::kOuts == 1
+                       ? 3
+                       : 2);
 }
 
 struct TmShape {
@@ -1589,7 +1597,7 @@ __device__ __forceinline__ void tm_emit(const Params &p, int64_t b0, int64_t row
 }
 
 template <class E, bool TRUNC, int L>
-__global__ void __launch_bounds__(tm_threads<L>(), tm_min_blocks<L>())
+__global__ void __launch_bounds__(tm_threads<L>(), tm_min_blocks<E, TRUNC, L>())
     time_major_kernel(Params p, TmShape sh) {
   static_assert((E::kBF16Slots | E::kU8Slots) == 0u, "time-major slots are 4-byte words");
   static_assert(kTmChunk % L == 0 && kTmChunk / L <= 32, "whole warps per chunk");
