@@ -20,7 +20,8 @@
 //  * block_chunk_kernel the selectable alternative: chunks staged into shared
 //                       memory by cp.async.bulk (1-D TMA) completing on an
 //                       mbarrier, chained in ticket order.
-//  * compact_tile_kernel compact inputs (bf16, uint8 masks) with T % 8 == 0:
+//  * eight_step_tile_kernel light calls (compact GAE; float32 discounted
+//                       returns) with T % 8 == 0:
 //                       eight steps per lane, whole rows packed into a tile
 //                       up to 4096 steps (no look-back), chained tiles
 //                       beyond.
@@ -1089,11 +1090,12 @@ __global__ void __launch_bounds__(W * 32, CallTileMinBlocks<E, TRUNC, S, W, MANY
 }
 
 // ---------------------------------------------------------------------------
-// Compact-input tiles (backward estimators over bf16 values and uint8
-// masks): eight consecutive steps per lane, so a lane reads each bf16 input
-// with one 16-byte load and each mask with one 8-byte load, and a warp
-// covers 256 steps with one shuffle scan. Needs T % 8 == 0 (a lane's eight
-// steps never straddle two rows) and 16-byte aligned arrays.
+// Eight-step tiles, for light backward calls: compact GAE (bf16 values,
+// uint8 masks) and float32 discounted returns. Each lane owns eight consecutive
+// steps, so it reads each bf16 input with one 16-byte load (a float32 input
+// with two) and a warp covers 256 steps with one shuffle scan. Needs
+// T % 8 == 0 (a lane's eight steps never straddle two rows) and 16-byte
+// aligned arrays.
 //  * T <= C (the tile length, W * 256 steps: 2048 or 4096): a tile holds
 //    R = C / T whole rows, scanned as one sequence. A row's last step is a
 //    cut (multiplier 0), so nothing carries from a row into the row before
@@ -1108,7 +1110,7 @@ __global__ void __launch_bounds__(W * 32, CallTileMinBlocks<E, TRUNC, S, W, MANY
 constexpr int kLane8 = 8;                   // steps per lane
 constexpr int kStrip8 = 32 * kLane8;        // steps per warp
 
-struct CompactShape {
+struct EightShape {
   WsHeader *ws;           // look-back workspace; NULL unless Q > 1
   int64_t rows_per_tile;  // R when whole rows share a tile (Q == 1)
   int64_t tiles_per_row;  // Q
@@ -1145,14 +1147,15 @@ __device__ __forceinline__ void load8(const Params &p, int k, int64_t off, float
 }
 
 template <class E, bool TRUNC, int W, int MINB>
-__global__ void __launch_bounds__(W * 32, MINB) compact_tile_kernel(Params p, CompactShape cs) {
+__global__ void __launch_bounds__(W * 32, MINB) eight_step_tile_kernel(Params p, EightShape cs) {
   static_assert(E::kBackward && !E::kPrevD && E::kOuts == 1,
                 "whole rows share a tile only where each row ends in a cut");
   using P = typename E::Pair;
+  using V = typename ValueOf<P>::type;
   constexpr int C = W * kStrip8;
   constexpr uint32_t kUse = E::kSlots | (TRUNC ? E::kOptSlots : 0u);
   __shared__ P s_warp[W];
-  __shared__ float s_carry[W];
+  __shared__ V s_carry[W];
   __shared__ uint32_t s_epoch;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -1236,8 +1239,8 @@ __global__ void __launch_bounds__(W * 32, MINB) compact_tile_kernel(Params p, Co
     E::template coeff<TRUNC>(p, s, boot, e[i], a0, a1);
   }
   // Steps past a row end or the array end read zeros, so their pairs are
-  // finite; they only compose behind a row's last step (a cut, multiplier 0),
-  // so they never reach an output.
+  // finite; they only compose behind a row's last step (a cut, multiplier
+  // 0), so they never reach an output.
   P agg = e[kLane8 - 1];
 #pragma unroll
   for (int i = kLane8 - 2; i >= 0; --i) agg = compose(e[i], agg);
@@ -1248,7 +1251,7 @@ __global__ void __launch_bounds__(W * 32, MINB) compact_tile_kernel(Params p, Co
   const P excl = lane == 31 ? identity(P{}) : down;
   // Rows that divide a warp's 256 steps never straddle two warps: each warp
   // ends at a row end, so nothing passes between warps (uniform per launch).
-  float carry = 0.f;
+  V carry = V(0);
   if (!cs.warp_rows) {
     uint64_t hint = 0;  // the nearest predecessor tile's inclusive word, read early
     if (warp == 0 && lane == 0 && Q > 1 && r > 0)
@@ -1261,19 +1264,19 @@ __global__ void __launch_bounds__(W * 32, MINB) compact_tile_kernel(Params p, Co
       const P tile_agg = shfl_idx(winc, 0);
       const P x1 = shfl_down(winc, 1);
       const P nb = (lane >= W - 1) ? identity(P{}) : x1;
-      float X = 0.f;
-      if (Q > 1) X = lookback<P, float>(cs.ws, b, N, r, tile_agg, s_epoch & kTagMask, lane, hint);
+      V X = V(0);
+      if (Q > 1) X = lookback<P, V>(cs.ws, b, N, r, tile_agg, s_epoch & kTagMask, lane, hint);
       if (lane < W) s_carry[lane] = apply(nb, X);
     }
     __syncthreads();
     carry = s_carry[warp];
   }
 
+  V nbv = apply(excl, carry);  // the value just after the lane's steps
   float o[kLane8];
-  float nbv = apply(excl, carry);  // the value just after the lane's steps
 #pragma unroll
   for (int i = kLane8 - 1; i >= 0; --i) {
-    const float A = apply(e[i], nbv);
+    const V A = apply(e[i], nbv);
     o[i] = E::out0(A, nbv, e[i], 0.f, 0.f);
     nbv = A;
   }

@@ -9,9 +9,9 @@
 namespace rlcs {
 
 // Internal launch shapes (not rlcs_shape values): time-major [T, N] inputs,
-// and compact-input tiles of eight steps per lane.
+// and tiles of eight steps per lane for light calls.
 constexpr int kShapeTimeMajor = RLCS_PLAN_TIME_MAJOR;
-constexpr int kShapeCompact = RLCS_PLAN_TIME_MAJOR + 1;
+constexpr int kShapeEight = RLCS_PLAN_TIME_MAJOR + 1;
 
 // Steps per lane of the time-major chunk kernel (measured on GB300): 16
 // warps of 8 steps for short rows, where more warps per chunk finish it
@@ -67,28 +67,29 @@ inline cudaError_t launch_ex(K kernel, dim3 grid, dim3 block, size_t smem, cudaS
 
 template <class E, bool TRUNC, int S>
 inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws, cudaStream_t s) {
-  if (plan.shape == kShapeCompact) {
-    if constexpr ((E::kBF16Slots | E::kU8Slots) != 0u && E::kBackward && !E::kPrevD &&
-                  E::kOuts == 1) {
-      const CompactShape cs{plan.Q > 1 ? ws : nullptr, plan.rows_per_tile, plan.Q,
+  if (plan.shape == kShapeEight) {
+    // the estimators the planner routes here (compact GAE, discounted returns)
+    if constexpr ((E::kBF16Slots | E::kU8Slots) != 0u ||
+                  (std::is_same<E, DiscountedReturns>::value && !TRUNC)) {
+      const EightShape cs{plan.Q > 1 ? ws : nullptr, plan.rows_per_tile, plan.Q,
                             (plan.Q == 1 && kStrip8 % p.T == 0) ? 1 : 0};
       const int64_t blocks =
           plan.Q > 1 ? p.N * plan.Q : (p.N + plan.rows_per_tile - 1) / plan.rows_per_tile;
       const dim3 grid((unsigned)blocks);
       if (plan.S == 4) {  // 4096-step tiles: 16 warps
         if (plan.many_waves)
-          return launch_ex(compact_tile_kernel<E, TRUNC, 16, 3>, grid, dim3(512), 0, s, plan.pdl,
+          return launch_ex(eight_step_tile_kernel<E, TRUNC, 16, 3>, grid, dim3(512), 0, s, plan.pdl,
                            p, cs);
-        return launch_ex(compact_tile_kernel<E, TRUNC, 16, 2>, grid, dim3(512), 0, s, plan.pdl, p,
+        return launch_ex(eight_step_tile_kernel<E, TRUNC, 16, 2>, grid, dim3(512), 0, s, plan.pdl, p,
                          cs);
       }
       if (plan.many_waves)
-        return launch_ex(compact_tile_kernel<E, TRUNC, 8, 6>, grid, dim3(256), 0, s, plan.pdl, p,
+        return launch_ex(eight_step_tile_kernel<E, TRUNC, 8, 6>, grid, dim3(256), 0, s, plan.pdl, p,
                          cs);
-      return launch_ex(compact_tile_kernel<E, TRUNC, 8, 4>, grid, dim3(256), 0, s, plan.pdl, p,
+      return launch_ex(eight_step_tile_kernel<E, TRUNC, 8, 4>, grid, dim3(256), 0, s, plan.pdl, p,
                        cs);
     } else {
-      return cudaErrorInvalidValue;  // only compact backward estimators take this shape
+      return cudaErrorInvalidValue;  // the planner sends no other estimator here
     }
   }
   if (plan.shape == kShapeTimeMajor) {

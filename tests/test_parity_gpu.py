@@ -132,6 +132,25 @@ def test_sixteen_warp_tiles_one_and_several_waves(rl, dev, N, T):
         rl.rlcs_set_shape_override(rl.RLCS_SHAPE_AUTO, 0)
 
 
+@pytest.mark.parametrize("N,T", [(1, 8), (300, 8), (37, 16), (33, 120), (7, 200), (300, 1000),
+                                 (5, 2040), (19, 2048), (3, 2056), (3, 3000), (400, 4096),
+                                 (41, 6000), (9, 8200), (2, 20000), (300, 6000), (20000, 128),
+                                 (37, 132)])
+def test_eight_step_tiles_for_light_calls(rl, dev, N, T):
+    """Discounted returns takes tiles of eight steps per lane when T % 8 == 0
+    (whole rows packed into 2048- or 4096-step tiles, chained tiles beyond,
+    both register budgets); rows with T % 8 != 0, unaligned arrays and
+    truncated calls take the other shapes. Traces and the prefix sum run
+    beside it on the same data (the four-step shapes)."""
+    light = ["discounted_returns", "eligibility_traces", "episodic_prefix_sum"]
+    src = rollout(N, T, 3300 + N + T, p_term=0.003, p_trunc=0.002)
+    check_all(rl, src, to_dev(src, dev), DEFAULT, light, False, tag=" [8-step %dx%d]" % (N, T))
+    check_all(rl, src, to_dev(src, dev, offset=1), DEFAULT, light, False,
+              tag=" [unaligned %dx%d]" % (N, T))
+    check_all(rl, src, to_dev(src, dev), DEFAULT, ["discounted_returns"], True,
+              tag=" [truncated %dx%d]" % (N, T))
+
+
 @pytest.mark.parametrize("shape,chunk,T", [(1, 0, 128), (1, 0, 300), (2, 1024, 3000),
                                            (2, 4096, 9000), (2, 2048, 2048), (3, 1024, 3000),
                                            (3, 4096, 9000), (3, 2048, 2048)])
