@@ -153,7 +153,8 @@ def max_over_ranks(dist, value, device=None):
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "clocks.mem,temperature.gpu")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
@@ -185,7 +186,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
+        sm, smax, mem, temp, reasons = [], [], [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         for line in self.lines:
             parts = [p.strip() for p in line.split(",")]
@@ -199,8 +200,16 @@ class ClockSampler:
             for name, val in zip(names, parts[4:8]):
                 if val.lower().startswith("active"):
                     reasons.add(name)
+            for dst, val in ((mem, parts[8:9]), (temp, parts[9:10])):
+                try:
+                    dst.append(float(val[0]))
+                except (IndexError, ValueError):
+                    pass
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(smax) if smax else None,
+                "sm_min_mhz": min(sm) if sm else None,
+                "mem_mhz": statistics.median(mem) if mem else None,
+                "temp_c_max": max(temp) if temp else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
@@ -663,6 +672,12 @@ def run_ours(args):
 
     # the long-row recipes, every estimator alone (same method as above)
     if not args.no_long_t:
+        # SM clocks over each section, beside its numbers (later sections run
+        # after seconds of load and may see lower clocks than the headline)
+        gpu_index = (dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ
+                     else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local]))
+        sect_clock = ClockSampler(gpu_index)
+        sect_clock.start()
         long_t = {}
         for name in ("longT_256x1024", "longT_256x4096", "longT_256x16384", "vlong_8x131072"):
             wl = WORKLOADS[name]
@@ -680,10 +695,14 @@ def run_ours(args):
             long_t[name] = {"step": step_l, "alone": res}
             del src_l
         rl.check_all_workspaces()
+        long_t["clocks"] = sect_clock.stop()
         detail["long_t_sweep"] = long_t
 
-        # entry points beyond the seven, alone, at the bench size and one long size
+        # entry points beyond the seven, alone, at the bench size and one long
+        # size; fp32 GAE on the same data is timed beside compact GAE
         from synthetic_rollouts import affine_inputs, compact_rollout
+        sect_clock = ClockSampler(gpu_index)
+        sect_clock.start()
         next_rows = {}
         for (nN, nT, seed) in ((N, T, w.seed), (256, 16384, 1004)):
             srcn = dict(rollout(nN, nT, seed, w.p_term), **affine_inputs(nN, nT, seed + 7))
@@ -695,6 +714,11 @@ def run_ours(args):
                        for k, v in srcn.items()}
             res = {}
             for est in EXTRA:
+                if est == "gae_compact":
+                    r_ = time_alone(torch, rl, "gae", srcn, dev, stream, prm, l2, nN, nT,
+                                    seconds=0.08)
+                    r_["frac_of_measured_hbm"] = r_["gbs"] / peak
+                    res["gae_fp32_same_data"] = r_
                 r_ = time_alone(torch, rl, est, srcn_tm if est.endswith("_tm") else srcn, dev,
                                 stream, prm, l2, nN, nT, seconds=0.08)
                 r_["frac_of_measured_hbm"] = r_["gbs"] / peak
@@ -702,6 +726,7 @@ def run_ours(args):
             next_rows["%dx%d" % (nN, nT)] = res
             del srcn, srcn_tm
         rl.check_all_workspaces()
+        next_rows["clocks"] = sect_clock.stop()
         detail["next_rows"] = next_rows
 
     e2e = run_e2e(torch, rl, src, dev, stream, prm, order, max(32, min(K, 512)), N, T)
@@ -785,6 +810,7 @@ def time_alone(torch, rl, est, src, dev, stream, prm, l2, N, T, seconds=0.15):
         cold.append(a.elapsed_time(b) / 1e3)
     del g, sets, flush
     torch.cuda.synchronize()
+    torch.cuda.empty_cache()  # the next measurement allocates afresh
     return {"us_per_launch": sec * 1e6, "us_median_of_replays": percentile(each, 0.5) * 1e6,
             "us_p10": percentile(each, 0.1) * 1e6, "us_p90": percentile(each, 0.9) * 1e6,
             "replays": reps,
