@@ -64,7 +64,11 @@ rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk);
  *   warps          warps per block (warp rows: 1 per row);
  *   strips         128-step strips per warp (time-major: steps per lane);
  *   many_waves     block tiles: the grid exceeds one wave of 2 blocks per
- *                  SM, so three-array calls take the 3-blocks/SM kernel.
+ *                  SM, so three-array calls take the 3-blocks/SM kernel;
+ *   envs           time-major: environments per block (32, or 8 for few
+ *                  environments; as chosen for calls that move four or more
+ *                  arrays, while three-array calls over more than 128
+ *                  environments keep 32 from T = 8192).
  * RLCS_ERR_INVALID_ARG for N <= 0, T <= 0 or a NULL `info`. */
 #define RLCS_PLAN_TIME_MAJOR 100
 typedef struct {
@@ -75,6 +79,7 @@ typedef struct {
   int warps;
   int strips;
   int many_waves;
+  int envs;
 } rlcs_plan_info;
 rlcs_status rlcs_internal_plan(int64_t N, int64_t T, int time_major, rlcs_plan_info *info);
 

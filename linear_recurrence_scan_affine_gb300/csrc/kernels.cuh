@@ -1714,6 +1714,131 @@ __global__ void __launch_bounds__(tm_threads<L>(), tm_min_blocks<E, TRUNC, L>())
   if (chained && threadIdx.x == 0) finish_launch(sh.ws, sh.groups * sh.chunks, s_epoch);
 }
 
+// Time-major rows of few environment groups: 8 environments per block over
+// a 512-step chunk, so an environment's chain has a quarter of the links of
+// the 128-step chunks. Lane l of warp w owns environment 8*g + (l % 8) and
+// the 16 steps 64*w + 16*(l / 8) .. +15 of the chunk; lanes 0..7 read the 8
+// environments' words at one step, so every access moves whole 32-byte
+// sectors. A warp composes its four runs per environment with two shuffle
+// rounds, the 8 warps meet in shared memory, and warp 0 runs the look-back
+// for the 8 environments (lanes 0..7).
+constexpr int kTmNarrowEnvs = 8;
+constexpr int kTmNarrowL = 16;                // steps per lane
+constexpr int kTmNarrowWarps = 8;
+constexpr int kTmNarrowChunk = kTmNarrowWarps * 4 * kTmNarrowL;  // 512 steps
+
+template <class E, bool TRUNC>
+__global__ void __launch_bounds__(kTmNarrowWarps * 32, tm_min_blocks<E, TRUNC, kTmNarrowL>())
+    time_major_narrow_kernel(Params p, TmShape sh) {
+  static_assert((E::kBF16Slots | E::kU8Slots) == 0u, "time-major slots are 4-byte words");
+  using P = typename E::Pair;
+  using V = typename ValueOf<P>::type;
+  constexpr int L = kTmNarrowL, kWarps = kTmNarrowWarps, kE = kTmNarrowEnvs;
+  __shared__ P s_agg[kWarps][kE];
+  __shared__ V s_in[kWarps][kE];
+  __shared__ TmSlices<P, V, kWarps> s_sl;
+  __shared__ uint32_t s_epoch;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int ev = lane & (kE - 1), run = lane >> 3;  // environment in the block, run in the warp
+  const int64_t N = p.N, T = p.T;
+  const int64_t q = div_nonneg((int64_t)blockIdx.x, sh.groups);  // chunk position in scan order
+  const int64_t g = (int64_t)blockIdx.x - q * sh.groups;
+  const int64_t chunk = E::kBackward ? sh.chunks - 1 - q : q;
+  const int64_t n = g * kE + ev;
+  const bool env_ok = n < N;
+  const int64_t tw = chunk * kTmNarrowChunk + (int64_t)warp * 4 * L;  // the warp's first step
+  const int64_t ts = tw + (int64_t)run * L;                            // this lane's first step
+  const bool chained = sh.chunks > 1;
+  // uniform across the warp: all four runs interior and the group full
+  const bool full = tw > 0 && tw + 4 * L < T && (g + 1) * kE <= N;
+  const int64_t rowb = N * 4;
+  const int64_t b0 = (ts * N + n) * 4;  // byte offset of step ts of this lane's environment
+
+  pdl_wait();
+  TmRaw<L> raw;
+  if (full)
+    tm_load<E, TRUNC, true, L>(p, b0, rowb, ts, T, env_ok, raw);
+  else
+    tm_load<E, TRUNC, false, L>(p, b0, rowb, ts, T, env_ok, raw);
+  const float boot = (E::kUsesRowValue && p.boot && env_ok) ? __ldg(p.boot + n) : 0.f;
+  if (chained && threadIdx.x == 0) s_epoch = ld_relaxed_gpu(&sh.ws->epoch);
+  pdl_launch_dependents();  // also keeps the loads above ahead of the arithmetic
+  P e[L];
+  float aux0[L], aux1[L];
+  if (full)
+    tm_build<E, TRUNC, true, L>(p, raw, ts, T, boot, e, aux0, aux1);
+  else
+    tm_build<E, TRUNC, false, L>(p, raw, ts, T, boot, e, aux0, aux1);
+
+  P agg = identity(P{});
+  if (E::kBackward) {
+#pragma unroll
+    for (int j = L - 1; j >= 0; --j) agg = compose(e[j], agg);
+  } else {
+#pragma unroll
+    for (int j = 0; j < L; ++j) agg = compose(e[j], agg);
+  }
+  if constexpr (E::kConstBeta) agg.m = span_multiplier<L>(e, const_beta_power<L>(p));
+  // the warp's four runs of each environment (lanes ev, ev+8, ev+16, ev+24)
+  P inc = agg, excl, wagg;
+  if (E::kBackward) {
+#pragma unroll
+    for (int off = 8; off < 32; off <<= 1) {
+      const P o = shfl_down(inc, off);
+      if (lane + off < 32) inc = compose(inc, o);
+    }
+    wagg = shfl_idx(inc, ev);
+    const P x = shfl_down(inc, 8);
+    excl = (run == 3) ? identity(P{}) : x;
+  } else {
+#pragma unroll
+    for (int off = 8; off < 32; off <<= 1) {
+      const P o = shfl_up(inc, off);
+      if (lane >= off) inc = compose(inc, o);
+    }
+    wagg = shfl_idx(inc, 24 + ev);
+    const P x = shfl_up(inc, 8);
+    excl = (run == 0) ? identity(P{}) : x;
+  }
+  if (run == 0) s_agg[warp][ev] = wagg;
+  __syncthreads();
+
+  // the chunk's pair (warp 0, lanes 0..7): warps outer-first from the scan origin side
+  P cagg = identity(P{});
+  if (warp == 0 && lane < kE) {
+    if (E::kBackward) {
+      for (int w = kWarps - 1; w >= 0; --w) cagg = compose(s_agg[w][lane], cagg);
+    } else {
+      for (int w = 0; w < kWarps; ++w) cagg = compose(s_agg[w][lane], cagg);
+    }
+  }
+  V X = V(0);
+  if (chained)  // uniform over the block: every thread takes part
+    X = tm_lookback<P, V, 1, kWarps>(sh.ws, (q * sh.groups + g) * kE, sh.groups * kE, q, cagg,
+                                     s_epoch & kTagMask, lane, warp, lane < kE && env_ok, s_sl);
+  if (warp == 0 && lane < kE) {
+    if (E::kBackward) {
+      for (int w = kWarps - 1; w >= 0; --w) {
+        s_in[w][lane] = X;
+        X = apply(s_agg[w][lane], X);
+      }
+    } else {
+      for (int w = 0; w < kWarps; ++w) {
+        s_in[w][lane] = X;
+        X = apply(s_agg[w][lane], X);
+      }
+    }
+  }
+  __syncthreads();
+
+  const V nb = apply(excl, s_in[warp][ev]);  // value adjacent to this lane's run, origin side
+  if (full)
+    tm_emit<E, true, L>(p, b0, rowb, ts, T, env_ok, nb, e, aux0, aux1);
+  else
+    tm_emit<E, false, L>(p, b0, rowb, ts, T, env_ok, nb, e, aux0, aux1);
+  if (chained && threadIdx.x == 0) finish_launch(sh.ws, sh.groups * sh.chunks, s_epoch);
+}
+
 // Short time-major rows (T <= 128): one chunk, no look-back, and 16
 // environments per block so that the grid has twice the blocks of the
 // 32-environment shape. Lane l of warp w owns environment 16*g + (l % 16)

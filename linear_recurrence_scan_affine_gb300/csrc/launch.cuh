@@ -19,6 +19,20 @@ constexpr int kShapeEight = RLCS_PLAN_TIME_MAJOR + 1;
 // lane pay.
 inline int tm_lane_steps(int64_t T) { return T >= 1024 ? 16 : 8; }
 
+// Time-major calls with few environments take 8 environments per block over
+// 512-step chunks (a quarter of the chain links of the 32-environment
+// shape). Measured on GB300 (GAE / V-trace / discounted returns, us): 8 x
+// 131072 14.0 / 15.3 / 12.9 against 29.8 / 36.1 / 27.8; 64 x 16384 9.7 /
+// 10.9 / 8.4 against 11.9 / 13.2 / 11.1; 256 x 4096 8.2 / 9.5 / 6.7 against
+// 9.3 / 10.5 / 8.5; 256 x 16384 19.5 / 29.0 / 19.8 against 20.9 / 28.9 /
+// 18.7, so calls that move three arrays keep the 32-environment shape above
+// 128 environments from T = 8192 on (128 x 16384 discounted returns: 12.6
+// narrow against 13.2); from N = 512 the narrow shape was slower
+// (1024 x 4096 GAE 18.9 against 18.0).
+inline bool tm_narrow(int64_t N, int64_t T, bool three_arrays) {
+  return N <= 256 && T >= 2048 && (T <= 8192 || N <= 128 || !three_arrays);
+}
+
 struct Plan {
   int shape;       // RLCS_SHAPE_WARP_ROW, RLCS_SHAPE_BLOCK_CHUNK or RLCS_SHAPE_BLOCK_TILE
   int S;           // strips per warp: 1, 2 or 4
@@ -103,6 +117,13 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
         const dim3 grid((unsigned)((p.N + kTmShortEnvs - 1) / kTmShortEnvs));
         return launch_ex(time_major_short_kernel<E, TRUNC>, grid, dim3(kTmShortWarps * 32), 0, s,
                          plan.pdl, p);
+      }
+      if (tm_narrow(p.N, p.T, three_arrays<E, TRUNC>())) {
+        const int64_t g8 = (p.N + kTmNarrowEnvs - 1) / kTmNarrowEnvs;
+        const int64_t q8 = (p.T + kTmNarrowChunk - 1) / kTmNarrowChunk;
+        const TmShape sh8{q8 > 1 ? ws : nullptr, g8, q8};
+        return launch_ex(time_major_narrow_kernel<E, TRUNC>, dim3((unsigned)(g8 * q8)),
+                         dim3(kTmNarrowWarps * 32), 0, s, plan.pdl, p, sh8);
       }
       const int64_t groups = (p.N + kTmEnvs - 1) / kTmEnvs;
       const TmShape sh{plan.Q > 1 ? ws : nullptr, groups, plan.Q};

@@ -363,10 +363,19 @@ rlcs_status rlcs_internal_plan(int64_t N, int64_t T, int time_major, rlcs_plan_i
     info->warps = 1;
     info->strips = plan.S;
   } else if (plan.shape == kShapeTimeMajor) {
-    const int L = tm_lane_steps(T);
-    info->tile = kTmChunk;
-    info->warps = kTmChunk / L;
-    info->strips = L;
+    if (tm_narrow(N, T, false)) {
+      info->tile = kTmNarrowChunk;
+      info->warps = kTmNarrowWarps;
+      info->strips = kTmNarrowL;
+      info->envs = kTmNarrowEnvs;
+      info->tiles_per_row = ceil_div(T, kTmNarrowChunk);
+    } else {
+      const int L = tm_lane_steps(T);
+      info->tile = kTmChunk;
+      info->warps = kTmChunk / L;
+      info->strips = L;
+      info->envs = kTmEnvs;
+    }
   } else {  // block tiles (the automatic long-row shape)
     info->tile = kMinChunk * plan.S;
     info->warps = plan.S == 1 ? tile_warps<1>() : (plan.S == 2 ? tile_warps<2>() : tile_warps<4>());

@@ -16,7 +16,9 @@ The rules under test:
     of two blocks per SM, 2048-step tiles (8 warps of 2 strips) otherwise;
   * many_waves: N * tiles_per_row > 2 * SMs;
   * time-major: chunks of 128 steps of 32 environments, 16 warps of 8 steps
-    below T = 1024 and 8 warps of 16 steps from there.
+    below T = 1024 and 8 warps of 16 steps from there; with at most 256
+    environments and T >= 2048, chunks of 512 steps of 8 environments
+    (8 warps of 4 runs of 16 steps).
 """
 import ctypes
 
@@ -30,7 +32,7 @@ WARP_ROW, BLOCK_CHUNK, BLOCK_TILE, TIME_MAJOR = 1, 2, 3, 100
 class PlanInfo(ctypes.Structure):
     _fields_ = [("shape", ctypes.c_int), ("sms", ctypes.c_int), ("tile", ctypes.c_int64),
                 ("tiles_per_row", ctypes.c_int64), ("warps", ctypes.c_int),
-                ("strips", ctypes.c_int), ("many_waves", ctypes.c_int)]
+                ("strips", ctypes.c_int), ("many_waves", ctypes.c_int), ("envs", ctypes.c_int)]
 
 
 @pytest.fixture(scope="module")
@@ -105,11 +107,19 @@ def test_the_recipes(plan):
 
 @pytest.mark.parametrize("N,T,chunks,lane_steps", [(4096, 128, 1, 8), (7, 1, 1, 8),
                                                     (33, 129, 2, 8), (256, 1023, 8, 8),
-                                                    (256, 1024, 8, 16), (8, 131072, 1024, 16)])
+                                                    (256, 1024, 8, 16), (257, 2048, 16, 16),
+                                                    (4096, 4096, 32, 16), (256, 2047, 16, 16)])
 def test_time_major_chunks(plan, N, T, chunks, lane_steps):
     p = plan(N, T, time_major=True)
-    assert (p.shape, p.tile, p.tiles_per_row, p.strips, p.warps) == (
-        TIME_MAJOR, 128, chunks, lane_steps, 128 // lane_steps)
+    assert (p.shape, p.tile, p.tiles_per_row, p.strips, p.warps, p.envs) == (
+        TIME_MAJOR, 128, chunks, lane_steps, 128 // lane_steps, 32)
+
+
+@pytest.mark.parametrize("N,T", [(8, 131072), (1, 2048), (256, 2048), (256, 16384), (100, 5000)])
+def test_time_major_few_environments_take_narrow_chunks(plan, N, T):
+    p = plan(N, T, time_major=True)
+    assert (p.shape, p.tile, p.tiles_per_row, p.strips, p.warps, p.envs) == (
+        TIME_MAJOR, 512, -(-T // 512), 16, 8, 8)
 
 
 def test_bad_arguments(plan):
