@@ -55,7 +55,10 @@ rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk);
  * nonzero: a [T, N] call) with no shape override in force, computed by the
  * same planner the entry points use and without launching anything, so the
  * planner can be tested on a machine without a GPU (the SM count is then
- * taken as 152, GB300's). Fields:
+ * taken as 152, GB300's). It describes the estimators' common plan: compact
+ * GAE and float32 discounted returns without truncation take tiles of eight
+ * steps per lane instead where T % 8 == 0 and the arrays are 16-byte
+ * aligned, which this query does not report. Fields:
  *   shape          an rlcs_shape, or RLCS_PLAN_TIME_MAJOR;
  *   sms            the SM count the plan was made for;
  *   tile           steps per warp row (128 * strips), row tile or chunk
