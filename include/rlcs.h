@@ -234,10 +234,10 @@ rlcs_status rlcs_gae_and_returns(const float *rewards, const float *values,
  * instead of 16 (13 instead of 24 with truncation). bootstrap_value stays
  * float32 [N]. bf16 to fp32 conversion is exact; the arithmetic is fp32.
  * Rows with T % 8 == 0 and 16-byte aligned arrays run eight steps per lane
- * (one 16-byte load per bf16 input): up to T = 2048 whole rows share a
- * 2048-step tile and the call needs no workspace; longer rows chain
- * 2048-step tiles through the workspace. Other calls take the warp-row
- * shape (T <= 512) or the register tiles. */
+ * (one 16-byte load per bf16 input): up to T = 4096 whole rows share a tile
+ * of 1024, 2048 or 4096 steps and the call needs no workspace; longer rows
+ * chain tiles through the workspace. Other calls take the warp-row shape
+ * (T <= 512) or the register tiles. */
 rlcs_status rlcs_gae_compact(const uint16_t *rewards, const uint16_t *values,
                              const uint8_t *terminateds, const uint8_t *truncateds,
                              const uint16_t *next_values, const float *bootstrap_value,

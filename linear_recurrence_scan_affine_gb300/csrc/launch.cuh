@@ -90,6 +90,13 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
       const int64_t blocks =
           plan.Q > 1 ? p.N * plan.Q : (p.N + plan.rows_per_tile - 1) / plan.rows_per_tile;
       const dim3 grid((unsigned)blocks);
+      if (plan.S == 1) {  // 1024-step tiles: 4 warps
+        if (plan.many_waves)
+          return launch_ex(eight_step_tile_kernel<E, TRUNC, 4, 12>, grid, dim3(128), 0, s,
+                           plan.pdl, p, cs);
+        return launch_ex(eight_step_tile_kernel<E, TRUNC, 4, 8>, grid, dim3(128), 0, s, plan.pdl,
+                         p, cs);
+      }
       if (plan.S == 4) {  // 4096-step tiles: 16 warps
         if (plan.many_waves)
           return launch_ex(eight_step_tile_kernel<E, TRUNC, 16, 3>, grid, dim3(512), 0, s, plan.pdl,

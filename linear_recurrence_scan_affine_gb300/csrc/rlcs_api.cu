@@ -220,19 +220,22 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
   // (forward; 4096 x 128 2.30 against 2.08 us, 256 x 16384 13.2 against
   // 12.8), GAE, TD(lambda) returns and Retrace in float32 (4096 x 128 2.64
   // against 2.57, 256 x 16384 14.7 against 14.3 for GAE).
-  // The tile length follows the register tiles' rule, 2048 steps at least
-  // (8 warps of 256).
+  // The tile length follows the register tiles' rule: 1024 steps (4 warps)
+  // for rows up to 1024 steps, measured against 2048 (us, compact GAE /
+  // discounted returns): 1024 x 1024 3.28 / 3.37 against 3.46 / 3.51,
+  // 16384 x 512 17.0 / 16.7 against 18.0 / 17.4, 4096 x 128 2.44 / 2.36
+  // against 2.40 / 2.45, 256 x 1024 2.40 / 2.21 against 2.30 / 2.14.
   const bool eight = esize != nullptr || (!opt && launch == launch_discounted_returns);
   if (eight && p.vec && T % 8 == 0 && !time_major && !t_time_major &&
       g_override_shape.load(std::memory_order_relaxed) == RLCS_SHAPE_AUTO) {
-    const int64_t tile = pick_chunk(N, T) >= 4096 ? 4096 : 2048;
+    const int64_t tile = T <= 1024 ? 1024 : (pick_chunk(N, T) >= 4096 ? 4096 : 2048);
     plan.shape = kShapeEight;
-    plan.S = (int)(tile / kMinChunk);  // 2: 8 warps, 4: 16 warps
+    plan.S = (int)(tile / kMinChunk);  // 1: 4 warps, 2: 8 warps, 4: 16 warps
     plan.Q = T <= tile ? 1 : ceil_div(T, tile);
     plan.rows_per_tile = T <= tile ? tile / T : 0;
     const int64_t blocks = plan.Q > 1 ? N * plan.Q : ceil_div(N, plan.rows_per_tile);
-    // one wave: 4 blocks of 8 warps or 2 of 16 per SM
-    plan.many_waves = blocks > (tile == 4096 ? 2 : 4) * (int64_t)sm_count();
+    // one wave: 8 blocks of 4 warps, 4 of 8 or 2 of 16 per SM
+    plan.many_waves = blocks > (tile == 4096 ? 2 : (tile == 2048 ? 4 : 8)) * (int64_t)sm_count();
   }
   WsHeader *wsh = nullptr;
   if (plan.shape != RLCS_SHAPE_WARP_ROW) {

@@ -135,7 +135,7 @@ def test_sixteen_warp_tiles_one_and_several_waves(rl, dev, N, T):
 @pytest.mark.parametrize("N,T", [(1, 8), (300, 8), (37, 16), (33, 120), (7, 200), (300, 1000),
                                  (5, 2040), (19, 2048), (3, 2056), (3, 3000), (400, 4096),
                                  (41, 6000), (9, 8200), (2, 20000), (300, 6000), (20000, 128),
-                                 (37, 132)])
+                                 (37, 132), (3, 1024), (700, 512), (13000, 256)])
 def test_eight_step_tiles_for_light_calls(rl, dev, N, T):
     """Discounted returns takes tiles of eight steps per lane when T % 8 == 0
     (whole rows packed into 2048- or 4096-step tiles, chained tiles beyond,
