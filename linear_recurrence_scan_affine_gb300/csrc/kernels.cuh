@@ -1724,17 +1724,21 @@ __global__ void __launch_bounds__(tm_threads<L>(), tm_min_blocks<E, TRUNC, L>())
 // rounds, the 8 warps meet in shared memory, and warp 0 runs the look-back
 // for the 8 environments (lanes 0..7).
 constexpr int kTmNarrowEnvs = 8;
-constexpr int kTmNarrowL = 16;                // steps per lane
+constexpr int kTmNarrowL = 16;                // steps per lane (long rows)
 constexpr int kTmNarrowWarps = 8;
 constexpr int kTmNarrowChunk = kTmNarrowWarps * 4 * kTmNarrowL;  // 512 steps
+template <int L>
+constexpr int tm_narrow_chunk() {
+  return kTmNarrowWarps * 4 * L;
+}
 
-template <class E, bool TRUNC>
-__global__ void __launch_bounds__(kTmNarrowWarps * 32, tm_min_blocks<E, TRUNC, kTmNarrowL>())
+template <class E, bool TRUNC, int L>
+__global__ void __launch_bounds__(kTmNarrowWarps * 32, tm_min_blocks<E, TRUNC, L>())
     time_major_narrow_kernel(Params p, TmShape sh) {
   static_assert((E::kBF16Slots | E::kU8Slots) == 0u, "time-major slots are 4-byte words");
   using P = typename E::Pair;
   using V = typename ValueOf<P>::type;
-  constexpr int L = kTmNarrowL, kWarps = kTmNarrowWarps, kE = kTmNarrowEnvs;
+  constexpr int kWarps = kTmNarrowWarps, kE = kTmNarrowEnvs;
   __shared__ P s_agg[kWarps][kE];
   __shared__ V s_in[kWarps][kE];
   __shared__ TmSlices<P, V, kWarps> s_sl;
@@ -1747,7 +1751,7 @@ __global__ void __launch_bounds__(kTmNarrowWarps * 32, tm_min_blocks<E, TRUNC, k
   const int64_t chunk = E::kBackward ? sh.chunks - 1 - q : q;
   const int64_t n = g * kE + ev;
   const bool env_ok = n < N;
-  const int64_t tw = chunk * kTmNarrowChunk + (int64_t)warp * 4 * L;  // the warp's first step
+  const int64_t tw = chunk * tm_narrow_chunk<L>() + (int64_t)warp * 4 * L;  // the warp's first step
   const int64_t ts = tw + (int64_t)run * L;                            // this lane's first step
   const bool chained = sh.chunks > 1;
   // uniform across the warp: all four runs interior and the group full

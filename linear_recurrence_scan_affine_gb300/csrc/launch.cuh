@@ -129,9 +129,10 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
         const int64_t g8 = (p.N + kTmNarrowEnvs - 1) / kTmNarrowEnvs;
         const int64_t q8 = (p.T + kTmNarrowChunk - 1) / kTmNarrowChunk;
         const TmShape sh8{q8 > 1 ? ws : nullptr, g8, q8};
-        return launch_ex(time_major_narrow_kernel<E, TRUNC>, dim3((unsigned)(g8 * q8)),
+        return launch_ex(time_major_narrow_kernel<E, TRUNC, kTmNarrowL>, dim3((unsigned)(g8 * q8)),
                          dim3(kTmNarrowWarps * 32), 0, s, plan.pdl, p, sh8);
       }
+
       const int64_t groups = (p.N + kTmEnvs - 1) / kTmEnvs;
       const TmShape sh{plan.Q > 1 ? ws : nullptr, groups, plan.Q};
       const dim3 grid((unsigned)(groups * plan.Q));
