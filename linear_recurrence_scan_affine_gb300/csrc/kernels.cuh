@@ -1148,7 +1148,7 @@ __device__ __forceinline__ void load8(const Params &p, int k, int64_t off, float
 }
 
 template <class E, bool TRUNC, int W, int MINB>
-__global__ void __launch_bounds__(W * 32, MINB) eight_step_tile_kernel(Params p, EightShape cs) {
+__global__ void __launch_bounds__(W * 32, MINB) eight_step_tile_kernel(Params p, EightShape es) {
   static_assert(E::kBackward && !E::kPrevD && E::kOuts == 1,
                 "whole rows share a tile only where each row ends in a cut");
   using P = typename E::Pair;
@@ -1160,14 +1160,14 @@ __global__ void __launch_bounds__(W * 32, MINB) eight_step_tile_kernel(Params p,
   __shared__ uint32_t s_epoch;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t N = p.N, T = p.T, b = blockIdx.x, Q = cs.tiles_per_row;
+  const int64_t N = p.N, T = p.T, b = blockIdx.x, Q = es.tiles_per_row;
   const int off = warp * kStrip8 + lane * kLane8;  // lane's first step within the tile
   // The lane's row, its first step's position in the row, and whether it
   // holds steps at all; the tile's first element and length for the prefetch.
   int64_t row, pos, r = 0, t_first, t_len;
   bool valid;
   if (Q == 1) {
-    const int64_t R = cs.rows_per_tile, row0 = b * R;
+    const int64_t R = es.rows_per_tile, row0 = b * R;
     const int64_t rows = (N - row0 < R) ? (N - row0) : R;
     const int o = off < (int)(R * T) ? off : 0;  // R * T <= C
     row = row0 + o / (int)T;
@@ -1216,7 +1216,7 @@ __global__ void __launch_bounds__(W * 32, MINB) eight_step_tile_kernel(Params p,
     }
   }
   const float boot = (E::kUsesRowValue && p.boot && row_end) ? __ldg(p.boot + row) : 0.f;
-  if (tid == 0 && Q > 1) s_epoch = ld_relaxed_gpu(&cs.ws->epoch);  // after the loads issue
+  if (tid == 0 && Q > 1) s_epoch = ld_relaxed_gpu(&es.ws->epoch);  // after the loads issue
   pdl_launch_dependents();
 
   P e[kLane8];
@@ -1253,10 +1253,10 @@ __global__ void __launch_bounds__(W * 32, MINB) eight_step_tile_kernel(Params p,
   // Rows that divide a warp's 256 steps never straddle two warps: each warp
   // ends at a row end, so nothing passes between warps (uniform per launch).
   V carry = V(0);
-  if (!cs.warp_rows) {
+  if (!es.warp_rows) {
     uint64_t hint = 0;  // the nearest predecessor tile's inclusive word, read early
     if (warp == 0 && lane == 0 && Q > 1 && r > 0)
-      hint = ld_relaxed_gpu_u64(&reinterpret_cast<WsRecord *>(cs.ws + 1)[b - N].inc);
+      hint = ld_relaxed_gpu_u64(&reinterpret_cast<WsRecord *>(es.ws + 1)[b - N].inc);
     if (lane == 0) s_warp[warp] = wtot;
     __syncthreads();
     if (warp == 0) {
@@ -1266,7 +1266,7 @@ __global__ void __launch_bounds__(W * 32, MINB) eight_step_tile_kernel(Params p,
       const P x1 = shfl_down(winc, 1);
       const P nb = (lane >= W - 1) ? identity(P{}) : x1;
       V X = V(0);
-      if (Q > 1) X = lookback<P, V>(cs.ws, b, N, r, tile_agg, s_epoch & kTagMask, lane, hint);
+      if (Q > 1) X = lookback<P, V>(es.ws, b, N, r, tile_agg, s_epoch & kTagMask, lane, hint);
       if (lane < W) s_carry[lane] = apply(nb, X);
     }
     __syncthreads();
@@ -1286,7 +1286,7 @@ __global__ void __launch_bounds__(W * 32, MINB) eight_step_tile_kernel(Params p,
     dst[0] = make_float4(o[0], o[1], o[2], o[3]);
     dst[1] = make_float4(o[4], o[5], o[6], o[7]);
   }
-  if (Q > 1 && tid == 0) finish_launch(cs.ws, N * Q, s_epoch);
+  if (Q > 1 && tid == 0) finish_launch(es.ws, N * Q, s_epoch);
 }
 
 // Grouped long-row launch: several calls' tiles in one grid, each call's

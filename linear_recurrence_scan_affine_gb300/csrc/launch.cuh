@@ -85,7 +85,7 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
     // the estimators the planner routes here (compact GAE, discounted returns)
     if constexpr ((E::kBF16Slots | E::kU8Slots) != 0u ||
                   (std::is_same<E, DiscountedReturns>::value && !TRUNC)) {
-      const EightShape cs{plan.Q > 1 ? ws : nullptr, plan.rows_per_tile, plan.Q,
+      const EightShape es{plan.Q > 1 ? ws : nullptr, plan.rows_per_tile, plan.Q,
                             (plan.Q == 1 && kStrip8 % p.T == 0) ? 1 : 0};
       const int64_t blocks =
           plan.Q > 1 ? p.N * plan.Q : (p.N + plan.rows_per_tile - 1) / plan.rows_per_tile;
@@ -93,22 +93,22 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
       if (plan.S == 1) {  // 1024-step tiles: 4 warps
         if (plan.many_waves)
           return launch_ex(eight_step_tile_kernel<E, TRUNC, 4, 12>, grid, dim3(128), 0, s,
-                           plan.pdl, p, cs);
+                           plan.pdl, p, es);
         return launch_ex(eight_step_tile_kernel<E, TRUNC, 4, 8>, grid, dim3(128), 0, s, plan.pdl,
-                         p, cs);
+                         p, es);
       }
       if (plan.S == 4) {  // 4096-step tiles: 16 warps
         if (plan.many_waves)
           return launch_ex(eight_step_tile_kernel<E, TRUNC, 16, 3>, grid, dim3(512), 0, s, plan.pdl,
-                           p, cs);
+                           p, es);
         return launch_ex(eight_step_tile_kernel<E, TRUNC, 16, 2>, grid, dim3(512), 0, s, plan.pdl, p,
-                         cs);
+                         es);
       }
       if (plan.many_waves)
         return launch_ex(eight_step_tile_kernel<E, TRUNC, 8, 6>, grid, dim3(256), 0, s, plan.pdl, p,
-                         cs);
+                         es);
       return launch_ex(eight_step_tile_kernel<E, TRUNC, 8, 4>, grid, dim3(256), 0, s, plan.pdl, p,
-                       cs);
+                       es);
     } else {
       return cudaErrorInvalidValue;  // the planner sends no other estimator here
     }
