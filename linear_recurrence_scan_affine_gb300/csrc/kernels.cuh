@@ -1716,29 +1716,34 @@ __global__ void __launch_bounds__(tm_threads<L>(), tm_min_blocks<E, TRUNC, L>())
 }
 
 // Time-major rows of few environment groups: 8 environments per block over
-// a 512-step chunk, so an environment's chain has a quarter of the links of
-// the 128-step chunks. Lane l of warp w owns environment 8*g + (l % 8) and
-// the 16 steps 64*w + 16*(l / 8) .. +15 of the chunk; lanes 0..7 read the 8
-// environments' words at one step, so every access moves whole 32-byte
-// sectors. A warp composes its four runs per environment with two shuffle
-// rounds, the 8 warps meet in shared memory, and warp 0 runs the look-back
-// for the 8 environments (lanes 0..7).
+// a 512- or 1024-step chunk, so an environment's chain has a quarter or an
+// eighth of the links of the 128-step chunks. Lane l of warp w owns
+// environment 8*g + (l % 8) and the 16 steps 64*w + 16*(l / 8) .. +15 of the
+// chunk; lanes 0..7 read the 8 environments' words at one step, so every
+// access moves whole 32-byte sectors. A warp composes its four runs per
+// environment with two shuffle rounds, the warps meet in shared memory, and
+// warp 0 runs the look-back for the 8 environments (lanes 0..7).
 constexpr int kTmNarrowEnvs = 8;
-constexpr int kTmNarrowL = 16;                // steps per lane (long rows)
-constexpr int kTmNarrowWarps = 8;
-constexpr int kTmNarrowChunk = kTmNarrowWarps * 4 * kTmNarrowL;  // 512 steps
-template <int L>
+constexpr int kTmNarrowL = 16;                // steps per lane
+// Warps per block: 8 (512-step chunks), or 16 (1024-step chunks, half the
+// chain links) when the grid fits in one block per SM, where fewer links
+// matter more than resident blocks.
+template <int W, int L>
 constexpr int tm_narrow_chunk() {
-  return kTmNarrowWarps * 4 * L;
+  return W * 4 * L;
+}
+template <class E, bool TRUNC, int W, int L>
+constexpr int tm_narrow_min_blocks() {
+  return tm_min_blocks<E, TRUNC, L>() * 8 / W > 0 ? tm_min_blocks<E, TRUNC, L>() * 8 / W : 1;
 }
 
-template <class E, bool TRUNC, int L>
-__global__ void __launch_bounds__(kTmNarrowWarps * 32, tm_min_blocks<E, TRUNC, L>())
+template <class E, bool TRUNC, int W, int L>
+__global__ void __launch_bounds__(W * 32, tm_narrow_min_blocks<E, TRUNC, W, L>())
     time_major_narrow_kernel(Params p, TmShape sh) {
   static_assert((E::kBF16Slots | E::kU8Slots) == 0u, "time-major slots are 4-byte words");
   using P = typename E::Pair;
   using V = typename ValueOf<P>::type;
-  constexpr int kWarps = kTmNarrowWarps, kE = kTmNarrowEnvs;
+  constexpr int kWarps = W, kE = kTmNarrowEnvs;
   __shared__ P s_agg[kWarps][kE];
   __shared__ V s_in[kWarps][kE];
   __shared__ TmSlices<P, V, kWarps> s_sl;
@@ -1751,7 +1756,7 @@ __global__ void __launch_bounds__(kTmNarrowWarps * 32, tm_min_blocks<E, TRUNC, L
   const int64_t chunk = E::kBackward ? sh.chunks - 1 - q : q;
   const int64_t n = g * kE + ev;
   const bool env_ok = n < N;
-  const int64_t tw = chunk * tm_narrow_chunk<L>() + (int64_t)warp * 4 * L;  // the warp's first step
+  const int64_t tw = chunk * tm_narrow_chunk<W, L>() + (int64_t)warp * 4 * L;  // the warp's first step
   const int64_t ts = tw + (int64_t)run * L;                            // this lane's first step
   const bool chained = sh.chunks > 1;
   // uniform across the warp: all four runs interior and the group full

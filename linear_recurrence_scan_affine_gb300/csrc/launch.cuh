@@ -20,9 +20,11 @@ constexpr int kShapeEight = RLCS_PLAN_TIME_MAJOR + 1;
 inline int tm_lane_steps(int64_t T) { return T >= 1024 ? 16 : 8; }
 
 // Time-major calls with few environments take 8 environments per block over
-// 512-step chunks (a quarter of the chain links of the 32-environment
-// shape). Measured on GB300 (GAE / V-trace / discounted returns, us): 8 x
-// 131072 14.0 / 15.3 / 12.9 against 29.8 / 36.1 / 27.8; 64 x 16384 9.7 /
+// 512- or 1024-step chunks (a quarter or an eighth of the chain links of the
+// 32-environment shape; the planner picks 1024 when that grid fits in one
+// block per SM). Measured on GB300 with 512-step chunks (GAE / V-trace /
+// discounted returns, us): 8 x 131072 14.0 / 15.3 / 12.9 against 29.8 /
+// 36.1 / 27.8; 64 x 16384 9.7 /
 // 10.9 / 8.4 against 11.9 / 13.2 / 11.1; 256 x 4096 8.2 / 9.5 / 6.7 against
 // 9.3 / 10.5 / 8.5; 256 x 16384 19.5 / 29.0 / 19.8 against 20.9 / 28.9 /
 // 18.7, so calls that move three arrays keep the 32-environment shape above
@@ -41,7 +43,8 @@ struct Plan {
                    // or the affine scan's reset mask)
   bool pdl;        // launch with programmatic stream serialization
   bool many_waves;  // block tiles: the grid exceeds one wave of 2 blocks per SM
-  int64_t rows_per_tile;  // compact tiles holding whole rows (Q == 1)
+  int64_t rows_per_tile;  // eight-step tiles holding whole rows (Q == 1)
+  bool tm_wide;           // time-major, few environments: 16-warp chunks
 };
 
 // Raise Kernel's dynamic shared-memory limit to `bytes` on the current
@@ -127,10 +130,19 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
       }
       if (tm_narrow(p.N, p.T, three_arrays<E, TRUNC>())) {
         const int64_t g8 = (p.N + kTmNarrowEnvs - 1) / kTmNarrowEnvs;
-        const int64_t q8 = (p.T + kTmNarrowChunk - 1) / kTmNarrowChunk;
+        constexpr int L = kTmNarrowL;
+        if (plan.tm_wide) {
+          constexpr int64_t chunk = tm_narrow_chunk<16, L>();
+          const int64_t q8 = (p.T + chunk - 1) / chunk;
+          const TmShape sh8{q8 > 1 ? ws : nullptr, g8, q8};
+          return launch_ex(time_major_narrow_kernel<E, TRUNC, 16, L>, dim3((unsigned)(g8 * q8)),
+                           dim3(16 * 32), 0, s, plan.pdl, p, sh8);
+        }
+        constexpr int64_t chunk = tm_narrow_chunk<8, L>();
+        const int64_t q8 = (p.T + chunk - 1) / chunk;
         const TmShape sh8{q8 > 1 ? ws : nullptr, g8, q8};
-        return launch_ex(time_major_narrow_kernel<E, TRUNC, kTmNarrowL>, dim3((unsigned)(g8 * q8)),
-                         dim3(kTmNarrowWarps * 32), 0, s, plan.pdl, p, sh8);
+        return launch_ex(time_major_narrow_kernel<E, TRUNC, 8, L>, dim3((unsigned)(g8 * q8)),
+                         dim3(8 * 32), 0, s, plan.pdl, p, sh8);
       }
 
       const int64_t groups = (p.N + kTmEnvs - 1) / kTmEnvs;

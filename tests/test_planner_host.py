@@ -17,8 +17,9 @@ The rules under test:
   * many_waves: N * tiles_per_row > 2 * SMs;
   * time-major: chunks of 128 steps of 32 environments, 16 warps of 8 steps
     below T = 1024 and 8 warps of 16 steps from there; with at most 256
-    environments and T >= 2048, chunks of 512 steps of 8 environments
-    (8 warps of 4 runs of 16 steps).
+    environments and T >= 2048, chunks of 8 environments: 1024 steps (16
+    warps of 4 runs of 16 steps) when that grid fits in one block per SM,
+    512 steps (8 warps) otherwise.
 """
 import ctypes
 
@@ -115,11 +116,17 @@ def test_time_major_chunks(plan, N, T, chunks, lane_steps):
         TIME_MAJOR, 128, chunks, lane_steps, 128 // lane_steps, 32)
 
 
-@pytest.mark.parametrize("N,T", [(8, 131072), (1, 2048), (256, 2048), (256, 16384), (100, 5000)])
+@pytest.mark.parametrize("N,T", [(8, 131072), (1, 2048), (256, 2048), (256, 16384), (100, 5000),
+                                 (128, 16384), (152, 8192)])
 def test_time_major_few_environments_take_narrow_chunks(plan, N, T):
     p = plan(N, T, time_major=True)
+    # 16 warps (1024-step chunks) when that grid fits in one block per SM
+    wide = -(-N // 8) * -(-T // 1024) <= p.sms
+    tile, warps = (1024, 16) if wide else (512, 8)
     assert (p.shape, p.tile, p.tiles_per_row, p.strips, p.warps, p.envs) == (
-        TIME_MAJOR, 512, -(-T // 512), 16, 8, 8)
+        TIME_MAJOR, tile, -(-T // tile), 16, warps, 8)
+    if p.sms == 152:
+        assert wide == ((N, T) not in ((256, 16384), (128, 16384)))
 
 
 def test_bad_arguments(plan):

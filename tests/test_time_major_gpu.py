@@ -4,8 +4,8 @@ Inputs are drawn [N, T] as everywhere else, transposed to [T, N] for the
 GPU, and the outputs transposed back and compared element by element with
 the float64 oracle at the usual bar (1e-4 relative; the prefix sum
 bit-exact). A block owns 32 environments and one chunk of T (128 steps),
-or, with at most 256 environments and T >= 2048, 8 environments and 512
-steps; chunks of the same environments are linked by a look-back through
+or, with at most 256 environments and T >= 2048, 8 environments and 512 or
+1024 steps; chunks of the same environments are linked by a look-back through
 the workspace. Sizes cover ragged environment groups (N not a multiple of
 32 or 8), exact group and chunk edges, ragged and many-chunk T (chains of
 up to 1024 chunks), both warp shapes (8-step spans below T = 1024, 16-step
@@ -22,7 +22,8 @@ from tests.parity_common import TOL, TOL_VLONG, compare
 pytestmark = pytest.mark.gpu
 
 SIZES = [(4096, 128), (1000, 300), (7, 1), (33, 129), (256, 1030), (9, 4097), (32, 128),
-         (31, 129), (64, 16384), (48, 1023), (5, 2048), (100, 2600), (255, 9001), (257, 2048)]
+         (31, 129), (64, 16384), (48, 1023), (5, 2048), (100, 2600), (255, 9001), (257, 2048),
+         (200, 20000), (17, 3000)]
 PRM = dict(gamma=0.99, lambda_=0.95, rho_bar=1.0, c_bar=1.0)
 
 
