@@ -39,7 +39,8 @@ rlcs_status rlcs_diag_stream_copy(const float *const *inputs, int n_inputs, floa
  *                          staged into shared memory by bulk copy (TMA),
  *                          chunks chained by decoupled look-back.
  * Setting an override forces a shape and, for the two block shapes, a tile
- * or chunk length of 1024, 2048 or 4096 steps (0 lets the library choose),
+ * or chunk length of 1024, 2048 or 4096 steps, or 8192 for the register
+ * tiles (0 lets the library choose),
  * for every later call in this process until reset with RLCS_SHAPE_AUTO.
  * Not thread-safe with concurrent calls. Returns RLCS_ERR_INVALID_ARG for an
  * unknown shape or length. */

@@ -10,8 +10,8 @@
 //  * warp_row_kernel    one warp per row (T <= 512): inputs go straight to
 //                       registers with 128-bit loads; no shared memory.
 //  * block_tile_kernel  the default for longer rows: one block per row tile
-//                       (8 warps of 1 or 2 strips: 1024 or 2048 steps; 16
-//                       warps of 2 strips: 4096 steps), inputs in registers,
+//                       (8 warps of 1 or 2 strips: 1024 or 2048 steps; 16 or
+//                       32 warps of 2 strips: 4096 or 8192 steps), inputs in registers,
 //                       warp aggregates composed in shared memory, the tiles of a
 //                       row chained in a single pass by a decoupled look-back
 //                       through the workspace (self-validating 64-bit
@@ -919,15 +919,16 @@ struct TileShape {
 };
 
 // Tile layouts: W warps of S strips, W * 128 * S steps per tile. 1024- and
-// 2048-step tiles are 8 warps of 1 or 2 strips; 4096-step tiles are 16
-// warps of 2 strips, which keeps the per-thread state of the 2048-step tile
+// 2048-step tiles are 8 warps of 1 or 2 strips; 4096- and 8192-step tiles
+// are 16 or 32 warps of 2 strips, which keeps the per-thread state of the
+// 2048-step tile
 // (measured on GB300 against 8 warps of 4 strips at 2 blocks/SM: 256 x 4096
 // single calls 3-28% faster, where a row is one tile and needs no
 // look-back, 8 x 131072 4-10% faster; the 256 x 4096 grouped step 25.6
 // against 26.5 us).
 template <int S>
 constexpr int tile_warps() {
-  return S >= 4 ? 16 : kChunkWarps;
+  return S >= 8 ? 32 : (S >= 4 ? 16 : kChunkWarps);
 }
 template <int S>
 constexpr int tile_strips() {
@@ -938,7 +939,7 @@ constexpr int tile_strips() {
 // 16-warp tiles and 4 for 8 warps of 2 strips (64 registers), 6 for 1024-step
 // tiles (40), so one block's look-back overlaps the others' loads.
 template <int S, int W> struct TileMinBlocks {
-  static constexpr int value = W >= 16 ? 2 : (S >= 2 ? 4 : 6);
+  static constexpr int value = W >= 32 ? 1 : (W >= 16 ? 2 : (S >= 2 ? 4 : 6));
 };
 // Single calls of estimators that move at most four arrays: 8-warp 2048-step
 // tiles at 5 blocks/SM (48 registers, a few bytes spilled). Measured on

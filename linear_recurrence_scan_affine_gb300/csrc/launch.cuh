@@ -175,7 +175,7 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
     return launch_ex(block_tile_kernel<E, TRUNC, TS, TW, false>, grid, block, 0, s, plan.pdl, p,
                      ts);
   }
-  if constexpr ((E::kBF16Slots | E::kU8Slots) == 0u) {
+  if constexpr ((E::kBF16Slots | E::kU8Slots) == 0u && S <= 4) {
     constexpr uint32_t kUse = Strips<E, TRUNC, S>::kUse;
     constexpr size_t smem = (size_t)__builtin_popcount(kUse) * kChunkWarps * kStrip * S * 4;
     if (const cudaError_t e = allow_dynamic_smem<block_chunk_kernel<E, TRUNC, S>>(smem)) return e;
@@ -192,6 +192,7 @@ inline cudaError_t launch_trunc(const Params &p, const Plan &plan, WsHeader *ws,
     case 1: return launch_shape<E, TRUNC, 1>(p, plan, ws, s);
     case 2: return launch_shape<E, TRUNC, 2>(p, plan, ws, s);
     case 4: return launch_shape<E, TRUNC, 4>(p, plan, ws, s);
+    case 8: return launch_shape<E, TRUNC, 8>(p, plan, ws, s);
     default: return cudaErrorInvalidValue;
   }
 }

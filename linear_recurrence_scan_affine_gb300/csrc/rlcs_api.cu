@@ -144,7 +144,17 @@ rlcs_status plan_call(int64_t N, int64_t T, bool trunc, Plan &plan, bool time_ma
   }
   plan.shape = (ov == RLCS_SHAPE_BLOCK_CHUNK) ? RLCS_SHAPE_BLOCK_CHUNK : RLCS_SHAPE_BLOCK_TILE;
   int64_t chunk = g_override_chunk.load(std::memory_order_relaxed);
-  if (ov == RLCS_SHAPE_AUTO || chunk == 0) chunk = pick_chunk(N, T);
+  if (ov == RLCS_SHAPE_AUTO || chunk == 0) {
+    chunk = pick_chunk(N, T);
+    // Single calls whose rows are long and few enough that 8192-step tiles
+    // (32 warps of 2 strips) fill at most one block per SM: half the chain
+    // links of 4096-step tiles. Measured on GB300 (V-trace / Retrace / GAE,
+    // us): 8 x 131072 8.36 / 8.55 / 6.96 against 9.37 / 9.41 / 8.06;
+    // 64 x 16384 7.28 / 7.04 / 5.57 against 7.75 / 7.57 / 6.11. (Grouped
+    // calls keep 4096 at most.)
+    if (ov == RLCS_SHAPE_AUTO && T > 8192 && N * ceil_div(T, 8192) <= (int64_t)sm_count())
+      chunk = 8192;
+  }
   plan.S = (int)(chunk / kMinChunk);
   plan.Q = ceil_div(T, chunk);
   plan.many_waves = N * plan.Q > 2 * (int64_t)sm_count();
@@ -348,7 +358,8 @@ rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk) {
       shape != RLCS_SHAPE_BLOCK_CHUNK && shape != RLCS_SHAPE_BLOCK_TILE)
     return RLCS_ERR_INVALID_ARG;
   const bool block = shape == RLCS_SHAPE_BLOCK_CHUNK || shape == RLCS_SHAPE_BLOCK_TILE;
-  if (block && !(chunk == 0 || chunk == 1024 || chunk == 2048 || chunk == 4096))
+  const bool tile8192 = shape == RLCS_SHAPE_BLOCK_TILE && chunk == 8192;  // register tiles only
+  if (block && !(chunk == 0 || chunk == 1024 || chunk == 2048 || chunk == 4096 || tile8192))
     return RLCS_ERR_INVALID_ARG;
   g_override_chunk.store(block ? chunk : 0);
   g_override_shape.store(shape);
@@ -388,9 +399,14 @@ rlcs_status rlcs_internal_plan(int64_t N, int64_t T, int time_major, rlcs_plan_i
     }
   } else {  // block tiles (the automatic long-row shape)
     info->tile = kMinChunk * plan.S;
-    info->warps = plan.S == 1 ? tile_warps<1>() : (plan.S == 2 ? tile_warps<2>() : tile_warps<4>());
-    info->strips =
-        plan.S == 1 ? tile_strips<1>() : (plan.S == 2 ? tile_strips<2>() : tile_strips<4>());
+    info->warps = plan.S == 1   ? tile_warps<1>()
+                  : plan.S == 2 ? tile_warps<2>()
+                  : plan.S == 4 ? tile_warps<4>()
+                                : tile_warps<8>();
+    info->strips = plan.S == 1   ? tile_strips<1>()
+                   : plan.S == 2 ? tile_strips<2>()
+                   : plan.S == 4 ? tile_strips<4>()
+                                 : tile_strips<8>();
   }
   return RLCS_OK;
 }

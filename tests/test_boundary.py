@@ -179,6 +179,8 @@ def test_shape_override_validation(lib):
     assert lib.rlcs_set_shape_override(3, 4096) == OK
     assert lib.rlcs_set_shape_override(2, 3000) == INVALID
     assert lib.rlcs_set_shape_override(2, 2048) == OK
+    assert lib.rlcs_set_shape_override(3, 8192) == OK       # register tiles only
+    assert lib.rlcs_set_shape_override(2, 8192) == INVALID
     assert lib.rlcs_set_shape_override(0, 0) == OK
     # warp-row is limited to T <= 512
     assert lib.rlcs_set_shape_override(1, 0) == OK

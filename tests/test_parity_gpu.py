@@ -132,6 +132,21 @@ def test_sixteen_warp_tiles_one_and_several_waves(rl, dev, N, T):
         rl.rlcs_set_shape_override(rl.RLCS_SHAPE_AUTO, 0)
 
 
+@pytest.mark.parametrize("N,T,forced", [(5, 8192, True), (3, 20000, True), (2, 40001, True),
+                                        (40, 9000, False), (76, 16384, False)])
+def test_thirty_two_warp_tiles(rl, dev, N, T, forced):
+    """8192-step tiles (32 warps of 2 strips): forced on ragged rows, and
+    taken by the planner where N * ceil(T / 8192) fits in one block per SM."""
+    if forced:
+        rl.rlcs_set_shape_override(rl.RLCS_SHAPE_BLOCK_TILE, 8192)
+    try:
+        src = rollout(N, T, 3400 + N + T, p_term=0.002, p_trunc=0.001)
+        check_all(rl, src, to_dev(src, dev), DEFAULT, ALL, True, tag=" [32 warps %dx%d]" % (N, T))
+        check_all(rl, src, to_dev(src, dev), DEFAULT, ALL, False, tag=" [32 warps %dx%d]" % (N, T))
+    finally:
+        rl.rlcs_set_shape_override(rl.RLCS_SHAPE_AUTO, 0)
+
+
 @pytest.mark.parametrize("N,T", [(1, 8), (300, 8), (37, 16), (33, 120), (7, 200), (300, 1000),
                                  (5, 2040), (19, 2048), (3, 2056), (3, 3000), (400, 4096),
                                  (41, 6000), (9, 8200), (2, 20000), (300, 6000), (20000, 128),

@@ -12,8 +12,10 @@ The rules under test:
   * T <= 1024 and T <= 2048: one 1024- or 2048-step tile of 8 warps per
     row, so the row needs no look-back;
   * T <= 4096: one 4096-step tile of 16 warps of 2 strips per row;
-  * longer rows: 4096-step tiles while N * ceil(T / 4096) fits in one wave
-    of two blocks per SM, 2048-step tiles (8 warps of 2 strips) otherwise;
+  * longer rows: 8192-step tiles (32 warps of 2 strips) for T > 8192 while
+    N * ceil(T / 8192) fits in one block per SM, else 4096-step tiles while
+    N * ceil(T / 4096) fits in one wave of two blocks per SM, 2048-step
+    tiles (8 warps of 2 strips) otherwise;
   * many_waves: N * tiles_per_row > 2 * SMs;
   * time-major: chunks of 128 steps of 32 environments, 16 warps of 8 steps
     below T = 1024 and 8 warps of 16 steps from there; with at most 256
@@ -82,13 +84,17 @@ def test_rows_up_to_4096_steps_are_one_tile(plan, N, T, tile, warps, strips):
 
 @pytest.mark.parametrize("N,T", [(8, 131072), (64, 16384), (256, 8192), (256, 16384),
                                  (4096, 8192), (3, 10000), (300, 5000), (152, 8192),
-                                 (153, 8192)])
+                                 (153, 8192), (76, 16384), (77, 16385), (152, 8193)])
 def test_longer_rows_chain_tiles(plan, N, T):
     p = plan(N, T)
-    one_wave = N * -(-T // 4096) <= 2 * p.sms
-    tile = 4096 if one_wave else 2048
+    if T > 8192 and N * -(-T // 8192) <= p.sms:
+        tile = 8192
+    elif N * -(-T // 4096) <= 2 * p.sms:
+        tile = 4096
+    else:
+        tile = 2048
     assert p.shape == BLOCK_TILE and p.tile == tile
-    assert (p.warps, p.strips) == ((16, 2) if tile == 4096 else (8, 2))
+    assert (p.warps, p.strips) == {8192: (32, 2), 4096: (16, 2), 2048: (8, 2)}[tile]
     assert p.tiles_per_row == -(-T // tile) and p.tiles_per_row > 1
     assert p.many_waves == int(N * p.tiles_per_row > 2 * p.sms)
 
@@ -97,7 +103,7 @@ def test_the_recipes(plan):
     # the long-row workloads on GB300 (152 SMs)
     p = plan(8, 131072)
     if p.sms == 152:
-        assert (p.tile, p.warps, p.tiles_per_row, p.many_waves) == (4096, 16, 32, 0)
+        assert (p.tile, p.warps, p.tiles_per_row, p.many_waves) == (8192, 32, 16, 0)
         p = plan(256, 16384)
         assert (p.tile, p.warps, p.tiles_per_row, p.many_waves) == (2048, 8, 8, 1)
         p = plan(256, 4096)
