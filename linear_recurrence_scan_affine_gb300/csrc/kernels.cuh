@@ -1097,7 +1097,7 @@ __global__ void __launch_bounds__(W * 32, CallTileMinBlocks<E, TRUNC, S, W, MANY
 // with two) and a warp covers 256 steps with one shuffle scan. Needs
 // T % 8 == 0 (a lane's eight steps never straddle two rows) and 16-byte
 // aligned arrays.
-//  * T <= C (the tile length, W * 256 steps: 1024, 2048 or 4096): a tile holds
+//  * T <= C (the tile length, W * 256 steps: 1024 to 8192): a tile holds
 //    R = C / T whole rows, scanned as one sequence. A row's last step is a
 //    cut (multiplier 0), so nothing carries from a row into the row before
 //    it, and a tile needs no look-back; when T divides 256 no row straddles
@@ -1107,7 +1107,8 @@ __global__ void __launch_bounds__(W * 32, CallTileMinBlocks<E, TRUNC, S, W, MANY
 // Each layout comes in two register budgets: MINB = 8, 4 or 2 blocks/SM
 // (4, 8 or 16 warps) without spills for grids of about one wave, 12, 6 or 3
 // with a few spilled bytes for larger grids, where resident blocks hide
-// latency.
+// latency; 32 warps (8192-step tiles, for few long rows whose grid fits in
+// one block per SM) take the whole register file of an SM.
 // ---------------------------------------------------------------------------
 constexpr int kLane8 = 8;                   // steps per lane
 constexpr int kStrip8 = 32 * kLane8;        // steps per warp

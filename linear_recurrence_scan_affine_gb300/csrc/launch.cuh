@@ -100,6 +100,9 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
         return launch_ex(eight_step_tile_kernel<E, TRUNC, 4, 8>, grid, dim3(128), 0, s, plan.pdl,
                          p, es);
       }
+      if (plan.S == 8)  // 8192-step tiles: 32 warps, one block per SM
+        return launch_ex(eight_step_tile_kernel<E, TRUNC, 32, 1>, grid, dim3(1024), 0, s, plan.pdl,
+                         p, es);
       if (plan.S == 4) {  // 4096-step tiles: 16 warps
         if (plan.many_waves)
           return launch_ex(eight_step_tile_kernel<E, TRUNC, 16, 3>, grid, dim3(512), 0, s, plan.pdl,

@@ -244,14 +244,18 @@ rlcs_status run(Params &p, const float *trunc, const float *next_values, void *c
   const bool eight = esize != nullptr || (!opt && launch == launch_discounted_returns);
   if (eight && p.vec && T % 8 == 0 && !time_major && !t_time_major &&
       g_override_shape.load(std::memory_order_relaxed) == RLCS_SHAPE_AUTO) {
-    const int64_t tile = T <= 1024 ? 1024 : (pick_chunk(N, T) >= 4096 ? 4096 : 2048);
+    const int64_t tile = T <= 1024                                            ? 1024
+                         : (T > 8192 && N * ceil_div(T, 8192) <= (int64_t)sm_count()) ? 8192
+                         : pick_chunk(N, T) >= 4096                                 ? 4096
+                                                                                    : 2048;
     plan.shape = kShapeEight;
-    plan.S = (int)(tile / kMinChunk);  // 1: 4 warps, 2: 8 warps, 4: 16 warps
+    plan.S = (int)(tile / kMinChunk);  // 1: 4 warps, 2: 8, 4: 16, 8: 32
     plan.Q = T <= tile ? 1 : ceil_div(T, tile);
     plan.rows_per_tile = T <= tile ? tile / T : 0;
     const int64_t blocks = plan.Q > 1 ? N * plan.Q : ceil_div(N, plan.rows_per_tile);
-    // one wave: 8 blocks of 4 warps, 4 of 8 or 2 of 16 per SM
-    plan.many_waves = blocks > (tile == 4096 ? 2 : (tile == 2048 ? 4 : 8)) * (int64_t)sm_count();
+    // one wave: 8 blocks of 4 warps, 4 of 8, 2 of 16 or 1 of 32 per SM
+    plan.many_waves =
+        blocks > (tile == 8192 ? 1 : tile == 4096 ? 2 : (tile == 2048 ? 4 : 8)) * (int64_t)sm_count();
   }
   WsHeader *wsh = nullptr;
   if (plan.shape != RLCS_SHAPE_WARP_ROW) {

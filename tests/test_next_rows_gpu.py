@@ -126,7 +126,7 @@ def test_gae_compact_sizes(rl, N, T, trunc):
 @pytest.mark.parametrize("N,T", [(1, 8), (300, 8), (37, 16), (33, 120), (7, 200), (300, 1000),
                                  (5, 2040), (19, 2048), (3, 2056), (3, 3000), (400, 4096),
                                  (41, 6000), (9, 8200), (2, 20000), (300, 6000), (20000, 128),
-                                 (37, 132), (9, 1028), (3, 1024), (700, 512), (13000, 256)])
+                                 (37, 132), (9, 1028), (3, 1024), (700, 512), (13000, 256), (76, 16384)])
 @pytest.mark.parametrize("trunc", [False, True])
 def test_gae_compact_eight_step_tiles(rl, N, T, trunc):
     """The automatic shape for T % 8 == 0: whole rows packed into tiles of

@@ -150,7 +150,7 @@ def test_thirty_two_warp_tiles(rl, dev, N, T, forced):
 @pytest.mark.parametrize("N,T", [(1, 8), (300, 8), (37, 16), (33, 120), (7, 200), (300, 1000),
                                  (5, 2040), (19, 2048), (3, 2056), (3, 3000), (400, 4096),
                                  (41, 6000), (9, 8200), (2, 20000), (300, 6000), (20000, 128),
-                                 (37, 132), (3, 1024), (700, 512), (13000, 256)])
+                                 (37, 132), (3, 1024), (700, 512), (13000, 256), (76, 16384)])
 def test_eight_step_tiles_for_light_calls(rl, dev, N, T):
     """Discounted returns takes tiles of eight steps per lane when T % 8 == 0
     (whole rows packed into 2048- or 4096-step tiles, chained tiles beyond,
