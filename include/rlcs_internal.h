@@ -72,7 +72,12 @@ rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk);
  *   envs           time-major: environments per block (32, or 8 for few
  *                  environments; as chosen for calls that move four or more
  *                  arrays, while three-array calls over more than 128
- *                  environments keep 32 from T = 8192).
+ *                  environments keep 32 from T = 8192);
+ *   lookback_slots time-major: predecessors each warp reads per environment
+ *                  and look-back round (1; 4 for the 8-environment chunks
+ *                  when there are at most 16 environment groups and at
+ *                  least 16 chunks per environment, so a round covers
+ *                  4 x warps predecessors).
  * RLCS_ERR_INVALID_ARG for N <= 0, T <= 0 or a NULL `info`. */
 #define RLCS_PLAN_TIME_MAJOR 100
 typedef struct {
@@ -84,6 +89,7 @@ typedef struct {
   int strips;
   int many_waves;
   int envs;
+  int lookback_slots;
 } rlcs_plan_info;
 rlcs_status rlcs_internal_plan(int64_t N, int64_t T, int time_major, rlcs_plan_info *info);
 

@@ -1383,8 +1383,9 @@ constexpr int tm_min_blocks() {
 
 struct TmShape {
   WsHeader *ws;    // workspace header; NULL when one chunk covers T
-  int64_t groups;  // G = ceil(N / 32)
-  int64_t chunks;  // chunks per environment = ceil(T / kTmChunk)
+  int64_t groups;  // G = ceil(N / 32) (ceil(N / 8) for the 8-environment chunks)
+  int64_t chunks;  // chunks per environment = ceil(T / chunk length)
+  int slots;       // look-back distances per warp and round, per environment (8-environment chunks: 1 or 4)
 };
 
 // One record of a chunk: its inclusive value (kStateInc), its aggregate
@@ -1408,123 +1409,166 @@ __device__ __forceinline__ uint32_t tm_read_record(const WsRecord *r, uint32_t t
 
 template <class P, class V, int kWarps>
 struct TmSlices {
-  P acc[kWarps][32];         // the slice's aggregates composed, up to its stop
-  uint32_t val[kWarps][32];  // the inclusive value's bits where the slice met one
+  P acc[kWarps][32];         // per warp and environment: the warp's records composed, up to its stop
+  uint32_t val[kWarps][32];  // the inclusive value's bits where the warp met one
   uint32_t stop[kWarps][32]; // 0: none, 1: inclusive value, 2: wait ran out, 3: scan origin
-  uint32_t open[32];         // lane still walking (set by warp 0 between rounds)
+  uint32_t open[32];         // environment still walking (set by warp 0 between rounds)
   uint32_t more;
 };
 
-// Decoupled look-back of the time-major tier, one chain per lane
-// (environment), run by the whole block. Lane l's record for this chunk is
-// self + l; its predecessors in scan order are self + l - d*stride for
-// d = 1..npred. Warp 0 publishes the chunk aggregate of every lane. Then,
-// round by round, warp w takes the distances d0 + w*R + 1 .. d0 + (w+1)*R:
-// it reads those records for every lane, waits (bounded) on any not yet
-// published, and composes them nearest first until it meets an inclusive
-// value; warp 0 chains the warps' results in order. One L2 round trip thus
-// brings a window of kWarps*R predecessors for all 32 environments, and the
-// waits on unpublished records run in parallel across the warps. (Many
-// chunks of an environment are in flight at once when there are few
-// environment groups; walking them one record per round trip was the
-// time-major tier's main cost.) On a timeout the status word records
+// Decoupled look-back of the time-major tier, one chain per environment,
+// run by the whole block. A warp's lanes cover 32/kSub environments, lane l
+// taking environment l % (32/kSub) and distance slot l / (32/kSub); the
+// first `slots` (1..kSub) slots read. The record of environment e for this
+// chunk is self + e; its predecessors in scan order are self + e - d*stride
+// for d = 1..npred. Warp 0 publishes the chunk aggregate of every
+// environment. Then, round by round, warp w takes the distances
+// d0 + w*slots + 1 .. d0 + (w+1)*slots, one per reading slot: each lane
+// reads its record, waits (bounded) if it is not yet published, and the
+// slots of an environment combine nearest first (stopping at an inclusive
+// value) with shuffles; warp 0 chains the warps' results in order. One L2
+// round trip thus brings a window of kWarps*slots predecessors for every
+// environment, and the waits on unpublished records run in parallel. (Many chunks of an environment are in flight at once when there
+// are few environment groups; walking them one record per round trip was
+// the time-major tier's main cost.) On a timeout the status word records
 // RLCS_ERR_TIMEOUT and the missing aggregates count as the identity.
-// Inactive lanes (environments past N) neither publish nor wait. Every
-// thread of the block calls this; the value just outside the chunk on its
-// scan-origin side is returned in warp 0, which also publishes the chunk's
-// inclusive value.
-template <class P, class V, int R, int kWarps>
+// Environments past N (env_ok false) neither publish nor wait. Every thread
+// of the block calls this; `agg` is read in warp 0's lanes of slot 0, where
+// the value just outside the chunk on its scan-origin side is returned and
+// the chunk's inclusive value published.
+template <class P, class V, int kSub, int kWarps>
 __device__ V tm_lookback(WsHeader *ws, int64_t self, int64_t stride, int64_t npred, P agg,
-                         uint32_t tag, int lane, int warp, bool active,
+                         uint32_t tag, int lane, int warp, bool env_ok, int slots,
                          TmSlices<P, V, kWarps> &sl) {
-  WsRecord *mine = reinterpret_cast<WsRecord *>(ws + 1) + self + lane;
+  static_assert(kSub == 1 || kSub == 2 || kSub == 4, "distance slots per warp");
+  constexpr int kE = 32 / kSub;  // environments per warp
+  const int env = lane % kE, slot = lane / kE;
+  const int nsub = slots < 1 ? 1 : (slots > kSub ? kSub : slots);
+  const bool owner = warp == 0 && slot == 0;  // publishes and walks for `env`
+  WsRecord *mine = reinterpret_cast<WsRecord *>(ws + 1) + self + env;
   const uint32_t tagA = (tag << 2) | kStateAgg, tagP = (tag << 2) | kStateInc;
   if (npred == 0) {  // the scan origin: nothing before it
-    if (warp == 0 && active) st_relaxed_gpu_u64(&mine->inc, tagged(tagP, vbits(apply(agg, V(0)))));
+    if (owner && env_ok) st_relaxed_gpu_u64(&mine->inc, tagged(tagP, vbits(apply(agg, V(0)))));
     return V(0);
   }
-  if (warp == 0) {
-    if (active) {
+  if (owner) {
+    if (env_ok) {
       st_relaxed_gpu_u64(&mine->m, tagged(tagA, vbits(agg.m)));
       st_relaxed_gpu_u64(&mine->c, tagged(tagA, vbits(agg.c)));
     }
-    sl.open[lane] = active ? 1u : 0u;
+    sl.open[env] = env_ok ? 1u : 0u;
   }
   __syncthreads();
   P acc = identity(P{});
   V X = V(0);
-  bool done = !active, timed_out = false;
-  constexpr int W = R * kWarps;
-  for (int64_t d0 = 0;; d0 += W) {
+  bool done = !(owner && env_ok), timed_out = false;
+  const int window = nsub * kWarps;
+  for (int64_t d0 = 0;; d0 += window) {
     P sacc = identity(P{});
     uint32_t stop = 0u, sval = 0u;
-    if (sl.open[lane]) {
-#pragma unroll 1
-      for (int j = 0; j < R; ++j) {
-        const int64_t d = d0 + warp * R + j + 1;
-        if (d > npred) {  // every predecessor composed: the origin's value is 0
-          stop = 3u;
-          break;
-        }
+    const int64_t d = d0 + warp * nsub + slot + 1;
+    if (slot < nsub && sl.open[env]) {
+      if (d > npred) {  // every predecessor composed: the origin's value is 0
+        stop = 3u;
+      } else {
         const WsRecord *r = mine - d * stride;
-        P e = identity(P{});
-        uint32_t s = tm_read_record<P, V>(r, tagA, tagP, e);
+        uint32_t s = tm_read_record<P, V>(r, tagA, tagP, sacc);
         if (s == 0u) {  // not yet published: wait for it (bounded)
           const uint64_t t0 = globaltimer_ns();
           unsigned backoff = 64;
-          while ((s = tm_read_record<P, V>(r, tagA, tagP, e)) == 0u) {
+          while ((s = tm_read_record<P, V>(r, tagA, tagP, sacc)) == 0u) {
             if (globaltimer_ns() - t0 > kWaitLimitNs) break;
             __nanosleep(backoff);
             if (backoff < 1024) backoff <<= 1;
           }
-          if (s == 0u) {
-            stop = 2u;
-            break;
-          }
         }
-        if (s == kStateInc) {
+        if (s == 0u) {
+          stop = 2u;
+          sacc = identity(P{});
+        } else if (s == kStateInc) {
           stop = 1u;
-          sval = vbits(e.c);
-          break;
+          sval = vbits(sacc.c);
+          sacc = identity(P{});
         }
-        sacc = compose(sacc, e);
       }
     }
-    sl.acc[warp][lane] = sacc;
-    sl.stop[warp][lane] = stop;
-    sl.val[warp][lane] = sval;
+    // the slots of each environment, nearest first: a slot that stopped
+    // hides the farther ones
+#pragma unroll
+    for (int off = kE; off < 32; off <<= 1) {
+      const P o = shfl_down(sacc, off);
+      const uint32_t ostop = __shfl_down_sync(kFull, stop, off);
+      const uint32_t oval = __shfl_down_sync(kFull, sval, off);
+      if (stop == 0u && slot + (off / kE) < nsub) {
+        sacc = compose(sacc, o);
+        stop = ostop;
+        sval = oval;
+      }
+    }
+    if (slot == 0) {
+      sl.acc[warp][env] = sacc;
+      sl.stop[warp][env] = stop;
+      sl.val[warp][env] = sval;
+    }
     __syncthreads();
     if (warp == 0) {
-      for (int w = 0; w < kWarps && !done; ++w) {
-        acc = compose(acc, sl.acc[w][lane]);
-        const uint32_t s = sl.stop[w][lane];
-        if (s == 1u) {
-          V v;
-          vfrom(sl.val[w][lane], v);
-          X = apply(acc, v);
-          done = true;
-        } else if (s != 0u) {  // the origin, or a wait that ran out (missing terms count as identity)
-          X = apply(acc, V(0));
-          done = true;
-          if (s == 2u) timed_out = true;
+      if (slot == 0) {
+        for (int w = 0; w < kWarps && !done; ++w) {
+          acc = compose(acc, sl.acc[w][env]);
+          const uint32_t st = sl.stop[w][env];
+          if (st == 1u) {
+            V v;
+            vfrom(sl.val[w][env], v);
+            X = apply(acc, v);
+            done = true;
+          } else if (st != 0u) {  // the origin, or a wait that ran out (missing terms count as identity)
+            X = apply(acc, V(0));
+            done = true;
+            if (st == 2u) timed_out = true;
+          }
         }
+        sl.open[env] = done ? 0u : 1u;
       }
-      sl.open[lane] = done ? 0u : 1u;
       const bool more = __any_sync(kFull, !done);
       if (lane == 0) sl.more = more ? 1u : 0u;
     }
     __syncthreads();
     if (!sl.more) break;
   }
-  if (warp == 0) {
+  if (owner) {
     if (timed_out) set_status(ws, kStatusTimeout);
-    if (active) st_relaxed_gpu_u64(&mine->inc, tagged(tagP, vbits(apply(agg, X))));
+    if (env_ok) st_relaxed_gpu_u64(&mine->inc, tagged(tagP, vbits(apply(agg, X))));
   }
   return X;
 }
 
 __device__ __forceinline__ float ldg_at(const void *base, int64_t byte_off) {
   return __ldg(reinterpret_cast<const float *>(static_cast<const char *>(base) + byte_off));
+}
+
+// L2 bulk prefetch of rows [t0, t1) of every input slot in the [T, N]
+// layout. Those rows are one contiguous range per slot, read in 32- or
+// 128-byte pieces by the `parts` blocks of that chunk (one per environment
+// group, adjacent in launch order); block `part` prefetches the part-th
+// 16-byte-aligned share, so DRAM sees long runs instead of one sector per
+// row per block. A hint only: issued before the grid-dependency wait (L2 is
+// the coherence point), and a share that is not 16-byte aligned is skipped.
+template <class E, bool TRUNC>
+__device__ __forceinline__ void tm_prefetch(const Params &p, int64_t t0, int64_t t1, int64_t part,
+                                            int64_t parts) {
+  constexpr uint32_t kUse = E::kSlots | (TRUNC ? E::kOptSlots : 0u);
+  const int64_t lo = t0 * p.N * 4, total = (t1 - t0) * p.N * 4;
+  const int64_t share = ((total + parts - 1) / parts + 15) & ~int64_t(15);
+  const int64_t s0 = part * share;
+  int64_t len = total - s0 < share ? total - s0 : share;
+  len &= ~int64_t(15);
+  if (len <= 0) return;
+#pragma unroll
+  for (int k = 0; k < kNumSlots; ++k) {
+    if (!(kUse & bit(k))) continue;
+    const char *a = reinterpret_cast<const char *>(p.in[k]) + lo + s0;
+    if ((reinterpret_cast<uintptr_t>(a) & 15u) == 0) prefetch_l2(a, (uint32_t)len);
+  }
 }
 
 // One warp's span of L steps for its 32 environments. b0 + j*rowb: byte
@@ -1646,6 +1690,17 @@ __global__ void __launch_bounds__(tm_threads<L>(), tm_min_blocks<E, TRUNC, L>())
   const int64_t rowb = N * 4;
   const int64_t b0 = (ts * N + n) * 4;  // byte offset of step ts of this lane's environment
 
+  // The chunk's rows into L2 for calls that move four arrays or more
+  // (measured on GB300, prefetch against none: GAE 1024 x 4096 16.7 / 17.8 us,
+  // 4096 x 512 14.5 / 15.8, V-trace 4096 x 512 17.2 / 19.3); the three-array
+  // calls ran slower with it (discounted returns 4096 x 512 13.8 / 9.9,
+  // 1024 x 16384 60.4 / 50.6, 1024 x 4096 16.8 / 15.5), so they skip it.
+  if constexpr (!three_arrays<E, TRUNC>()) {
+    if (threadIdx.x == 0) {
+      const int64_t c0 = chunk * kTmChunk, c1 = c0 + kTmChunk < T ? c0 + kTmChunk : T;
+      tm_prefetch<E, TRUNC>(p, c0, c1, g, sh.groups);
+    }
+  }
   pdl_wait();
   TmRaw<L> raw;
   if (full)
@@ -1693,7 +1748,7 @@ __global__ void __launch_bounds__(tm_threads<L>(), tm_min_blocks<E, TRUNC, L>())
     // V-trace 28.9 against 30.8, discounted returns 18.7 against 21.1; two
     // or four distances per warp were slower)
     X = tm_lookback<P, V, 1, kWarps>(sh.ws, (q * sh.groups + g) * kTmEnvs, sh.groups * kTmEnvs, q,
-                                     cagg, s_epoch & kTagMask, lane, warp, env_ok, s_sl);
+                                     cagg, s_epoch & kTagMask, lane, warp, env_ok, 1, s_sl);
   if (warp == 0) {
     if (E::kBackward) {
       for (int w = kWarps - 1; w >= 0; --w) {
@@ -1766,6 +1821,14 @@ __global__ void __launch_bounds__(W * 32, tm_narrow_min_blocks<E, TRUNC, W, L>()
   const int64_t rowb = N * 4;
   const int64_t b0 = (ts * N + n) * 4;  // byte offset of step ts of this lane's environment
 
+  // the chunk's rows into L2 (measured on GB300, prefetch against none:
+  // GAE 8 x 131072 10.3 / 11.2 us, 64 x 16384 7.2 / 8.3, 256 x 4096 6.6 /
+  // 7.6; discounted returns 8 x 131072 9.4 / 10.3; 256 x 16384 unchanged)
+  if (threadIdx.x == 0) {
+    const int64_t c0 = chunk * tm_narrow_chunk<W, L>();
+    const int64_t c1 = c0 + tm_narrow_chunk<W, L>() < T ? c0 + tm_narrow_chunk<W, L>() : T;
+    tm_prefetch<E, TRUNC>(p, c0, c1, g, sh.groups);
+  }
   pdl_wait();
   TmRaw<L> raw;
   if (full)
@@ -1826,8 +1889,9 @@ __global__ void __launch_bounds__(W * 32, tm_narrow_min_blocks<E, TRUNC, W, L>()
   }
   V X = V(0);
   if (chained)  // uniform over the block: every thread takes part
-    X = tm_lookback<P, V, 1, kWarps>(sh.ws, (q * sh.groups + g) * kE, sh.groups * kE, q, cagg,
-                                     s_epoch & kTagMask, lane, warp, lane < kE && env_ok, s_sl);
+    X = tm_lookback<P, V, 32 / kE, kWarps>(sh.ws, (q * sh.groups + g) * kE, sh.groups * kE, q,
+                                           cagg, s_epoch & kTagMask, lane, warp, env_ok,
+                                           sh.slots, s_sl);
   if (warp == 0 && lane < kE) {
     if (E::kBackward) {
       for (int w = kWarps - 1; w >= 0; --w) {
@@ -1881,6 +1945,10 @@ __global__ void __launch_bounds__(kTmShortWarps * 32) time_major_short_kernel(Pa
   const int64_t rowb = N * 4;
   const int64_t b0 = (ts * N + n) * 4;  // byte offset of step ts of this lane's environment
 
+  // all T rows into L2, a share per block (measured on GB300 at 4096 x 128:
+  // GAE 2.67 against 3.31 us without, V-trace 3.86 / 4.61, discounted
+  // returns 2.74 / 3.27)
+  if (threadIdx.x == 0) tm_prefetch<E, TRUNC>(p, 0, T, g, (int64_t)gridDim.x);
   pdl_wait();
   TmRaw<L> raw;
   if (full)

@@ -30,9 +30,23 @@ inline int tm_lane_steps(int64_t T) { return T >= 1024 ? 16 : 8; }
 // 18.7, so calls that move three arrays keep the 32-environment shape above
 // 128 environments from T = 8192 on (128 x 16384 discounted returns: 12.6
 // narrow against 13.2); from N = 512 the narrow shape was slower
-// (1024 x 4096 GAE 18.9 against 18.0).
+// (1024 x 4096 GAE 18.9 against 18.0). Re-measured with the chunk prefetch and
+// the wider look-back window: 256 x 16384 discounted returns 19.6 narrow
+// against 18.8, and N = 512 or 1024 narrow 0-17% slower.
 inline bool tm_narrow(int64_t N, int64_t T, bool three_arrays) {
   return N <= 256 && T >= 2048 && (T <= 8192 || N <= 128 || !three_arrays);
+}
+
+// Look-back distances per warp and round for the 8-environment chunks: 4
+// (all 32 lanes read, a window of 4 x warps predecessors per L2 round trip)
+// when few environment groups have long chains, so that many chunks of one
+// environment are in flight at once; else 1 (lanes 0..7). Measured on GB300
+// (GAE and discounted returns, us, 4 against 1): 8 x 131072 8.1 / 10.3 and
+// 7.3 / 9.3; 32 x 65536 13.5 / 14.2 and 12.9 / 14.6; 64 x 16384 6.9 / 7.1
+// and 6.3 / 6.5; with 32 groups, 256 x 16384 GAE 20.0 / 19.4 and
+// 256 x 4096 6.6 / 6.6.
+inline int tm_window_slots(int64_t groups, int64_t chunks) {
+  return groups <= 16 && chunks >= 16 ? 4 : 1;
 }
 
 struct Plan {
@@ -137,19 +151,19 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
         if (plan.tm_wide) {
           constexpr int64_t chunk = tm_narrow_chunk<16, L>();
           const int64_t q8 = (p.T + chunk - 1) / chunk;
-          const TmShape sh8{q8 > 1 ? ws : nullptr, g8, q8};
+          const TmShape sh8{q8 > 1 ? ws : nullptr, g8, q8, tm_window_slots(g8, q8)};
           return launch_ex(time_major_narrow_kernel<E, TRUNC, 16, L>, dim3((unsigned)(g8 * q8)),
                            dim3(16 * 32), 0, s, plan.pdl, p, sh8);
         }
         constexpr int64_t chunk = tm_narrow_chunk<8, L>();
         const int64_t q8 = (p.T + chunk - 1) / chunk;
-        const TmShape sh8{q8 > 1 ? ws : nullptr, g8, q8};
+        const TmShape sh8{q8 > 1 ? ws : nullptr, g8, q8, tm_window_slots(g8, q8)};
         return launch_ex(time_major_narrow_kernel<E, TRUNC, 8, L>, dim3((unsigned)(g8 * q8)),
                          dim3(8 * 32), 0, s, plan.pdl, p, sh8);
       }
 
       const int64_t groups = (p.N + kTmEnvs - 1) / kTmEnvs;
-      const TmShape sh{plan.Q > 1 ? ws : nullptr, groups, plan.Q};
+      const TmShape sh{plan.Q > 1 ? ws : nullptr, groups, plan.Q, 1};
       const dim3 grid((unsigned)(groups * plan.Q));
       if (tm_lane_steps(p.T) == 16)
         return launch_ex(time_major_kernel<E, TRUNC, 16>, grid, dim3(tm_threads<16>()), 0, s,

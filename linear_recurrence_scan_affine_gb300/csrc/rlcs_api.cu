@@ -394,12 +394,14 @@ rlcs_status rlcs_internal_plan(int64_t N, int64_t T, int time_major, rlcs_plan_i
       info->strips = kTmNarrowL;
       info->envs = kTmNarrowEnvs;
       info->tiles_per_row = ceil_div(T, info->tile);
+      info->lookback_slots = tm_window_slots(ceil_div(N, kTmNarrowEnvs), info->tiles_per_row);
     } else {
       const int L = tm_lane_steps(T);
       info->tile = kTmChunk;
       info->warps = kTmChunk / L;
       info->strips = L;
       info->envs = kTmEnvs;
+      info->lookback_slots = 1;
     }
   } else {  // block tiles (the automatic long-row shape)
     info->tile = kMinChunk * plan.S;

@@ -21,7 +21,8 @@ The rules under test:
     below T = 1024 and 8 warps of 16 steps from there; with at most 256
     environments and T >= 2048, chunks of 8 environments: 1024 steps (16
     warps of 4 runs of 16 steps) when that grid fits in one block per SM,
-    512 steps (8 warps) otherwise.
+    512 steps (8 warps) otherwise; their look-back reads four predecessors
+    per warp and round for at most 16 groups of at least 16 chunks, else one.
 """
 import ctypes
 
@@ -35,7 +36,8 @@ WARP_ROW, BLOCK_CHUNK, BLOCK_TILE, TIME_MAJOR = 1, 2, 3, 100
 class PlanInfo(ctypes.Structure):
     _fields_ = [("shape", ctypes.c_int), ("sms", ctypes.c_int), ("tile", ctypes.c_int64),
                 ("tiles_per_row", ctypes.c_int64), ("warps", ctypes.c_int),
-                ("strips", ctypes.c_int), ("many_waves", ctypes.c_int), ("envs", ctypes.c_int)]
+                ("strips", ctypes.c_int), ("many_waves", ctypes.c_int), ("envs", ctypes.c_int),
+                ("lookback_slots", ctypes.c_int)]
 
 
 @pytest.fixture(scope="module")
@@ -133,6 +135,24 @@ def test_time_major_few_environments_take_narrow_chunks(plan, N, T):
         TIME_MAJOR, tile, -(-T // tile), 16, warps, 8)
     if p.sms == 152:
         assert wide == ((N, T) not in ((256, 16384), (128, 16384)))
+
+
+@pytest.mark.parametrize("N,T,slots", [(8, 131072, 4), (64, 16384, 4), (128, 16384, 4),
+                                       (32, 65536, 4), (13, 20000, 4), (100, 40000, 4),
+                                       (256, 16384, 1), (200, 20000, 1), (256, 4096, 1),
+                                       (9, 4097, 1), (129, 16384, 1), (4096, 4096, 1)])
+def test_time_major_lookback_window(plan, N, T, slots):
+    # four predecessors per warp and round for few 8-environment groups
+    # (at most 16) with long chains (at least 16 chunks); one otherwise, and
+    # always one for the 32-environment chunks
+    p = plan(N, T, time_major=True)
+    if p.envs == 8:
+        groups, chunks = -(-N // 8), p.tiles_per_row
+        assert p.lookback_slots == (4 if groups <= 16 and chunks >= 16 else 1)
+    else:
+        assert p.lookback_slots == 1
+    if p.sms == 152:
+        assert p.lookback_slots == slots
 
 
 def test_bad_arguments(plan):

@@ -6,10 +6,13 @@ the float64 oracle at the usual bar (1e-4 relative; the prefix sum
 bit-exact). A block owns 32 environments and one chunk of T (128 steps),
 or, with at most 256 environments and T >= 2048, 8 environments and 512 or
 1024 steps; chunks of the same environments are linked by a look-back through
-the workspace. Sizes cover ragged environment groups (N not a multiple of
-32 or 8), exact group and chunk edges, ragged and many-chunk T (chains of
-up to 1024 chunks), both warp shapes (8-step spans below T = 1024, 16-step
-spans from there), both block shapes, truncations and the degenerate T = 1.
+the workspace, which reads one predecessor per warp and round or, for few
+8-environment groups with long chains, four. Sizes cover ragged environment
+groups (N not a multiple of 32 or 8), exact group and chunk edges, ragged
+and many-chunk T (chains of up to 1024 chunks), both warp shapes (8-step
+spans below T = 1024, 16-step spans from there), both block shapes, both
+look-back windows (13 x 20000 and 100 x 40000 take four distances per warp,
+with a partial last group), truncations and the degenerate T = 1.
 """
 import numpy as np
 import pytest
@@ -23,7 +26,7 @@ pytestmark = pytest.mark.gpu
 
 SIZES = [(4096, 128), (1000, 300), (7, 1), (33, 129), (256, 1030), (9, 4097), (32, 128),
          (31, 129), (64, 16384), (48, 1023), (5, 2048), (100, 2600), (255, 9001), (257, 2048),
-         (200, 20000), (17, 3000)]
+         (200, 20000), (17, 3000), (13, 20000), (100, 40000)]
 PRM = dict(gamma=0.99, lambda_=0.95, rho_bar=1.0, c_bar=1.0)
 
 
