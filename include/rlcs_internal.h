@@ -69,10 +69,8 @@ rlcs_status rlcs_set_shape_override(rlcs_shape shape, int64_t chunk);
  *   strips         128-step strips per warp (time-major: steps per lane);
  *   many_waves     block tiles: the grid exceeds one wave of 2 blocks per
  *                  SM, so three-array calls take the 3-blocks/SM kernel;
- *   envs           time-major: environments per block (32, or 8 for few
- *                  environments; as chosen for calls that move four or more
- *                  arrays, while three-array calls over more than 128
- *                  environments keep 32 from T = 8192);
+ *   envs           time-major: environments per block (32, or 8 for at
+ *                  most 256 environments and T >= 2048);
  *   lookback_slots time-major: predecessors each warp reads per environment
  *                  and look-back round (1; 4 for the 8-environment chunks
  *                  when there are at most 16 environment groups and at

@@ -1364,21 +1364,48 @@ template <int L>
 constexpr int tm_threads() {
   return kTmChunk / L * 32;
 }
-// Resident blocks per SM the compiler must allow: 2 for the 8-warp shape
-// (16 steps per lane), which caps its heaviest instances at 128 registers
-// (measured on GB300: Retrace at 256 x 16384 took 42.7 us uncapped and
-// 31.5 us capped; the others unchanged; 4 blocks per SM was slower for
-// all). Calls that move four arrays (GAE, TD(lambda) returns) take 3
-// (80 registers): GAE 5-7% faster at 256 x 16384 and 1024 x 4096; V-trace
-// and Retrace spilled and slowed by up to 1.6x there, and the three-array
-// calls did not move, so they keep 2.
+// Resident blocks per SM the compiler must allow, for 8-warp blocks (16
+// steps per lane; the 32-environment kernel from T = 1024 and the
+// 8-environment kernel's 512-step chunks) and 16-warp blocks (8 steps per
+// lane, L = 8):
+//  * 2 by default, which caps the heaviest instances at 128 registers
+//    (measured on GB300: Retrace at 256 x 16384 took 42.7 us uncapped and
+//    31.5 us capped);
+//  * 3 (80 registers) for calls that move four arrays with one output
+//    (GAE, TD(lambda) returns): GAE 5-7% faster at 256 x 16384 and
+//    1024 x 4096; V-trace and Retrace spilled and slowed by up to 1.6x there;
+//  * for three-array calls, 4 (64 registers), or 3 for the ones that spill
+//    more there (eligibility traces 24-56 bytes, the affine scan 32-56).
+//    Measured against 2 (us): 8-environment chunks, discounted returns
+//    128 x 16384 9.6 / 11.3, 32 x 65536 11.5 / 13.1, prefix sum 128 x 16384
+//    9.3 / 11.8, 256 x 8192 10.2 / 11.9, traces at 3 128 x 16384 10.5 / 10.9
+//    (10.1 at 4), 32 x 65536 11.7 / 12.8 (12.2 at 4); 32-environment chunks
+//    (which held 3 blocks at 80 registers), discounted returns 1024 x 16384
+//    46.8 / 50.0, 512 x 8192 16.4 / 16.9, prefix sum 1024 x 16384 47.6 /
+//    51.6;
+//  * at L = 8, 1 for four arrays or more, 2 for three-array calls (the prefix
+//    sum used 67 registers uncapped, one 512-thread block per SM).
+template <class E>
+struct TmThreeArrayBlocks {
+  static constexpr int value = 4;
+};
+template <>
+struct TmThreeArrayBlocks<EligibilityTraces> {
+  static constexpr int value = 3;
+};
+template <bool B>
+struct TmThreeArrayBlocks<Affine<B>> {
+  static constexpr int value = 3;
+};
 template <class E, bool TRUNC, int L>
 constexpr int tm_min_blocks() {
-  return L < 16 ? 1
-                : (__builtin_popcount(E::kSlots | (TRUNC ? E::kOptSlots : 0u)) + E::kOuts == 4 &&
-                           E::kOuts == 1
-                       ? 3
-                       : 2);
+  return L < 16 ? (three_arrays<E, TRUNC>() ? 2 : 1)
+         : three_arrays<E, TRUNC>()
+             ? TmThreeArrayBlocks<E>::value
+             : (__builtin_popcount(E::kSlots | (TRUNC ? E::kOptSlots : 0u)) + E::kOuts == 4 &&
+                        E::kOuts == 1
+                    ? 3
+                    : 2);
 }
 
 struct TmShape {
@@ -1389,7 +1416,10 @@ struct TmShape {
 };
 
 // One record of a chunk: its inclusive value (kStateInc), its aggregate
-// pair (kStateAgg), or nothing of this epoch yet (0).
+// pair (kStateAgg), or nothing of this epoch yet (0). The aggregate words
+// are read only when the inclusive word is stale (measured on GB300:
+// reading all three at once was up to 2 us slower, e.g. discounted returns
+// at 256 x 16384 20.7 against 18.7 us).
 template <class P, class V>
 __device__ __forceinline__ uint32_t tm_read_record(const WsRecord *r, uint32_t tagA, uint32_t tagP,
                                                    P &pv) {
@@ -1789,9 +1819,11 @@ template <int W, int L>
 constexpr int tm_narrow_chunk() {
   return W * 4 * L;
 }
+// The 8-environment kernel: the 8-warp shape takes the budgets above; the
+// 16-warp shape (grids of at most one block per SM) takes one block.
 template <class E, bool TRUNC, int W, int L>
 constexpr int tm_narrow_min_blocks() {
-  return tm_min_blocks<E, TRUNC, L>() * 8 / W > 0 ? tm_min_blocks<E, TRUNC, L>() * 8 / W : 1;
+  return W >= 16 ? 1 : tm_min_blocks<E, TRUNC, L>();
 }
 
 template <class E, bool TRUNC, int W, int L>

@@ -22,20 +22,14 @@ inline int tm_lane_steps(int64_t T) { return T >= 1024 ? 16 : 8; }
 // Time-major calls with few environments take 8 environments per block over
 // 512- or 1024-step chunks (a quarter or an eighth of the chain links of the
 // 32-environment shape; the planner picks 1024 when that grid fits in one
-// block per SM). Measured on GB300 with 512-step chunks (GAE / V-trace /
-// discounted returns, us): 8 x 131072 14.0 / 15.3 / 12.9 against 29.8 /
-// 36.1 / 27.8; 64 x 16384 9.7 /
-// 10.9 / 8.4 against 11.9 / 13.2 / 11.1; 256 x 4096 8.2 / 9.5 / 6.7 against
-// 9.3 / 10.5 / 8.5; 256 x 16384 19.5 / 29.0 / 19.8 against 20.9 / 28.9 /
-// 18.7, so calls that move three arrays keep the 32-environment shape above
-// 128 environments from T = 8192 on (128 x 16384 discounted returns: 12.6
-// narrow against 13.2); from N = 512 the narrow shape was slower
-// (1024 x 4096 GAE 18.9 against 18.0). Re-measured with the chunk prefetch and
-// the wider look-back window: 256 x 16384 discounted returns 19.6 narrow
-// against 18.8, and N = 512 or 1024 narrow 0-17% slower.
-inline bool tm_narrow(int64_t N, int64_t T, bool three_arrays) {
-  return N <= 256 && T >= 2048 && (T <= 8192 || N <= 128 || !three_arrays);
-}
+// block per SM). Measured on GB300 (us, 8 against 32 environments per
+// block): GAE 8 x 131072 8.1 against 29.8, 64 x 16384 6.9 against 11.9,
+// 256 x 16384 19.4 against 20.9; with 4 blocks per SM for the three-array
+// calls, discounted returns 256 x 16384 16.5 against 18.7 and 200 x 20000
+// 16.7 against 19.9, prefix sum 16.1 against 19.3 and 16.7 against 20.9.
+// From N = 512 the narrow shape was 0-17% slower (1024 x 4096 GAE 18.8
+// against 16.6).
+inline bool tm_narrow(int64_t N, int64_t T) { return N <= 256 && T >= 2048; }
 
 // Look-back distances per warp and round for the 8-environment chunks: 4
 // (all 32 lanes read, a window of 4 x warps predecessors per L2 round trip)
@@ -145,7 +139,7 @@ inline cudaError_t launch_shape(const Params &p, const Plan &plan, WsHeader *ws,
         return launch_ex(time_major_short_kernel<E, TRUNC>, grid, dim3(kTmShortWarps * 32), 0, s,
                          plan.pdl, p);
       }
-      if (tm_narrow(p.N, p.T, three_arrays<E, TRUNC>())) {
+      if (tm_narrow(p.N, p.T)) {
         const int64_t g8 = (p.N + kTmNarrowEnvs - 1) / kTmNarrowEnvs;
         constexpr int L = kTmNarrowL;
         if (plan.tm_wide) {

@@ -387,7 +387,7 @@ rlcs_status rlcs_internal_plan(int64_t N, int64_t T, int time_major, rlcs_plan_i
     info->warps = 1;
     info->strips = plan.S;
   } else if (plan.shape == kShapeTimeMajor) {
-    if (tm_narrow(N, T, false)) {
+    if (tm_narrow(N, T)) {
       const int W = plan.tm_wide ? 16 : 8;
       info->tile = (int64_t)W * 4 * kTmNarrowL;
       info->warps = W;
