@@ -1523,16 +1523,20 @@ __device__ V tm_lookback(WsHeader *ws, int64_t self, int64_t stride, int64_t npr
       }
     }
     // the slots of each environment, nearest first: a slot that stopped
-    // hides the farther ones
+    // hides the farther ones (nsub is uniform over the block)
+    // (measured on GB300, skipping it for one slot: 256 x 16384 GAE 19.9
+    // against 20.5 us, 256 x 4096 V-trace 8.6 against 9.3)
+    if (nsub > 1) {
 #pragma unroll
-    for (int off = kE; off < 32; off <<= 1) {
-      const P o = shfl_down(sacc, off);
-      const uint32_t ostop = __shfl_down_sync(kFull, stop, off);
-      const uint32_t oval = __shfl_down_sync(kFull, sval, off);
-      if (stop == 0u && slot + (off / kE) < nsub) {
-        sacc = compose(sacc, o);
-        stop = ostop;
-        sval = oval;
+      for (int off = kE; off < 32; off <<= 1) {
+        const P o = shfl_down(sacc, off);
+        const uint32_t ostop = __shfl_down_sync(kFull, stop, off);
+        const uint32_t oval = __shfl_down_sync(kFull, sval, off);
+        if (stop == 0u && slot + (off / kE) < nsub) {
+          sacc = compose(sacc, o);
+          stop = ostop;
+          sval = oval;
+        }
       }
     }
     if (slot == 0) {
