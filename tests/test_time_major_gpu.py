@@ -191,3 +191,30 @@ def test_time_major_long_row_recipes(rl, name):
             {"out": back(rl.rlcs_eligibility_traces_tm(tm(src["x"]), d, gm, lm))},
             {"out": oracle.eligibility_traces(src["x"], dn, gm, lm)}, TOL)
     rl.check_all_workspaces()
+
+
+@pytest.mark.parametrize("N,T", [(4096, 128), (64, 16384), (256, 16384), (1024, 4096)])
+@pytest.mark.parametrize("shift", [1, 2])
+def test_time_major_inputs_off_16_byte_boundaries(rl, N, T, shift):
+    # Every time-major shape prefetches its chunk's rows into L2 in 16-byte
+    # aligned pieces and skips an input whose base is off that boundary; the
+    # loads themselves take any 4-byte aligned array. Inputs start 4 or 8
+    # bytes into their allocation (the short, 8- and 32-environment shapes;
+    # GAE moves four arrays, discounted returns three).
+    src = rollout(N, T, 14000 + N + T + shift, p_term=0.01)
+
+    def shifted(a):
+        flat = torch.empty(N * T + shift, dtype=torch.float32, device="cuda")
+        view = flat[shift:].view(T, N)
+        view.copy_(tm(a))
+        assert view.data_ptr() % 16 == 4 * shift % 16
+        return view
+
+    r, v, d = shifted(src["rewards"]), shifted(src["values"]), shifted(src["terminateds"])
+    B = torch.from_numpy(src["bootstrap_value"]).cuda()
+    gm, lm = PRM["gamma"], PRM["lambda_"]
+    rn, vn, dn, Bn = src["rewards"], src["values"], src["terminateds"], src["bootstrap_value"]
+    compare("gae", {"out": back(rl.rlcs_gae_tm(r, v, d, gm, lm, B))},
+            {"out": oracle.gae(rn, vn, dn, gm, lm, Bn)}, TOL)
+    compare("discounted_returns", {"out": back(rl.rlcs_discounted_returns_tm(r, d, gm, B))},
+            {"out": oracle.discounted_returns(rn, dn, gm, Bn)}, TOL)
