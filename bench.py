@@ -20,8 +20,9 @@ clocks sampled during the timed region). Everything else goes to the JSON
 file named by --detail: every estimator alone, the step in several schedules
 (seven streams, one stream, one rlcs_run_group call, 2 or 3 groups on their
 own streams), GAE at 64 x 512, the five truncated estimators at 4096 x 128,
-the long-row sweep (256 x {1024, 4096, 16384}, 8 x 131072) and the extra
-entry points (fused GAE + returns, affine scan, compact GAE, time-major).
+the long-row sweep (256 x {1024, 4096, 16384}, 8 x 131072), the extra
+entry points (fused GAE + returns, affine scan, compact GAE, time-major) and
+the time-major entry points at 256 x 4096, 8 x 131072 and 1024 x 4096.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--detail PATH] [--no-long-t]
@@ -729,6 +730,27 @@ def run_ours(args):
         next_rows["clocks"] = sect_clock.stop()
         detail["next_rows"] = next_rows
 
+        # the seven time-major entry points at three more sizes: 8-environment
+        # chunks in one block per SM (256 x 4096) and in one partial wave
+        # (8 x 131072), and 32-environment chunks (1024 x 4096)
+        sect_clock = ClockSampler(gpu_index)
+        sect_clock.start()
+        tm_sizes = {}
+        for (nN, nT, seed) in ((256, 4096, 1004), (8, 131072, 1004), (1024, 4096, 1004)):
+            srcn_tm = {k: (np.ascontiguousarray(v.T) if v.ndim == 2 else v)
+                       for k, v in rollout(nN, nT, seed, w.p_term).items()}
+            res = {}
+            for est in ESTIMATORS:
+                r_ = time_alone(torch, rl, est + "_tm", srcn_tm, dev, stream, prm, l2, nN, nT,
+                                seconds=0.08)
+                r_["frac_of_measured_hbm"] = r_["gbs"] / peak
+                res[est + "_tm"] = r_
+            tm_sizes["%dx%d" % (nN, nT)] = res
+            del srcn_tm
+        rl.check_all_workspaces()
+        tm_sizes["clocks"] = sect_clock.stop()
+        detail["time_major_sizes"] = tm_sizes
+
     e2e = run_e2e(torch, rl, src, dev, stream, prm, order, max(32, min(K, 512)), N, T)
     e2e["value"] *= world
     detail["e2e"] = e2e
@@ -1118,7 +1140,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-long-t", action="store_true",
-                    help="skip the long-row sweep and the extra entry points")
+                    help="skip the long-row sweep, the extra entry points and the time-major sizes")
     ap.add_argument("--schedule", choices=("streams", "serial", "grouped"), default="streams",
                     help="how the headline step issues its seven calls")
     ap.add_argument("--detail", default="bench_detail.json",
