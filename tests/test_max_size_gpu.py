@@ -6,7 +6,8 @@ per float array). Rows are independent, so the oracle checks sampled rows one
 by one: the first and last rows and the rows on either side of the 2^31-
 element offset. Shapes: the warp rows (T = 128), the register tiles (T =
 16388: the last tile of each row is partial, so its later warps' spans lie
-wholly past the row end) and the time-major layout ([T, N], T = 128).
+wholly past the row end) and the time-major layout ([T, N]: T = 128, and 9
+environments over 2^28 steps in 8-environment chunks, checked whole).
 """
 import numpy as np
 import pytest
@@ -100,4 +101,34 @@ def test_time_major_past_two_to_the_31(rl):
                                  cols["terminateds"], GAMMA, LAM, 1.0, 1.0, B)
     compare("vtrace", {"vs": vs[:, envs].T.cpu().numpy(), "pg": pg[:, envs].T.cpu().numpy()},
             {"vs": ovs, "pg": opg}, TOL, " [tm %dx%d]" % (T, N))
+    rl.check_all_workspaces()
+
+
+def test_time_major_few_environments_past_two_to_the_31(rl):
+    # The 8-environment chunks (N <= 256, T >= 2048) with the four-predecessor
+    # look-back window: 9 environments (a full group and a partial one) over
+    # 2^28 steps, so every step from t = 2^31 / 9 on lies past the 2^31-element
+    # offset. Both environments checked whole, GAE (four arrays, 3 blocks/SM)
+    # and discounted returns (three arrays, 4 blocks/SM).
+    N, T = 9, 1 << 28
+    assert N * T > LIMIT
+    dev = torch.device("cuda:0")
+    g = device_rollout(torch, N, T, 9500, 0.001,
+                       ("rewards", "values", "terminateds", "bootstrap_value"), dev,
+                       time_major=True)
+    envs = [0, N - 1]
+    cols = {k: g[k][:, envs].T.cpu().numpy() for k in ("rewards", "values", "terminateds")}
+    B = g["bootstrap_value"][envs].cpu().numpy()
+    out = rl.rlcs_gae_tm(g["rewards"], g["values"], g["terminateds"], GAMMA, LAM,
+                         g["bootstrap_value"])
+    compare("gae", {"out": out[:, envs].T.cpu().numpy()},
+            {"out": oracle.gae(cols["rewards"], cols["values"], cols["terminateds"], GAMMA,
+                               LAM, B)}, TOL, " [tm %dx%d]" % (T, N))
+    del out
+    out = rl.rlcs_discounted_returns_tm(g["rewards"], g["terminateds"], GAMMA,
+                                        g["bootstrap_value"])
+    compare("discounted_returns", {"out": out[:, envs].T.cpu().numpy()},
+            {"out": oracle.discounted_returns(cols["rewards"], cols["terminateds"], GAMMA, B)},
+            TOL, " [tm %dx%d]" % (T, N))
+    del out
     rl.check_all_workspaces()
